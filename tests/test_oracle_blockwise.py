@@ -1,0 +1,88 @@
+"""Pins for the blockwise-FP8 quantization oracle (CPU only): closed-form
+blocks, an exact-rational restatement of the fp32 arithmetic, tile
+structure of the 128x128 weight scales, and segment isolation of the
+column-wise operand."""
+
+import os
+
+import numpy as np
+
+import oracle
+from oracle import scalar
+from oracle.blockwise import transpose_bw_128x128
+import synth
+from conftest import parse_value, read_records
+
+
+def f32_bits(x):
+    return int(np.array([x], dtype=np.float32).view(np.uint32)[0])
+
+
+def test_golden_constant_blocks(golden_dir):
+    recs = read_records(os.path.join(golden_dir, "blockwise_blocks.txt"))
+    assert len(recs) == 3
+    for name, val, s_hex, code_hex in recs:
+        v = parse_value(val)
+        x = synth.f32_to_bf16_bits(np.full((2, 256), v, dtype=np.float32))
+        codes, s = oracle.quantize_bw_1x128(x)
+        assert s.shape == (2, 2)
+        assert all(f32_bits(t) == int(s_hex, 16) for t in s.ravel()), name
+        assert (codes == int(code_hex, 16)).all(), name
+
+
+def test_matches_exact_rational_formulation():
+    rng = np.random.default_rng(21)
+    x = synth.normal_bf16(rng, (6, 256), std=1.0, outlier_frac=0.02)
+    v = synth.bf16_bits_to_f32(x)
+    # a row of tiny values (below the 1e-4 floor) and a row with a zero block
+    x[4] = synth.f32_to_bf16_bits(v[4] * np.float32(1e-7))
+    x[5, :128] = 0
+    codes, s = oracle.quantize_bw_1x128(x)
+    for r in range(x.shape[0]):
+        for b in range(2):
+            blk = [int(t) for t in x[r, 128 * b: 128 * b + 128]]
+            sf, cs = scalar.quantize_block_bw(blk)
+            assert float(sf) == float(s[r, b])
+            assert list(codes[r, 128 * b: 128 * b + 128]) == cs, (r, b)
+
+
+def test_weight_tiles_and_transpose():
+    rng = np.random.default_rng(22)
+    w = synth.normal_bf16(rng, (2, 256, 384))
+    codes, s = oracle.quantize_bw_128x128(w)
+    assert s.shape == (2, 2, 3)
+    # one tile checked against the exact-rational formulation
+    tile = w[1, 128:256, 256:384]
+    sf, cs = scalar.quantize_block_bw([int(t) for t in tile.ravel()])
+    assert float(sf) == float(s[1, 1, 2])
+    assert list(codes[1, 128:256, 256:384].ravel()) == cs
+    # each tile's scale depends only on that tile's amax
+    w2 = w.copy()
+    w2[0, :128, :128] = synth.f32_to_bf16_bits(np.full((128, 128), 1000.0, dtype=np.float32))
+    _, s2 = oracle.quantize_bw_128x128(w2)
+    changed = s2 != s
+    assert changed[0, 0, 0] and changed.sum() == 1
+    ct, st = transpose_bw_128x128(codes, s)
+    assert np.array_equal(ct[1], codes[1].T) and np.array_equal(st[1], s[1].T)
+    deq = oracle.dequantize_bw_128x128(codes, s)
+    assert np.allclose(deq, synth.bf16_bits_to_f32(w), rtol=2 ** -3, atol=float(s.max()) * 2 ** -9)
+
+
+def test_colwise_padded_segments():
+    splits = np.array([200, 0, 1, 128, 55], dtype=np.int32)
+    consts = [2.0 ** 8, 1.0, -2.0 ** -9, 3.0, 2.0 ** 14]
+    C = 128
+    x = synth.f32_to_bf16_bits(np.concatenate(
+        [np.full((m, C), c, dtype=np.float32) for m, c in zip(splits, consts)]))
+    codes, s, poff = oracle.quantize_bw_colwise_padded(x, splits)
+    assert s.shape == (C, int(poff[-1]) // 128)
+    for g, (m, c) in enumerate(zip(splits, consts)):
+        assert poff[g + 1] - poff[g] == -(-m // 128) * 128
+        for b in range(int(poff[g]) // 128, int(poff[g + 1]) // 128):
+            # a constant block's dequant scale is fl32(|c|/448)
+            want = np.float32(np.float32(abs(c)) / np.float32(448.0))
+            assert (s[:, b] == want).all(), (g, b)
+        j0 = int(poff[g])
+        seg = codes[:, j0: j0 + m]
+        assert (seg == (0xFE if c < 0 else 0x7E)).all()
+        assert (codes[:, j0 + m: int(poff[g + 1])] == 0).all()
