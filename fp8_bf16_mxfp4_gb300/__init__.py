@@ -1,0 +1,235 @@
+"""GB300 grouped microscaled (MX) GEMM library -- Python binding.
+
+Argument marshalling only: every computation runs in libmxg.so (CUDA kernels
+for sm_103a) through its C ABI (include/mxg.h).  PyTorch provides device
+memory and the current stream.  There is no CPU fallback: without the built
+library or a GPU these functions raise.
+
+Layouts (row-major, K-major operands):
+  * E2M1 codes: uint8 [rows, cols/2], element 2j in the low nibble.
+  * E4M3 codes: uint8 [rows, cols].
+  * UE8M0 scales: uint8 [rows, cols/32] (one per 32 elements along cols).
+"""
+
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib
+
+__all__ = [
+    "MXOperand", "MXGError", "mx_quantize_rowwise", "mx_quantize_colwise_segment_padded",
+    "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "gemm_workspace_size",
+    "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns",
+    "library_path",
+]
+
+ELEM = {"e2m1": 1, "e4m3": 2}
+PASS = {"fwd": 0, "dgrad": 1, "wgrad": 2}
+_OUT = {torch.bfloat16: 1, torch.float32: 2}
+
+library_path = _lib.LIB_PATH
+
+
+class MXGError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        msg = _lib.load().mxg_status_string(code).decode()
+        super().__init__(f"{what}: {msg} (status {code})")
+
+
+def _ok(code: int, what: str):
+    if code != 0:
+        raise MXGError(code, what)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(dev) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libmxg operates on CUDA tensors only")
+
+
+@dataclass
+class MXOperand:
+    """A quantized K-major operand: codes, UE8M0 scales, element format and
+    logical column count (the contraction length)."""
+    data: torch.Tensor
+    scale: torch.Tensor
+    elem: str
+    cols: int
+
+    @property
+    def rows(self) -> int:
+        return self.data.shape[0]
+
+    def c(self) -> _lib.MxOperandC:
+        return _lib.MxOperandC(self.data.data_ptr(), self.scale.data_ptr(), self.rows, self.cols,
+                               self.data.stride(0), self.scale.stride(0), ELEM[self.elem], 0)
+
+
+_status = {}
+
+
+def status_tensor(device) -> torch.Tensor:
+    """Per-device int32 status word used when the caller passes none."""
+    d = torch.device(device)
+    idx = d.index if d.index is not None else torch.cuda.current_device()
+    if idx not in _status:
+        _status[idx] = torch.zeros(1, dtype=torch.int32, device=f"cuda:{idx}")
+    return _status[idx]
+
+
+def check_status(status: torch.Tensor | None = None, device=None) -> int:
+    """Synchronise, read and clear the device status word; raise on error."""
+    st = status if status is not None else status_tensor(device or torch.cuda.current_device())
+    code = _lib.load().mxg_check_status(_ptr(st), _stream(st.device))
+    _ok(code, "device-side check")
+    return code
+
+
+def set_wait_timeout_ns(ns: int):
+    _lib.load().mxg_set_wait_timeout_ns(int(ns))
+
+
+def mx_padded_rows_capacity(rows: int, G: int, pad: int) -> int:
+    return int(_lib.load().mx_padded_rows_capacity(rows, G, pad))
+
+
+def _codes_cols(elem: str, cols: int) -> int:
+    return cols // 2 if elem == "e2m1" else cols
+
+
+def mx_quantize_rowwise(x: torch.Tensor, elem: str, q: torch.Tensor | None = None,
+                        s: torch.Tensor | None = None) -> MXOperand:
+    """BF16 [rows, cols] -> MX operand quantized along cols."""
+    _need_cuda(x)
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bfloat16 tensor")
+    rows, cols = x.shape
+    if q is None:
+        q = torch.empty((rows, _codes_cols(elem, cols)), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
+    lib = _lib.load()
+    _ok(lib.mx_quantize_rowwise(_ptr(x), rows, cols, x.stride(0), ELEM[elem], _ptr(q), q.stride(0),
+                                _ptr(s), s.stride(0), _stream(x.device)), "mx_quantize_rowwise")
+    return MXOperand(q, s, elem, cols)
+
+
+def mx_quantize_colwise_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, pad_multiple: int,
+                                       elem: str, capacity: int | None = None,
+                                       status: torch.Tensor | None = None, check: bool = False):
+    """BF16 [S, C] with experts' rows concatenated -> (operand [C, capacity],
+    int64 padded offsets [G+1]).  Columns beyond the last expert's padded end
+    are left uninitialised."""
+    _need_cuda(x, m_splits)
+    S, C = x.shape
+    G = m_splits.numel()
+    if capacity is None:
+        capacity = mx_padded_rows_capacity(S, G, pad_multiple)
+    qT = torch.empty((C, _codes_cols(elem, capacity)), dtype=torch.uint8, device=x.device)
+    sT = torch.empty((C, capacity // 32), dtype=torch.uint8, device=x.device)
+    poff = torch.empty(G + 1, dtype=torch.int64, device=x.device)
+    st = status if status is not None else status_tensor(x.device)
+    lib = _lib.load()
+    _ok(lib.mx_quantize_colwise_segment_padded(
+        _ptr(x), S, C, x.stride(0), _ptr(m_splits), G, pad_multiple, ELEM[elem], _ptr(qT),
+        qT.stride(0), _ptr(sT), sT.stride(0), capacity, _ptr(poff), _ptr(st), _stream(x.device)),
+        "mx_quantize_colwise_segment_padded")
+    if check:
+        check_status(st)
+    return MXOperand(qT, sT, elem, capacity), poff
+
+
+def gemm_workspace_size(pass_: str, G: int, S: int, N: int, K: int, pad: int = 32) -> int:
+    return int(_lib.load().mxg_gemm_workspace_size(PASS[pass_], G, S, N, K, pad))
+
+
+def _workspace(nbytes: int, device, ws: torch.Tensor | None):
+    if ws is not None:
+        return ws
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def grouped_gemm_fwd(A: MXOperand, W: MXOperand, m_splits: torch.Tensor, N: int,
+                     out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                     check: bool = False) -> torch.Tensor:
+    """Y[off_g+i, :] = A[off_g+i, :] @ W[g*N:(g+1)*N, :]^T for every expert g."""
+    _need_cuda(A.data, W.data, m_splits)
+    G = m_splits.numel()
+    dev = A.data.device
+    if out is None:
+        out = torch.empty((A.rows, N), dtype=out_dtype, device=dev)
+    need = gemm_workspace_size("fwd", G, A.rows, N, A.cols)
+    ws = _workspace(need, dev, workspace)
+    st = status if status is not None else status_tensor(dev)
+    a, w = A.c(), W.c()
+    _ok(_lib.load().grouped_gemm_fwd(ctypes.byref(a), ctypes.byref(w), _ptr(m_splits), G, N,
+                                     _ptr(out), out.stride(0), _OUT[out.dtype], _ptr(ws),
+                                     ws.numel(), _ptr(st), _stream(dev)), "grouped_gemm_fwd")
+    if check:
+        check_status(st)
+    return out
+
+
+def grouped_gemm_dgrad(dY: MXOperand, Wt: MXOperand, m_splits: torch.Tensor,
+                       out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                       check: bool = False) -> torch.Tensor:
+    """dX[off_g+i, :] = dY[off_g+i, :] @ Wt[:, g*N:(g+1)*N]^T (Wt = W^T quantized along N)."""
+    _need_cuda(dY.data, Wt.data, m_splits)
+    G = m_splits.numel()
+    dev = dY.data.device
+    K = Wt.rows
+    if out is None:
+        out = torch.empty((dY.rows, K), dtype=out_dtype, device=dev)
+    need = gemm_workspace_size("dgrad", G, dY.rows, dY.cols, K)
+    ws = _workspace(need, dev, workspace)
+    st = status if status is not None else status_tensor(dev)
+    a, b = dY.c(), Wt.c()
+    _ok(_lib.load().grouped_gemm_dgrad(ctypes.byref(a), ctypes.byref(b), _ptr(m_splits), G,
+                                       _ptr(out), out.stride(0), _OUT[out.dtype], _ptr(ws),
+                                       ws.numel(), _ptr(st), _stream(dev)), "grouped_gemm_dgrad")
+    if check:
+        check_status(st)
+    return out
+
+
+def grouped_gemm_wgrad(dYt: MXOperand, Xt: MXOperand, m_splits: torch.Tensor, total_rows: int,
+                       pad_multiple: int, out: torch.Tensor | None = None,
+                       out_dtype=torch.float32, accumulate: bool = False,
+                       workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                       check: bool = False) -> torch.Tensor:
+    """dW[g] (+)= dYt[:, seg_g] @ Xt[:, seg_g]^T over expert g's padded token
+    segment; out is [G, N, K]."""
+    _need_cuda(dYt.data, Xt.data, m_splits)
+    G = m_splits.numel()
+    dev = dYt.data.device
+    N, K = dYt.rows, Xt.rows
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate needs an existing out tensor")
+        out = torch.empty((G, N, K), dtype=out_dtype, device=dev)
+    need = gemm_workspace_size("wgrad", G, dYt.cols, N, K, pad_multiple)
+    ws = _workspace(need, dev, workspace)
+    st = status if status is not None else status_tensor(dev)
+    a, b = dYt.c(), Xt.c()
+    _ok(_lib.load().grouped_gemm_wgrad(ctypes.byref(a), ctypes.byref(b), _ptr(m_splits), G,
+                                       total_rows, pad_multiple, _ptr(out), _OUT[out.dtype],
+                                       1 if accumulate else 0, _ptr(ws), ws.numel(), _ptr(st),
+                                       _stream(dev)), "grouped_gemm_wgrad")
+    if check:
+        check_status(st)
+    return out

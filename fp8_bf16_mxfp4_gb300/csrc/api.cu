@@ -1,0 +1,346 @@
+// C-ABI layer of libmxg: argument checks, device checks and dispatch.
+//
+// Host checks never touch the GPU, so the error paths can be exercised on a
+// machine without one.  Device placement is taken from the operands' pointers
+// (not from the calling thread's current device): the review "Check operand
+// device instead of current CUDA device" on ROCm TransformerEngine PR #745.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mxg {
+
+static std::atomic<uint64_t> g_wait_timeout_ns{2000000000ull};
+uint64_t wait_timeout_ns() { return g_wait_timeout_ns.load(std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+struct DevInfo {
+  int checked = 0;  // 0 unknown, 1 ok, -1 unsupported
+  int num_sms = 0;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// All non-null pointers must be device (or managed) memory of one device that
+// is an sm_103 part.  On success *dev and *num_sms describe it.
+mxg_status check_device(std::initializer_list<const void*> ptrs, int* dev, int* num_sms) {
+  int d = -1;
+  for (const void* p : ptrs) {
+    if (p == nullptr) continue;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+      cudaGetLastError();
+      return MXG_ERR_DEVICE;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return MXG_ERR_DEVICE;
+    if (d < 0) d = attr.device;
+    else if (attr.device != d) return MXG_ERR_DEVICE;
+  }
+  if (d < 0 || d >= kMaxDevices) return MXG_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev[d].checked == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) {
+      cudaGetLastError();
+      return MXG_ERR_CUDA;
+    }
+    g_dev[d].checked = (major == 10 && minor == 3) ? 1 : -1;
+    g_dev[d].num_sms = sms;
+  }
+  if (g_dev[d].checked != 1) return MXG_ERR_DEVICE;
+  *dev = d;
+  *num_sms = g_dev[d].num_sms;
+  return MXG_OK;
+}
+
+// Makes `dev` current for the scope of a call and restores the caller's.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+inline mxg_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MXG_OK;
+  cudaGetLastError();
+  return MXG_ERR_CUDA;
+}
+
+inline int64_t code_bytes(int elem, int64_t cols) { return elem == MXG_E2M1 ? cols / 2 : cols; }
+inline bool valid_elem(int32_t e) { return e == MXG_E2M1 || e == MXG_E4M3; }
+
+// Host checks of one MX GEMM operand.  An operand with no elements (rows == 0,
+// or cols == 0 where `allow_no_cols`) may have NULL data and scale pointers.
+mxg_status check_operand(const mxg_mx_operand* op, bool allow_no_cols = false) {
+  if (op == nullptr) return MXG_ERR_NULL;
+  if (!valid_elem(op->elem) || op->reserved != 0) return MXG_ERR_UNSUPPORTED;
+  if (op->rows < 0 || op->cols < 0 || op->cols % 32 != 0) return MXG_ERR_SHAPE;
+  if (op->cols == 0 && !allow_no_cols) return MXG_ERR_SHAPE;
+  if (op->ld < code_bytes(op->elem, op->cols) || op->scale_ld < op->cols / 32) return MXG_ERR_SHAPE;
+  if (op->ld % 16 != 0) return MXG_ERR_ALIGN;
+  if (op->rows == 0 || op->cols == 0) return MXG_OK;
+  if (op->data == nullptr || op->scale == nullptr) return MXG_ERR_NULL;
+  if (!aligned16(op->data)) return MXG_ERR_ALIGN;
+  return MXG_OK;
+}
+
+// `rows` == 0 allows a NULL output.
+mxg_status check_out(const void* out, int64_t rows, int64_t ld_out, int64_t ncols, int32_t dtype) {
+  if (dtype != MXG_OUT_BF16 && dtype != MXG_OUT_F32) return MXG_ERR_UNSUPPORTED;
+  if (ld_out < ncols) return MXG_ERR_SHAPE;
+  const int64_t esz = dtype == MXG_OUT_BF16 ? 2 : 4;
+  if ((ld_out * esz) % 16 != 0) return MXG_ERR_ALIGN;
+  if (rows == 0) return MXG_OK;
+  if (out == nullptr) return MXG_ERR_NULL;
+  if (!aligned16(out)) return MXG_ERR_ALIGN;
+  return MXG_OK;
+}
+
+}  // namespace
+}  // namespace mxg
+
+using namespace mxg;
+
+extern "C" {
+
+int32_t mxg_version(void) { return 100; }
+
+void mxg_set_wait_timeout_ns(uint64_t ns) { g_wait_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed); }
+uint64_t mxg_get_wait_timeout_ns(void) { return wait_timeout_ns(); }
+
+const char* mxg_status_string(mxg_status s) {
+  switch (s) {
+    case MXG_OK: return "ok";
+    case MXG_ERR_NULL: return "a required pointer is NULL";
+    case MXG_ERR_SHAPE: return "sizes inconsistent or not divisible as required";
+    case MXG_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+    case MXG_ERR_SPLITS: return "m_splits has a negative entry or does not sum to the row count";
+    case MXG_ERR_UNSUPPORTED: return "format combination or option not supported";
+    case MXG_ERR_DEVICE: return "pointer not on one sm_103 device";
+    case MXG_ERR_CUDA: return "CUDA runtime error";
+    case MXG_ERR_TIMEOUT: return "a bounded in-kernel wait ran out";
+    case MXG_ERR_WORKSPACE: return "workspace missing or too small";
+    case MXG_ERR_CAPACITY: return "padded rows exceed the output capacity";
+  }
+  return "unknown status";
+}
+
+int64_t mx_padded_rows_capacity(int64_t rows, int32_t G, int32_t pad) {
+  if (rows < 0 || G < 1 || pad < 1) return -1;
+  const int64_t nonempty = rows < G ? rows : (int64_t)G;  // experts that can add padding
+  return ((rows + nonempty * (pad - 1)) / pad) * pad;
+}
+
+mxg_status mxg_check_status(int32_t* d_status, void* stream) {
+  if (d_status == nullptr) return MXG_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, d_status, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(d_status, 0, sizeof(int32_t), st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return MXG_ERR_CUDA;
+  }
+  return static_cast<mxg_status>(v);
+}
+
+mxg_status mx_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                               int32_t elem, void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
+                               void* stream) {
+  if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0) return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < code_bytes(elem, cols) || ld_s < cols / 32) return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % (elem == MXG_E2M1 ? 4 : 8) != 0) return MXG_ERR_ALIGN;
+  if (rows == 0) return MXG_OK;  // nothing to read or write; pointers may be NULL
+  if (x == nullptr || q == nullptr || s == nullptr) return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned(q, elem == MXG_E2M1 ? 4 : 8)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, q, s}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_mx_rowwise(x, rows, cols, ld_x, elem, q, ld_q, s, ld_s,
+                                       static_cast<cudaStream_t>(stream), sms));
+}
+
+mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64_t cols,
+                                              int64_t ld_x, const int32_t* d_m_splits,
+                                              int32_t G, int32_t pad_multiple, int32_t elem,
+                                              void* qT, int64_t ld_q, uint8_t* sT, int64_t ld_s,
+                                              int64_t capacity, int64_t* d_pad_offsets,
+                                              int32_t* d_status, void* stream) {
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  if (pad_multiple <= 0 || pad_multiple % 32 != 0) return MXG_ERR_SHAPE;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0 || capacity < 0 || capacity % 32 != 0)
+    return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < code_bytes(elem, capacity) || ld_s < capacity / 32) return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 16 != 0) return MXG_ERR_ALIGN;
+  // x may be NULL when there are no rows; qT / sT when there is no capacity
+  if ((rows > 0 && x == nullptr) || (capacity > 0 && (qT == nullptr || sT == nullptr)))
+    return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned16(qT) || !aligned(d_pad_offsets, 8)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, d_m_splits, qT, sT, d_pad_offsets, d_status}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_mx_colwise(x, rows, cols, ld_x, d_m_splits, G, pad_multiple, elem, qT,
+                                       ld_q, sT, ld_s, capacity, d_pad_offsets, d_status,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t mxg_gemm_workspace_size(int32_t pass, int32_t G, int64_t S, int64_t N, int64_t K,
+                               int32_t pad_multiple) {
+  if (G < 1 || G > kMaxExperts || S < 0 || N <= 0 || K <= 0) return 0;
+  if (pass < MXG_PASS_FWD || pass > MXG_PASS_WGRAD) return 0;
+  if (pass == MXG_PASS_WGRAD && (pad_multiple <= 0 || pad_multiple % 32 != 0)) return 0;
+  return gemm_workspace_bytes(pass, G, S, N, K, pad_multiple);
+}
+
+mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
+                            const int32_t* d_m_splits, int32_t G, int64_t N, void* out,
+                            int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
+                            int32_t* d_status, void* stream) {
+  mxg_status st;
+  if ((st = check_operand(A)) != MXG_OK || (st = check_operand(W)) != MXG_OK) return st;
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if ((st = check_out(out, A->rows, ld_out, N, out_dtype)) != MXG_OK) return st;
+  if (G < 1 || G > kMaxExperts || N <= 0 || N % 32 != 0) return MXG_ERR_SHAPE;
+  if (W->rows == 0) return MXG_ERR_SHAPE;
+  if (A->cols != W->cols || W->rows != (int64_t)G * N) return MXG_ERR_SHAPE;
+  const bool a8w4 = A->elem == MXG_E4M3 && W->elem == MXG_E2M1;
+  if (A->elem == MXG_E2M1 && W->elem == MXG_E4M3) return MXG_ERR_UNSUPPORTED;
+  if (a8w4) {
+    if (A->cols % 128 != 0) return MXG_ERR_SHAPE;
+    if (!aligned(W->data, 32) || W->ld % 32 != 0) return MXG_ERR_ALIGN;
+  }
+  const size_t need = gemm_workspace_bytes(MXG_PASS_FWD, G, A->rows, N, A->cols, 32);
+  if (ws_bytes < need || (need > 0 && ws == nullptr)) return MXG_ERR_WORKSPACE;
+  if (ws != nullptr && !aligned(ws, 256)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if ((st = check_device({A->data, A->scale, W->data, W->scale, d_m_splits, out, ws, d_status},
+                         &dev, &sms)) != MXG_OK)
+    return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  GemmArgs a{};
+  a.pass = MXG_PASS_FWD;
+  a.G = G;
+  a.a_data = static_cast<const uint8_t*>(A->data); a.a_ld = A->ld;
+  a.a_scale = A->scale; a.a_scale_ld = A->scale_ld;
+  a.a_rows = A->rows; a.a_cols = A->cols; a.a_elem = A->elem;
+  a.b_data = static_cast<const uint8_t*>(W->data); a.b_ld = W->ld;
+  a.b_scale = W->scale; a.b_scale_ld = W->scale_ld;
+  a.b_rows = W->rows; a.b_cols = W->cols; a.b_elem = W->elem;
+  a.splits = d_m_splits;
+  a.total_rows = A->rows;
+  a.N = N; a.K = A->cols;
+  a.pad = 32;
+  a.out = out; a.ld_out = ld_out; a.out_dtype = out_dtype; a.accumulate = 0;
+  a.ws = ws; a.ws_bytes = ws_bytes; a.status = d_status;
+  return launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+mxg_status grouped_gemm_dgrad(const mxg_mx_operand* dY, const mxg_mx_operand* Wt,
+                              const int32_t* d_m_splits, int32_t G, void* out, int64_t ld_out,
+                              int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* d_status,
+                              void* stream) {
+  mxg_status st;
+  if ((st = check_operand(dY)) != MXG_OK || (st = check_operand(Wt)) != MXG_OK) return st;
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  const int64_t N = dY->cols, K = Wt->rows;
+  if (K <= 0 || K % 32 != 0 || Wt->cols != (int64_t)G * N) return MXG_ERR_SHAPE;
+  if ((st = check_out(out, dY->rows, ld_out, K, out_dtype)) != MXG_OK) return st;
+  if (dY->elem != Wt->elem) return MXG_ERR_UNSUPPORTED;  // a8w4 is forward-only
+  const size_t need = gemm_workspace_bytes(MXG_PASS_DGRAD, G, dY->rows, N, K, 32);
+  if (ws_bytes < need || (need > 0 && ws == nullptr)) return MXG_ERR_WORKSPACE;
+  if (ws != nullptr && !aligned(ws, 256)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if ((st = check_device({dY->data, dY->scale, Wt->data, Wt->scale, d_m_splits, out, ws, d_status},
+                         &dev, &sms)) != MXG_OK)
+    return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  GemmArgs a{};
+  a.pass = MXG_PASS_DGRAD;
+  a.G = G;
+  a.a_data = static_cast<const uint8_t*>(dY->data); a.a_ld = dY->ld;
+  a.a_scale = dY->scale; a.a_scale_ld = dY->scale_ld;
+  a.a_rows = dY->rows; a.a_cols = dY->cols; a.a_elem = dY->elem;
+  a.b_data = static_cast<const uint8_t*>(Wt->data); a.b_ld = Wt->ld;
+  a.b_scale = Wt->scale; a.b_scale_ld = Wt->scale_ld;
+  a.b_rows = Wt->rows; a.b_cols = Wt->cols; a.b_elem = Wt->elem;
+  a.splits = d_m_splits;
+  a.total_rows = dY->rows;
+  a.N = N; a.K = K;
+  a.pad = 32;
+  a.out = out; a.ld_out = ld_out; a.out_dtype = out_dtype; a.accumulate = 0;
+  a.ws = ws; a.ws_bytes = ws_bytes; a.status = d_status;
+  return launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+mxg_status grouped_gemm_wgrad(const mxg_mx_operand* dYt, const mxg_mx_operand* Xt,
+                              const int32_t* d_m_splits, int32_t G, int64_t total_rows,
+                              int32_t pad_multiple, void* out, int32_t out_dtype,
+                              int32_t accumulate, void* ws, size_t ws_bytes, int32_t* d_status,
+                              void* stream) {
+  mxg_status st;
+  if ((st = check_operand(dYt, true)) != MXG_OK || (st = check_operand(Xt, true)) != MXG_OK) return st;
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (G < 1 || G > kMaxExperts || total_rows < 0) return MXG_ERR_SHAPE;
+  if (pad_multiple <= 0 || pad_multiple % 32 != 0) return MXG_ERR_SHAPE;
+  const int64_t N = dYt->rows, K = Xt->rows;
+  if (N <= 0 || K <= 0 || N % 32 != 0 || K % 32 != 0 || dYt->cols != Xt->cols) return MXG_ERR_SHAPE;
+  if ((st = check_out(out, 1, K, K, out_dtype)) != MXG_OK) return st;
+  if (accumulate && out_dtype != MXG_OUT_F32) return MXG_ERR_UNSUPPORTED;
+  if (dYt->elem != Xt->elem) return MXG_ERR_UNSUPPORTED;
+  const size_t need = gemm_workspace_bytes(MXG_PASS_WGRAD, G, dYt->cols, N, K, pad_multiple);
+  if (ws_bytes < need || (need > 0 && ws == nullptr)) return MXG_ERR_WORKSPACE;
+  if (ws != nullptr && !aligned(ws, 256)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if ((st = check_device({dYt->data, dYt->scale, Xt->data, Xt->scale, d_m_splits, out, ws, d_status},
+                         &dev, &sms)) != MXG_OK)
+    return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  GemmArgs a{};
+  a.pass = MXG_PASS_WGRAD;
+  a.G = G;
+  a.a_data = static_cast<const uint8_t*>(dYt->data); a.a_ld = dYt->ld;
+  a.a_scale = dYt->scale; a.a_scale_ld = dYt->scale_ld;
+  a.a_rows = dYt->rows; a.a_cols = dYt->cols; a.a_elem = dYt->elem;
+  a.b_data = static_cast<const uint8_t*>(Xt->data); a.b_ld = Xt->ld;
+  a.b_scale = Xt->scale; a.b_scale_ld = Xt->scale_ld;
+  a.b_rows = Xt->rows; a.b_cols = Xt->cols; a.b_elem = Xt->elem;
+  a.splits = d_m_splits;
+  a.total_rows = total_rows;
+  a.N = N; a.K = K;
+  a.pad = pad_multiple;
+  a.out = out; a.ld_out = K; a.out_dtype = out_dtype; a.accumulate = accumulate ? 1 : 0;
+  a.ws = ws; a.ws_bytes = ws_bytes; a.status = d_status;
+  return launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+}  // extern "C"

@@ -1,0 +1,772 @@
+// Single-launch grouped MX GEMM for sm_103a (tcgen05 block-scaled MMA).
+//
+// The three passes of an MoE expert layer ("Triton mxfp4 (and a8w4) grouped
+// GEMM kernel", ROCm TransformerEngine PR #723; per-pass shapes from
+// "Integrate MXFP4 hipblaslt GEMM support", PR #697) are one problem: for each
+// expert g, C_g[M_g x N_g] = A_g[M_g x Kc_g] * B_g[N_g x Kc_g]^T with both
+// operands K-major and MX-quantized along Kc:
+//
+//   pass   A (rows)        B (rows)         contraction           output rows
+//   fwd    X  rows off_g   W  rows g*N      K, from 0             off_g + i
+//   dgrad  dY rows off_g   Wt rows 0..K-1   N, B from col g*N     off_g + i
+//   wgrad  dYt rows 0..N   Xt rows 0..K     p_g, from col poff_g  g*N + n
+//
+// Launch sequence on the caller's stream (all device-side, no host sync):
+//   1. plan kernel (1 CTA): validates m_splits (>= 0, sum == rows, padded
+//      total <= capacity) and writes per-expert prefix tables to the
+//      workspace.  A failure is reported in *status and disables 2 and 3.
+//   2. scale-pack kernel: UE8M0 bytes from the plain [rows, cols/32] layout
+//      into 512-byte chunks (128 rows x 4 blocks, the order tcgen05.cp
+//      32x128b.warpx4 expects: byte (r%32)*16 + (r/32)*4 + block), one chunk
+//      per (row tile, 128-element k chunk) with every expert's rows (or k
+//      range) starting on a fresh chunk -- the "scale packing" step that the
+//      HipKittens grouped MXFP8 kernel (PR #661) also performs.
+//   3. the persistent GEMM kernel, one CTA per SM, 192 threads:
+//        warp 0    TMA producer: A/B data tiles (128-byte swizzle) and scale
+//                  chunks into a 4-stage shared-memory ring (mbarriers);
+//        warp 1    TMEM owner and MMA issuer (one thread): tcgen05.cp of the
+//                  stage's scales into TMEM, 4 tcgen05.mma per stage
+//                  (kind::mxf4 for MXFP4, kind::mxf8f6f4 for MXFP8 / a8w4)
+//                  accumulating a 128x256 fp32 tile in TMEM;
+//        warps 2-5 epilogue: tcgen05.ld, fp32 -> BF16/FP32 (optionally +=),
+//                  row/column-masked stores of the expert's valid region.
+//      Tiles (expert, m-tile, n-tile) are enumerated expert-major, n fastest,
+//      and strided over the CTAs.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace mxg {
+namespace {
+
+constexpr int BM = 128;           // tile rows (TMEM lanes)
+constexpr int BN = 256;           // tile columns (TMEM fp32 columns)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kATileBytes = BM * 128;  // 128 bytes of K per row per stage
+constexpr int kBTileBytes = BN * 128;
+constexpr int kChunkBytes = 512;       // 128 rows x 4 scale bytes
+constexpr int kTmemCols = 512;
+constexpr int kSfTmemCol0 = 256;       // scale staging columns start after the accumulator
+
+enum Kind { KIND_MXF4 = 0, KIND_A8W4 = 1, KIND_MXF8 = 2 };
+
+template <int kKind>
+struct KindCfg {
+  static constexpr int kMmaK = kKind == KIND_MXF4 ? 64 : 32;      // elements per MMA
+  static constexpr int kStageK = kKind == KIND_MXF4 ? 256 : 128;  // elements per stage
+  static constexpr int kKPS = kStageK / 128;                      // scale k-chunks per stage
+  static constexpr int kSfBytes = kKPS * kChunkBytes * 3;         // A: 1 row chunk, B: 2
+  static constexpr int kSfCols = kKPS * 12;                       // TMEM columns per stage
+  // instruction descriptor element types (A, B)
+  static constexpr uint32_t kAType = kKind == KIND_MXF4 ? 1u : 0u;  // mxf4: E2M1=1; f8f6f4: E4M3=0
+  static constexpr uint32_t kBType = kKind == KIND_MXF4 ? 1u : (kKind == KIND_A8W4 ? 5u : 0u);
+};
+
+// Offsets of the per-expert tables inside the plan (int32 arrays of G+1).
+struct PlanView {
+  int32_t* hdr;  // [0] valid, [1] total tiles
+  int32_t* off;  // prefix of m_g
+  int32_t* rt;   // prefix of ceil(m_g/128)
+  int32_t* poff; // prefix of p_g = ceil(m_g/pad)*pad
+  int32_t* kc;   // prefix of ceil(p_g/128)
+  int32_t* tiles;// prefix of tiles per expert
+};
+
+constexpr int kPlanHdrInts = 16;
+inline size_t plan_bytes(int G) {
+  size_t b = (kPlanHdrInts + 5 * (size_t)(G + 1)) * sizeof(int32_t);
+  return (b + 255) & ~(size_t)255;
+}
+__host__ __device__ inline PlanView plan_view(void* ws, int G) {
+  PlanView v;
+  int32_t* p = static_cast<int32_t*>(ws);
+  v.hdr = p;
+  v.off = p + kPlanHdrInts;
+  v.rt = v.off + (G + 1);
+  v.poff = v.rt + (G + 1);
+  v.kc = v.poff + (G + 1);
+  v.tiles = v.kc + (G + 1);
+  return v;
+}
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+MXG_DEVINL int cdiv_d(int a, int b) { return (a + b - 1) / b; }
+
+struct Params {
+  int pass, G, accumulate, out_dtype;
+  int64_t S, N, K, cap;
+  int pad;
+  int rtA_fixed;  // A row tiles when fixed (wgrad: ceil(N/128))
+  int rtB;        // B row tiles total (fwd: G*ceil(N/128); dgrad/wgrad: ceil(K/128))
+  int kcA_fixed;  // A k-chunks when fixed (fwd: ceil(K/128); dgrad: ceil(N/128))
+  int kcB_fixed;  // B k-chunks when fixed (fwd: ceil(K/128); dgrad: G*ceil(N/128))
+  const int32_t* plan;
+  const uint8_t* packA;
+  const uint8_t* packB;
+  void* out;
+  int64_t ld_out;
+  int32_t* status;
+  uint64_t timeout_ns;  // every wait of the main loops
+  uint64_t drain_ns;    // teardown waits for copies / MMAs still in flight (>= 200 ms)
+  uint32_t idesc;
+};
+
+// Per-expert geometry of one pass (see the table at the top of the file).
+struct Geo {
+  int64_t a_row0, b_row0, a_k0, b_k0, out_row0;
+  int M, Nn, Kc;
+  int a_rt0, b_rt0, a_kc0, b_kc0;
+};
+
+MXG_DEVINL Geo group_geo(const Params& p, const int32_t* off, const int32_t* rt,
+                         const int32_t* poff, const int32_t* kc, int g) {
+  Geo e;
+  const int nrt = (int)((p.N + 127) / 128);
+  if (p.pass == MXG_PASS_FWD) {
+    e.a_row0 = off[g]; e.b_row0 = (int64_t)g * p.N; e.a_k0 = 0; e.b_k0 = 0;
+    e.M = off[g + 1] - off[g]; e.Nn = (int)p.N; e.Kc = (int)p.K;
+    e.a_rt0 = rt[g]; e.b_rt0 = g * nrt; e.a_kc0 = 0; e.b_kc0 = 0;
+    e.out_row0 = off[g];
+  } else if (p.pass == MXG_PASS_DGRAD) {
+    e.a_row0 = off[g]; e.b_row0 = 0; e.a_k0 = 0; e.b_k0 = (int64_t)g * p.N;
+    e.M = off[g + 1] - off[g]; e.Nn = (int)p.K; e.Kc = (int)p.N;
+    e.a_rt0 = rt[g]; e.b_rt0 = 0; e.a_kc0 = 0; e.b_kc0 = g * nrt;
+    e.out_row0 = off[g];
+  } else {
+    e.a_row0 = 0; e.b_row0 = 0; e.a_k0 = poff[g]; e.b_k0 = poff[g];
+    e.M = (int)p.N; e.Nn = (int)p.K; e.Kc = poff[g + 1] - poff[g];
+    e.a_rt0 = 0; e.b_rt0 = 0; e.a_kc0 = kc[g]; e.b_kc0 = kc[g];
+    e.out_row0 = (int64_t)g * p.N;
+  }
+  return e;
+}
+
+// ---------------------------------------------------------------------------
+// 1. Plan: split validation + prefix tables (one CTA of 256 threads, two
+//    experts per thread).
+// ---------------------------------------------------------------------------
+constexpr int kPlanThreads = 256;
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __restrict__ splits,
+                                                            Params p, int32_t* plan_ws) {
+  PlanView pv = plan_view(plan_ws, p.G);
+  __shared__ int64_t wsum[8][5];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int G = p.G;
+  const int nt_n = p.pass == MXG_PASS_FWD ? (int)cdiv_d((int)p.N, BN) : (int)cdiv_d((int)p.K, BN);
+  const int wg_tiles = (int)(cdiv_d((int)p.N, BM) * cdiv_d((int)p.K, BN));
+  int64_t v[2][5];
+  bool neg = false;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int g = 2 * tid + i;
+    const int64_t m = g < G ? (int64_t)splits[g] : 0;
+    neg |= m < 0;
+    const int64_t mm = m > 0 ? m : 0;
+    const int64_t pg = p.pass == MXG_PASS_WGRAD ? ((mm + p.pad - 1) / p.pad) * p.pad : 0;
+    v[i][0] = m;
+    v[i][1] = (mm + BM - 1) / BM;
+    v[i][2] = pg;
+    v[i][3] = (pg + 127) / 128;
+    if (g >= G) v[i][4] = 0;
+    else if (p.pass == MXG_PASS_WGRAD) v[i][4] = (pg > 0 || !p.accumulate) ? wg_tiles : 0;
+    else v[i][4] = v[i][1] * nt_n;
+  }
+  int64_t incl[5];
+#pragma unroll
+  for (int q = 0; q < 5; ++q) {
+    int64_t s = v[0][q] + v[1][q];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t o = __shfl_up_sync(0xffffffffu, s, d);
+      if (lane >= d) s += o;
+    }
+    incl[q] = s;
+    if (lane == 31) wsum[wid][q] = s;
+  }
+  const int any_neg = __syncthreads_or(neg);
+  int32_t* tabs[5] = {pv.off, pv.rt, pv.poff, pv.kc, pv.tiles};
+  __shared__ int64_t totals[5];
+#pragma unroll
+  for (int q = 0; q < 5; ++q) {
+    int64_t base = 0;
+    for (int w = 0; w < wid; ++w) base += wsum[w][q];
+    const int64_t ex = base + incl[q] - (v[0][q] + v[1][q]);
+    if (2 * tid <= G) tabs[q][2 * tid] = (int32_t)ex;
+    if (2 * tid + 1 <= G) tabs[q][2 * tid + 1] = (int32_t)(ex + v[0][q]);
+    if (tid == kPlanThreads - 1) totals[q] = base + incl[q];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int bad = 0;
+    if (any_neg || totals[0] != p.S) bad = MXG_ERR_SPLITS;
+    else if (p.pass == MXG_PASS_WGRAD && totals[2] > p.cap) bad = MXG_ERR_CAPACITY;
+    else if (totals[4] > 0x7FFFFFFF) bad = MXG_ERR_SHAPE;
+    if (bad) report(p.status, bad);
+    pv.hdr[0] = bad ? 0 : 1;
+    pv.hdr[1] = bad ? 0 : (int32_t)totals[4];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. Scale packing.  blockIdx.y selects the operand (0 = A, 1 = B).
+// ---------------------------------------------------------------------------
+struct PackSrc {
+  const uint8_t* src;
+  int64_t ld;
+  uint8_t* dst;
+};
+
+MXG_DEVINL int find_prefix(const int32_t* pre, int G, int x) {  // last g with pre[g] <= x
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, PackSrc sb) {
+  const int32_t* plan = p.plan;
+  const PlanView pv = plan_view(const_cast<int32_t*>(plan), p.G);
+  if (pv.hdr[0] == 0) return;
+  const bool isA = blockIdx.y == 0;
+  const PackSrc ps = isA ? sa : sb;
+  const int G = p.G;
+  const int nrt = (int)((p.N + 127) / 128);
+  // totals for this operand
+  int RT, KC;
+  if (p.pass == MXG_PASS_FWD) {
+    RT = isA ? pv.rt[G] : p.rtB;
+    KC = p.kcA_fixed;
+  } else if (p.pass == MXG_PASS_DGRAD) {
+    RT = isA ? pv.rt[G] : p.rtB;
+    KC = isA ? p.kcA_fixed : p.kcB_fixed;
+  } else {
+    RT = isA ? p.rtA_fixed : p.rtB;
+    KC = pv.kc[G];
+  }
+  const int64_t total = (int64_t)RT * KC;
+  const int r = threadIdx.x;
+  for (int64_t id = blockIdx.x; id < total; id += gridDim.x) {
+    const int kcg = (int)(id / RT), rtg = (int)(id % RT);
+    int g, t, c;
+    int64_t row0, k0;
+    int R, KB;
+    if (p.pass == MXG_PASS_WGRAD || (p.pass == MXG_PASS_DGRAD && !isA)) {
+      // rows shared, contraction segmented per expert
+      if (p.pass == MXG_PASS_WGRAD) {
+        g = find_prefix(pv.kc, G, kcg);
+        c = kcg - pv.kc[g];
+        k0 = pv.poff[g];
+        KB = (pv.poff[g + 1] - pv.poff[g]) / 32;
+      } else {
+        g = kcg / nrt;
+        c = kcg - g * nrt;
+        k0 = (int64_t)g * p.N;
+        KB = (int)(p.N / 32);
+      }
+      t = rtg;
+      row0 = 0;
+      R = (int)(isA ? p.N : p.K);
+    } else {
+      // rows segmented per expert, contraction shared
+      if (isA) {
+        g = find_prefix(pv.rt, G, rtg);
+        t = rtg - pv.rt[g];
+        row0 = pv.off[g];
+        R = pv.off[g + 1] - pv.off[g];
+      } else {  // fwd B: G blocks of N rows
+        g = rtg / nrt;
+        t = rtg - g * nrt;
+        row0 = (int64_t)g * p.N;
+        R = (int)p.N;
+      }
+      c = kcg;
+      k0 = 0;
+      KB = (int)((p.pass == MXG_PASS_FWD ? p.K : p.N) / 32);
+    }
+    uint32_t w = 0;
+    const int rr = t * 128 + r;
+    if (rr < R) {
+      const uint8_t* srow = ps.src + (row0 + rr) * ps.ld + (k0 >> 5);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int kb = c * 4 + j;
+        if (kb < KB) w |= (uint32_t)__ldg(srow + kb) << (8 * j);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(ps.dst + id * kChunkBytes + (r & 31) * 16 + (r >> 5) * 4) = w;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. The GEMM kernel.
+// ---------------------------------------------------------------------------
+template <int kKind>
+struct Smem {
+  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kDataBytes = kStages * kStageBytes;
+  static constexpr int kSfOff = kDataBytes;
+  static constexpr int kBarOff = kSfOff + kStages * KindCfg<kKind>::kSfBytes;
+  static constexpr int kNumBars = 2 * kStages + 3;  // full, empty, tmem_full, tmem_empty, drain
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem addr, abort flag
+  static constexpr int kTabOff = kMiscOff + 16;
+  static constexpr int kTabBytes = 5 * (kMaxExperts + 1) * 4;
+  static constexpr int kTotal = kTabOff + kTabBytes + 1024;  // + alignment slack
+};
+
+MXG_DEVINL void store_row_chunk(const Params& p, int64_t row, int64_t col, const uint32_t* r) {
+  if (p.out_dtype == MXG_OUT_BF16) {
+    uint32_t h[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+      h[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * p.ld_out + col);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+  } else {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.ld_out + col);
+    if (p.accumulate) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float4 o = dst[i];
+        o.x += __uint_as_float(r[4 * i]);
+        o.y += __uint_as_float(r[4 * i + 1]);
+        o.z += __uint_as_float(r[4 * i + 2]);
+        o.w += __uint_as_float(r[4 * i + 3]);
+        dst[i] = o;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+    }
+  }
+}
+
+template <int kKind>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const Params p) {
+  using Cfg = KindCfg<kKind>;
+  using L = Smem<kKind>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.G;
+
+  const PlanView pv = plan_view(const_cast<int32_t*>(p.plan), G);
+  if (pv.hdr[0] == 0) return;  // invalid splits: nothing is written
+  const int total_tiles = pv.hdr[1];
+  if ((int)blockIdx.x >= total_tiles) return;
+
+  // per-expert tables into shared memory
+  int32_t* t_off = reinterpret_cast<int32_t*>(smem + L::kTabOff);
+  int32_t* t_rt = t_off + (kMaxExperts + 1);
+  int32_t* t_poff = t_rt + (kMaxExperts + 1);
+  int32_t* t_kc = t_poff + (kMaxExperts + 1);
+  int32_t* t_tiles = t_kc + (kMaxExperts + 1);
+  for (int i = threadIdx.x; i <= G; i += kThreads) {
+    t_off[i] = pv.off[i];
+    t_rt[i] = pv.rt[i];
+    t_poff[i] = pv.poff[i];
+    t_kc[i] = pv.kc[i];
+    t_tiles[i] = pv.tiles[i];
+  }
+  const uint32_t bar0 = sbase + L::kBarOff;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t tmem_full = bar0 + 8u * (2 * kStages);
+  const uint32_t tmem_empty = tmem_full + 8;
+  const uint32_t drain_bar = tmem_full + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    ptx::mbar_init(tmem_full, 1);
+    ptx::mbar_init(tmem_empty, 4);
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto locate = [&](int tile, int& g, int& mt, int& nt, Geo& e) {
+    g = find_prefix(t_tiles, G, tile);
+    e = group_geo(p, t_off, t_rt, t_poff, t_kc, g);
+    const int local = tile - t_tiles[g];
+    const int ntn = cdiv_d(e.Nn, BN);
+    mt = local / ntn;
+    nt = local - mt * ntn;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed_phase[kStages];
+      bool armed[kStages];
+      for (int s = 0; s < kStages; ++s) { armed[s] = false; armed_phase[s] = 0; }
+      const int rtA = p.pass == MXG_PASS_WGRAD ? p.rtA_fixed : pv.rt[G];
+      const int rtB = p.rtB;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        int g, mt, nt;
+        Geo e;
+        locate(tile, g, mt, nt, e);
+        const int nk = cdiv_d(e.Kc, Cfg::kStageK);
+        const int nb_rows = min(2, cdiv_d(e.Nn - nt * BN, 128));
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          const int kc_valid = min(Cfg::kKPS, cdiv_d(e.Kc - kb * Cfg::kStageK, 128));
+          // The 4-bit-unpacking load of the a8w4 weight tile counts the packed
+          // source bytes (64 per row), although it fills 128 bytes per row.
+          constexpr uint32_t kBTx = kKind == KIND_A8W4 ? kBTileBytes / 2 : kBTileBytes;
+          const uint32_t bytes = kATileBytes + kBTx + kc_valid * kChunkBytes * (1 + nb_rows);
+          const uint32_t fb = full_bar(stage);
+          ptx::mbar_arrive_expect_tx(fb, bytes);
+          armed[stage] = true;
+          armed_phase[stage] = phase;
+          const uint32_t sA = sbase + stage * L::kStageBytes;
+          const uint32_t sB = sA + kATileBytes;
+          const int64_t ka = e.a_k0 + (int64_t)kb * Cfg::kStageK;
+          const int64_t kbk = e.b_k0 + (int64_t)kb * Cfg::kStageK;
+          const int xa = kKind == KIND_MXF4 ? (int)(ka >> 1) : (int)ka;
+          const int xb = kKind == KIND_MXF4 ? (int)(kbk >> 1) : (int)kbk;
+          ptx::tma_load_2d(sA, &tmA, xa, (int)(e.a_row0 + (int64_t)mt * BM), fb);
+          ptx::tma_load_2d(sB, &tmB, xb, (int)(e.b_row0 + (int64_t)nt * BN), fb);
+          const uint32_t sf = sbase + L::kSfOff + stage * Cfg::kSfBytes;
+          for (int c = 0; c < kc_valid; ++c) {
+            const int kcA = e.a_kc0 + kb * Cfg::kKPS + c;
+            const int kcB = e.b_kc0 + kb * Cfg::kKPS + c;
+            const uint8_t* srcA = p.packA + ((int64_t)kcA * rtA + e.a_rt0 + mt) * kChunkBytes;
+            const uint8_t* srcB = p.packB + ((int64_t)kcB * rtB + e.b_rt0 + 2 * nt) * kChunkBytes;
+            ptx::bulk_load(sf + c * kChunkBytes, srcA, kChunkBytes, fb);
+            ptx::bulk_load(sf + Cfg::kKPS * kChunkBytes + c * 2 * kChunkBytes, srcB,
+                           nb_rows * kChunkBytes, fb);
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // do not leave copies in flight: wait (bounded) for every armed stage
+      for (int s = 0; s < kStages; ++s)
+        if (armed[s]) {
+          volatile int no_abort = 0;
+          ptx::mbar_wait(full_bar(s), armed_phase[s], &no_abort, p.status, p.drain_ns);
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        int g, mt, nt;
+        Geo e;
+        locate(tile, g, mt, nt, e);
+        if (!ptx::mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const int nk = cdiv_d(e.Kc, Cfg::kStageK);
+        const int nb_rows = min(2, cdiv_d(e.Nn - nt * BN, 128));
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const int rem = e.Kc - kb * Cfg::kStageK;
+          const int kc_valid = min(Cfg::kKPS, cdiv_d(rem, 128));
+          const int steps = min(4, cdiv_d(rem, Cfg::kMmaK));
+          const uint32_t sA = sbase + stage * L::kStageBytes;
+          const uint32_t sB = sA + kATileBytes;
+          const uint32_t sf = sbase + L::kSfOff + stage * Cfg::kSfBytes;
+          const uint32_t tsf = tmem + kSfTmemCol0 + stage * Cfg::kSfCols;  // A: kKPS*4 cols, then B
+          for (int c = 0; c < kc_valid; ++c) {
+            ptx::tc_cp_32x128b_warpx4(tsf + 4 * c, ptx::smem_desc(sf + c * kChunkBytes, 0, 128, 0));
+            for (int rr = 0; rr < nb_rows; ++rr)
+              ptx::tc_cp_32x128b_warpx4(
+                  tsf + Cfg::kKPS * 4 + 8 * c + 4 * rr,
+                  ptx::smem_desc(sf + Cfg::kKPS * kChunkBytes + (2 * c + rr) * kChunkBytes, 0, 128, 0));
+          }
+          const uint64_t adesc0 = ptx::smem_desc(sA, 16, 1024, 2);
+          const uint64_t bdesc0 = ptx::smem_desc(sB, 16, 1024, 2);
+          for (int j = 0; j < steps; ++j) {
+            const int kel = j * Cfg::kMmaK;  // element offset inside the stage
+            const int c = kel >> 7;
+            const uint32_t sfid = (uint32_t)((kel & 127) >> 5);
+            const uint32_t idesc = p.idesc | (sfid << 4) | (sfid << 29);
+            const uint64_t adv = (uint64_t)((j * 32) >> 4);  // 32 bytes of K per MMA
+            const uint32_t sfa = tsf + 4 * c;
+            const uint32_t sfb = tsf + Cfg::kKPS * 4 + 8 * c;
+            if constexpr (kKind == KIND_MXF4)
+              ptx::mma_mxf4(tmem, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+            else
+              ptx::mma_mxf8f6f4(tmem, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+          }
+          issued = true;
+          ptx::tc_commit(empty_bar(stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        ptx::tc_commit(tmem_full);
+        acc_phase ^= 1u;
+      }
+      if (issued) {  // every MMA has retired before TMEM is released
+        ptx::tc_commit(drain_bar);
+        volatile int no_abort = 0;
+        ptx::mbar_wait(drain_bar, 0, &no_abort, p.status, p.drain_ns);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int g, mt, nt;
+      Geo e;
+      locate(tile, g, mt, nt, e);
+      if (!ptx::mbar_wait(tmem_full, acc_phase, abort_flag, p.status, p.timeout_ns)) break;
+      ptx::tc_fence_after();
+      const int row = mt * BM + quarter * 32 + lane;
+      const bool row_ok = row < e.M;
+      const int64_t orow = e.out_row0 + row;
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col = nt * BN + c * 32;
+        if (col >= e.Nn) break;  // warp-uniform
+        uint32_t r[32];
+        if (e.Kc > 0) {
+          __syncwarp();
+          ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(c * 32), r);
+          ptx::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0;
+          if (p.accumulate) continue;  // empty expert, accumulating: leave untouched
+        }
+        if (row_ok) store_row_chunk(p, orow, col, r);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tmem_empty);
+      acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2-D K-major operand map: inner extent `inner` (in elements of `dt`), `rows`
+// rows at `ld_bytes`; box = `box_inner` x `box_rows`; 128-byte swizzle.
+bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int64_t inner,
+               int64_t rows, int64_t ld_bytes, int box_inner, int box_rows) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)ld_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct PackSizes {
+  int64_t rtA, kcA, rtB, kcB;  // upper bounds (chunks)
+};
+
+PackSizes pack_sizes(int pass, int G, int64_t S, int64_t N, int64_t K, int pad) {
+  PackSizes s;
+  const int64_t rt_rows = (S + (int64_t)G * (BM - 1)) / BM;  // >= sum ceil(m_g/128)
+  if (pass == MXG_PASS_FWD) {
+    s.rtA = rt_rows; s.kcA = cdiv(K, 128);
+    s.rtB = G * cdiv(N, 128); s.kcB = cdiv(K, 128);
+  } else if (pass == MXG_PASS_DGRAD) {
+    s.rtA = rt_rows; s.kcA = cdiv(N, 128);
+    s.rtB = cdiv(K, 128); s.kcB = G * cdiv(N, 128);
+  } else {  // S = column capacity of the padded operands
+    const int64_t kc = S / 128 + G;  // >= sum ceil(p_g/128) whenever sum p_g <= S
+    s.rtA = cdiv(N, 128); s.kcA = kc;
+    s.rtB = cdiv(K, 128); s.kcB = kc;
+  }
+  (void)pad;
+  return s;
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int pass, int G, int64_t S, int64_t N, int64_t K, int pad) {
+  const PackSizes s = pack_sizes(pass, G, S, N, K, pad);
+  return plan_bytes(G) + align256((size_t)(s.rtA * s.kcA) * kChunkBytes) +
+         align256((size_t)(s.rtB * s.kcB) * kChunkBytes) + 1024;
+}
+
+mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_sms) {
+  int kind;
+  if (a.a_elem == MXG_E2M1 && a.b_elem == MXG_E2M1) kind = KIND_MXF4;
+  else if (a.a_elem == MXG_E4M3 && a.b_elem == MXG_E2M1) kind = KIND_A8W4;
+  else if (a.a_elem == MXG_E4M3 && a.b_elem == MXG_E4M3) kind = KIND_MXF8;
+  else return MXG_ERR_UNSUPPORTED;
+  if (a.total_rows > 0x7FFFFFFF || a.N > 0x7FFFFFFF || a.K > 0x7FFFFFFF) return MXG_ERR_SHAPE;
+
+  const int64_t S = a.pass == MXG_PASS_WGRAD ? a.a_cols : a.total_rows;
+  const PackSizes ps = pack_sizes(a.pass, a.G, S, a.N, a.K, a.pad);
+  uint8_t* ws = static_cast<uint8_t*>(a.ws);
+  uint8_t* packA = ws + plan_bytes(a.G);
+  uint8_t* packB = packA + align256((size_t)(ps.rtA * ps.kcA) * kChunkBytes);
+
+  Params p{};
+  p.pass = a.pass;
+  p.G = a.G;
+  p.accumulate = a.accumulate;
+  p.out_dtype = a.out_dtype;
+  p.S = a.total_rows;
+  p.N = a.N;
+  p.K = a.K;
+  p.cap = a.a_cols;
+  p.pad = a.pad;
+  p.rtA_fixed = (int)cdiv(a.N, 128);
+  p.rtB = (int)ps.rtB;
+  p.kcA_fixed = (int)(a.pass == MXG_PASS_FWD ? cdiv(a.K, 128) : cdiv(a.N, 128));
+  p.kcB_fixed = (int)(a.pass == MXG_PASS_FWD ? cdiv(a.K, 128) : a.G * cdiv(a.N, 128));
+  p.plan = reinterpret_cast<const int32_t*>(ws);
+  p.packA = packA;
+  p.packB = packB;
+  p.out = a.out;
+  p.ld_out = a.ld_out;
+  p.status = a.status;
+  p.timeout_ns = wait_timeout_ns();
+  p.drain_ns = std::max<uint64_t>(p.timeout_ns, 200000000ull);
+
+  // instruction descriptor: dense, K-major A and B, UE8M0 scales, M=128, N=256
+  uint32_t at = kind == KIND_MXF4 ? 1u : 0u;
+  uint32_t bt = kind == KIND_MXF4 ? 1u : (kind == KIND_A8W4 ? 5u : 0u);
+  p.idesc = (at << 7) | (bt << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+            ((uint32_t)(BM >> 4) << 24);
+
+  // 1. plan
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.splits, p, reinterpret_cast<int32_t*>(ws));
+  if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
+
+  // An empty forward / dgrad batch needs only the split validation.
+  if (a.pass != MXG_PASS_WGRAD && a.total_rows == 0) return MXG_OK;
+
+  // 2. scale packing (both operands in one launch)
+  PackSrc sa{a.a_scale, a.a_scale_ld, packA};
+  PackSrc sb{a.b_scale, a.b_scale_ld, packB};
+  const int64_t chunks = std::max(ps.rtA * ps.kcA, ps.rtB * ps.kcB);
+  int64_t gx = std::min<int64_t>(chunks, (int64_t)num_sms * 16);
+  if (gx < 1) gx = 1;
+  pack_scales_kernel<<<dim3((unsigned)gx, 2), 128, 0, stream>>>(p, sa, sb);
+  if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
+
+  // 3. tensor maps + GEMM
+  CUtensorMap tmA, tmB;
+  bool ok;
+  if (a.a_cols == 0) {
+    // wgrad with zero capacity: every expert is empty and no tile loads data;
+    // the maps only need to be well formed (over the workspace).
+    ok = make_tmap(&tmA, ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, 16, 1, 16, 128, BM) &&
+         make_tmap(&tmB, ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, 16, 1, 16, 128, BN);
+  } else if (kind == KIND_MXF4) {
+    ok = make_tmap(&tmA, a.a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_cols / 2, a.a_rows, a.a_ld, 128, BM) &&
+         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_cols / 2, a.b_rows, a.b_ld, 128, BN);
+  } else if (kind == KIND_A8W4) {
+    ok = make_tmap(&tmA, a.a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_cols, a.a_rows, a.a_ld, 128, BM) &&
+         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.b_cols, a.b_rows, a.b_ld, 128, BN);
+  } else {
+    ok = make_tmap(&tmA, a.a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_cols, a.a_rows, a.a_ld, 128, BM) &&
+         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_cols, a.b_rows, a.b_ld, 128, BN);
+  }
+  if (!ok) return MXG_ERR_CUDA;
+
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static std::mutex mu;
+  static bool attr_set[64][3] = {};
+  const void* fn;
+  int smem;
+  switch (kind) {
+    case KIND_MXF4: fn = (const void*)grouped_mx_gemm_kernel<KIND_MXF4>; smem = Smem<KIND_MXF4>::kTotal; break;
+    case KIND_A8W4: fn = (const void*)grouped_mx_gemm_kernel<KIND_A8W4>; smem = Smem<KIND_A8W4>::kTotal; break;
+    default: fn = (const void*)grouped_mx_gemm_kernel<KIND_MXF8>; smem = Smem<KIND_MXF8>::kTotal; break;
+  }
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 64 && !attr_set[dev][kind]) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return MXG_ERR_CUDA;
+      }
+      attr_set[dev][kind] = true;
+    }
+  }
+  const dim3 grid((unsigned)num_sms), block(kThreads);
+  switch (kind) {
+    case KIND_MXF4: grouped_mx_gemm_kernel<KIND_MXF4><<<grid, block, smem, stream>>>(tmA, tmB, p); break;
+    case KIND_A8W4: grouped_mx_gemm_kernel<KIND_A8W4><<<grid, block, smem, stream>>>(tmA, tmB, p); break;
+    default: grouped_mx_gemm_kernel<KIND_MXF8><<<grid, block, smem, stream>>>(tmA, tmB, p); break;
+  }
+  if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
+  return MXG_OK;
+}
+
+}  // namespace mxg

@@ -1,0 +1,56 @@
+// Internal launcher declarations shared between the C-ABI layer and kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mxg.h"
+
+namespace mxg {
+
+uint64_t wait_timeout_ns();
+
+cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int elem,
+                              void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
+                              cudaStream_t stream, int num_sms);
+
+cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                              const int32_t* splits, int G, int pad, int elem, void* qT,
+                              int64_t ld_q, uint8_t* sT, int64_t ld_s, int64_t capacity,
+                              int64_t* pad_offsets, int32_t* status, cudaStream_t stream);
+
+// Grouped MX GEMM (tcgen05 block-scaled).  See gemm_mx.cu.
+struct GemmArgs {
+  int pass;  // mxg_pass
+  int G;
+  // operand A (M side) and B (N side): codes, row stride (bytes), plain scales
+  const uint8_t* a_data;
+  int64_t a_ld;
+  const uint8_t* a_scale;
+  int64_t a_scale_ld;
+  int64_t a_rows, a_cols;
+  int a_elem;
+  const uint8_t* b_data;
+  int64_t b_ld;
+  const uint8_t* b_scale;
+  int64_t b_scale_ld;
+  int64_t b_rows, b_cols;
+  int b_elem;
+  const int32_t* splits;
+  int64_t total_rows;  // S
+  int64_t N, K;        // fwd: out [S,N] over K; dgrad: out [S,K] over N; wgrad: out [G,N,K]
+  int pad;             // wgrad pad multiple
+  void* out;
+  int64_t ld_out;
+  int out_dtype;
+  int accumulate;
+  void* ws;
+  size_t ws_bytes;
+  int32_t* status;
+};
+
+size_t gemm_workspace_bytes(int pass, int G, int64_t S, int64_t N, int64_t K, int pad);
+mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_sms);
+
+}  // namespace mxg

@@ -1,0 +1,282 @@
+// BF16 -> MX (E2M1 / E4M3 + UE8M0 per 32) quantization kernels.
+//
+// Row-wise: the `_row_operand` bridge of "Triton mxfp4 (and a8w4) grouped GEMM
+// kernel" (ROCm TransformerEngine PR #723) and the MXFP8 E4M3 reference
+// quantizer of PR #745.  Column-wise segment-padded: the wgrad operand
+// `_col_operand_grouped_padded` of PR #723.  The scale rule is the OCP MX one
+// with the exponent floor at -127 required by the PR #745 review ("Clamp tiny
+// block scales to preserve nonzero values").
+//
+// Both kernels are HBM-bound.  Row-wise: one 16-byte load of 8 BF16 values per
+// thread per step, a 32-block spread over 4 adjacent lanes (amax by two
+// shuffles), outputs written as 4-byte (E2M1) / 8-byte (E4M3) coalesced
+// stores.  Column-wise: a CTA stages a 128-token x 128-column BF16 tile in
+// shared memory with 16-byte loads, then each thread quantizes columns down
+// the token axis and writes 64 (E2M1) / 128 (E4M3) contiguous bytes of a
+// transposed output row.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mxg {
+
+namespace {
+
+template <int kElem>
+struct MxFmt;
+template <>
+struct MxFmt<MXG_E2M1> {
+  static constexpr int kEmax = 2;
+};
+template <>
+struct MxFmt<MXG_E4M3> {
+  static constexpr int kEmax = 8;
+};
+
+// Quantize 8 BF16 values (four 32-bit words) with inverse scale `sinv`.
+// E2M1 -> one 32-bit word (8 nibbles); E4M3 -> two 32-bit words.
+template <int kElem>
+MXG_DEVINL void quantize8(const uint32_t* w, float sinv, uint32_t* out) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16lo_to_f32(w[i]) * sinv;
+    v[2 * i + 1] = bf16hi_to_f32(w[i]) * sinv;
+  }
+  if constexpr (kElem == MXG_E2M1) {
+    out[0] = cvt_e2m1x8(v) | e2m1x8_signs(w);
+  } else {
+    out[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]) | e4m3x4_signs(w[0], w[1]);
+    out[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]) | e4m3x4_signs(w[2], w[3]);
+  }
+}
+
+constexpr int kRowThreads = 256;
+constexpr int kRowUnroll = 4;  // 16-byte loads in flight per thread
+
+template <int kElem>
+__global__ void __launch_bounds__(kRowThreads) mx_rowwise_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
+    uint8_t* __restrict__ q, int64_t ld_q, uint8_t* __restrict__ s, int64_t ld_s) {
+  const int64_t chunks_per_row = cols >> 3;  // 8 elements per chunk
+  const int64_t total = rows * chunks_per_row;
+  const int64_t step = (int64_t)gridDim.x * kRowThreads * kRowUnroll;
+  // Chunk ids t = base + u*kRowThreads + threadIdx.x.  The loop bound is
+  // block-uniform so the shuffles see full warps; chunks_per_row is a multiple
+  // of 4, so the 4 lanes of a 32-block always share a row.
+  for (int64_t base = (int64_t)blockIdx.x * kRowThreads * kRowUnroll; base < total; base += step) {
+    uint32_t w[kRowUnroll][4];
+    int64_t r[kRowUnroll], c8[kRowUnroll];
+#pragma unroll
+    for (int u = 0; u < kRowUnroll; ++u) {
+      const int64_t t = base + u * kRowThreads + threadIdx.x;
+      r[u] = t < total ? t / chunks_per_row : -1;
+      c8[u] = t < total ? t - r[u] * chunks_per_row : 0;
+      uint4 raw = make_uint4(0, 0, 0, 0);
+      if (r[u] >= 0) raw = __ldcs(reinterpret_cast<const uint4*>(x + r[u] * ld_x + c8[u] * 8));
+      w[u][0] = raw.x; w[u][1] = raw.y; w[u][2] = raw.z; w[u][3] = raw.w;
+    }
+#pragma unroll
+    for (int u = 0; u < kRowUnroll; ++u) {
+      uint32_t am = max(max(bf16x2_absmax_bits(w[u][0]), bf16x2_absmax_bits(w[u][1])),
+                        max(bf16x2_absmax_bits(w[u][2]), bf16x2_absmax_bits(w[u][3])));
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      if (r[u] < 0) continue;
+      const int e = mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax);
+      uint32_t o[2];
+      quantize8<kElem>(w[u], pow2_neg(e), o);
+      if constexpr (kElem == MXG_E2M1) {
+        *reinterpret_cast<uint32_t*>(q + r[u] * ld_q + c8[u] * 4) = o[0];
+      } else {
+        *reinterpret_cast<uint2*>(q + r[u] * ld_q + c8[u] * 8) = make_uint2(o[0], o[1]);
+      }
+      if ((threadIdx.x & 3) == 0) s[r[u] * ld_s + (c8[u] >> 2)] = (uint8_t)(e + 127);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Column-wise, segment-padded.
+// ---------------------------------------------------------------------------
+constexpr int kColTokens = 128;  // padded token positions per CTA (4 blocks)
+constexpr int kColCols = 128;    // input columns per CTA
+constexpr int kColThreads = 256;
+
+// Per-CTA expert table: splits validated and prefix-summed in shared memory.
+struct SegTable {
+  int64_t off[kMaxExperts + 1];   // row offsets
+  int64_t poff[kMaxExperts + 1];  // padded offsets
+};
+
+// Builds the prefix tables with a block-wide scan (blockDim.x == 256, two
+// experts per thread).  Returns false -- after reporting when `do_report` --
+// if a split is negative, the splits do not sum to `rows`, or the padded
+// total exceeds `capacity`.  All threads must call it.
+__device__ bool build_seg_table(SegTable& t, const int32_t* __restrict__ splits, int G,
+                                int64_t rows, int pad, int64_t capacity, int32_t* status,
+                                bool do_report) {
+  __shared__ int64_t warp_m[8], warp_p[8];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int64_t m0 = 0, m1 = 0;
+  if (2 * tid < G) m0 = splits[2 * tid];
+  if (2 * tid + 1 < G) m1 = splits[2 * tid + 1];
+  const bool neg = (m0 < 0) || (m1 < 0);
+  const int64_t p0 = m0 > 0 ? ((m0 + pad - 1) / pad) * pad : 0;
+  const int64_t p1 = m1 > 0 ? ((m1 + pad - 1) / pad) * pad : 0;
+  int64_t sm = m0 + m1, sp = p0 + p1;  // inclusive warp scans of the pair sums
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int64_t om = __shfl_up_sync(0xffffffffu, sm, d);
+    const int64_t op = __shfl_up_sync(0xffffffffu, sp, d);
+    if (lane >= d) { sm += om; sp += op; }
+  }
+  if (lane == 31) { warp_m[wid] = sm; warp_p[wid] = sp; }
+  const int any_neg = __syncthreads_or(neg);
+  int64_t bm = 0, bp = 0;
+  for (int w = 0; w < wid; ++w) { bm += warp_m[w]; bp += warp_p[w]; }
+  // exclusive prefix before this thread's pair
+  const int64_t em = bm + sm - (m0 + m1), ep = bp + sp - (p0 + p1);
+  if (2 * tid <= G) { t.off[2 * tid] = em; t.poff[2 * tid] = ep; }
+  if (2 * tid + 1 <= G) { t.off[2 * tid + 1] = em + m0; t.poff[2 * tid + 1] = ep + p0; }
+  __syncthreads();
+  int bad = 0;
+  if (any_neg) bad = MXG_ERR_SPLITS;
+  else if (t.off[G] != rows) bad = MXG_ERR_SPLITS;
+  else if (t.poff[G] > capacity) bad = MXG_ERR_CAPACITY;
+  if (bad && do_report && tid == 0) report(status, bad);
+  return bad == 0;
+}
+
+// Expert owning padded position j (poff[g] <= j < poff[g+1]); -1 if beyond.
+__device__ int find_segment(const SegTable& t, int G, int64_t j) {
+  if (j >= t.poff[G]) return -1;
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {  // last g with poff[g] <= j
+    const int mid = (lo + hi + 1) >> 1;
+    if (t.poff[mid] <= j) lo = mid; else hi = mid - 1;
+  }
+  return lo;  // the last such g is non-empty since poff[g+1] > j
+}
+
+template <int kElem>
+__global__ void __launch_bounds__(kColThreads) mx_colwise_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
+    const int32_t* __restrict__ splits, int G, int pad, uint8_t* __restrict__ qT, int64_t ld_q,
+    uint8_t* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
+    int32_t* status) {
+  __shared__ SegTable tab;
+  __shared__ __align__(16) uint16_t tile[kColTokens][kColCols + 8];  // +8: spread banks
+  const bool first = blockIdx.x == 0 && blockIdx.y == 0;
+  if (!build_seg_table(tab, splits, G, rows, pad, capacity, status, first)) return;
+  if (first && pad_offsets != nullptr) {
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) pad_offsets[g] = tab.poff[g];
+  }
+  const int64_t j0 = (int64_t)blockIdx.x * kColTokens;  // first padded position
+  if (j0 >= tab.poff[G]) return;
+  const int64_t c0 = (int64_t)blockIdx.y * kColCols;
+
+  // Stage the tile: token position j -> source row (or zero padding).
+  for (int idx = threadIdx.x; idx < kColTokens * (kColCols / 8); idx += kColThreads) {
+    const int jr = idx / (kColCols / 8);
+    const int cc = (idx % (kColCols / 8)) * 8;
+    const int64_t j = j0 + jr;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    const int g = find_segment(tab, G, j);
+    if (g >= 0) {
+      const int64_t tok = j - tab.poff[g];
+      if (tok < tab.off[g + 1] - tab.off[g] && c0 + cc < cols)
+        v = __ldcs(reinterpret_cast<const uint4*>(x + (tab.off[g] + tok) * ld_x + c0 + cc));
+    }
+    *reinterpret_cast<uint4*>(&tile[jr][cc]) = v;
+  }
+  __syncthreads();
+
+  // Each thread: one column, two 32-blocks (threads t and t+128 share a column).
+  const int col = threadIdx.x & (kColCols - 1);
+  const int half = threadIdx.x >> 7;  // blocks {2*half, 2*half+1}
+  if (c0 + col >= cols) return;
+  uint8_t* qrow = qT + (c0 + col) * ld_q;
+  uint8_t sc[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const int blk = 2 * half + b;
+    const int64_t jb = j0 + 32 * blk;
+    if (jb >= tab.poff[G]) {
+      sc[b] = 0xFF;  // marker: beyond the last expert, nothing written
+      continue;
+    }
+    uint32_t w[16];
+    uint32_t am = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t lo = tile[32 * blk + 2 * i][col];
+      const uint32_t hi = tile[32 * blk + 2 * i + 1][col];
+      w[i] = lo | (hi << 16);
+      am = max(am, bf16x2_absmax_bits(w[i]));
+    }
+    const int e = mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax);
+    const float sinv = pow2_neg(e);
+    sc[b] = (uint8_t)(e + 127);
+    if constexpr (kElem == MXG_E2M1) {
+      uint4 o;
+      quantize8<kElem>(&w[0], sinv, &o.x);
+      quantize8<kElem>(&w[4], sinv, &o.y);
+      quantize8<kElem>(&w[8], sinv, &o.z);
+      quantize8<kElem>(&w[12], sinv, &o.w);
+      *reinterpret_cast<uint4*>(qrow + jb / 2) = o;
+    } else {
+      uint4 o0, o1;
+      quantize8<kElem>(&w[0], sinv, &o0.x);
+      quantize8<kElem>(&w[4], sinv, &o0.z);
+      quantize8<kElem>(&w[8], sinv, &o1.x);
+      quantize8<kElem>(&w[12], sinv, &o1.z);
+      *reinterpret_cast<uint4*>(qrow + jb) = o0;
+      *reinterpret_cast<uint4*>(qrow + jb + 16) = o1;
+    }
+  }
+  uint8_t* srow = sT + (c0 + col) * ld_s + (j0 >> 5) + 2 * half;
+  if (sc[0] != 0xFF) srow[0] = sc[0];
+  if (sc[1] != 0xFF) srow[1] = sc[1];
+}
+
+}  // namespace
+
+cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int elem,
+                              void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
+                              cudaStream_t stream, int num_sms) {
+  const int64_t total = rows * (cols / 8);
+  const int threads = kRowThreads;
+  int64_t blocks = (total + threads * kRowUnroll - 1) / (threads * kRowUnroll);
+  const int64_t cap = (int64_t)num_sms * 8 * 2;  // two full waves, then grid-stride
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  auto* xp = static_cast<const uint16_t*>(x);
+  auto* qp = static_cast<uint8_t*>(q);
+  if (elem == MXG_E2M1)
+    mx_rowwise_kernel<MXG_E2M1><<<(unsigned)blocks, threads, 0, stream>>>(xp, rows, cols, ld_x, qp,
+                                                                          ld_q, s, ld_s);
+  else
+    mx_rowwise_kernel<MXG_E4M3><<<(unsigned)blocks, threads, 0, stream>>>(xp, rows, cols, ld_x, qp,
+                                                                          ld_q, s, ld_s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                              const int32_t* splits, int G, int pad, int elem, void* qT,
+                              int64_t ld_q, uint8_t* sT, int64_t ld_s, int64_t capacity,
+                              int64_t* pad_offsets, int32_t* status, cudaStream_t stream) {
+  const int64_t gx = (capacity + kColTokens - 1) / kColTokens;
+  const int64_t gy = (cols + kColCols - 1) / kColCols;
+  dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)gy);
+  auto* xp = static_cast<const uint16_t*>(x);
+  auto* qp = static_cast<uint8_t*>(qT);
+  if (elem == MXG_E2M1)
+    mx_colwise_kernel<MXG_E2M1><<<grid, kColThreads, 0, stream>>>(
+        xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status);
+  else
+    mx_colwise_kernel<MXG_E4M3><<<grid, kColThreads, 0, stream>>>(
+        xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mxg

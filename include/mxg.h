@@ -1,0 +1,218 @@
+/*
+ * mxg.h -- C ABI of the GB300 grouped microscaled GEMM library (libmxg.so).
+ *
+ * The library computes the hot path of a mixture-of-experts linear layer whose
+ * operands use OCP microscaling (MX) formats: BF16 -> MXFP4 (E2M1) / MXFP8
+ * (E4M3) quantization with one UE8M0 scale per 32 elements, and the
+ * single-launch grouped GEMMs over experts whose row counts (m_splits) live in
+ * device memory:
+ *
+ *   forward (TN)  Y[off_g+i, n]  = sum_k A[off_g+i, k] * W[g*N+n, k]
+ *   dgrad   (NN)  dX[off_g+i, k] = sum_n dY[off_g+i, n] * Wt[k, g*N+n]
+ *   wgrad   (NT)  dW[g, n, k]   (+)= sum over expert g's padded token segment
+ *                                   of dYt[n, j] * Xt[k, j]
+ *
+ * Sources: "Triton mxfp4 (and a8w4) grouped GEMM kernel" (ROCm
+ * TransformerEngine PR #723: the three passes, the split checks, the
+ * segment-padded column-wise wgrad operand); PR #745 (the a8w4 mix, fwd only,
+ * and the -127 scale-exponent clamp); "Add ROCm Triton blockwise FP8 grouped
+ * GEMM" (PR #716: 1x128 / 128x128 blockwise FP8); "Integrate MXFP4 hipblaslt
+ * GEMM support" (PR #697: per-pass shapes).  off_g is the exclusive prefix sum
+ * of m_splits.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All data pointers are DEVICE pointers owned by the caller; the library
+ *    allocates nothing, keeps no state between calls (except the wait timeout
+ *    below) and enqueues work on `stream` only, without synchronising, except
+ *    mxg_check_status.  `stream` is a cudaStream_t passed as void* (NULL = the
+ *    legacy default stream).
+ *  - Matrices are row-major.  Strides (`ld*`) are in BYTES for quantized codes
+ *    and scale bytes, and in ELEMENTS for BF16 / FP32 buffers, as stated per
+ *    argument.  The quantized code layouts are: E4M3 one byte per element;
+ *    E2M1 two per byte, element 2j in the low nibble.  UE8M0 scale byte b
+ *    encodes 2^(b-127).
+ *  - Host checks run first and do not touch the GPU: null pointers, sizes,
+ *    divisibility, 16-byte alignment of pointers and strides, 1 <= G <= 512.
+ *    Then the pointers' device and the device architecture (sm_103) are
+ *    checked.  A failing check returns its code and enqueues nothing.
+ *  - Checks that need device data (m_splits >= 0, sum(m_splits) == rows,
+ *    padded rows within capacity) run inside the kernels: the first failure is
+ *    written to *d_status (an int32 in device memory, initialised to 0 by the
+ *    caller) with an atomic compare-and-swap, and the kernels then write no
+ *    output.  mxg_check_status reads and clears it.
+ *  - Every in-kernel wait is bounded by a time limit (mxg_set_wait_timeout_ns);
+ *    a wait that runs out records MXG_ERR_TIMEOUT in *d_status and the kernel
+ *    returns instead of hanging.
+ */
+#ifndef MXG_H_
+#define MXG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mxg_status {
+  MXG_OK = 0,
+  MXG_ERR_NULL = 1,        /* a required pointer is NULL */
+  MXG_ERR_SHAPE = 2,       /* sizes inconsistent or not divisible as required */
+  MXG_ERR_ALIGN = 3,       /* pointer or stride not 16-byte aligned */
+  MXG_ERR_SPLITS = 4,      /* device-side: negative split or sum != rows */
+  MXG_ERR_UNSUPPORTED = 5, /* format combination / option not provided */
+  MXG_ERR_DEVICE = 6,      /* pointer not device memory, mixed devices, or not sm_103 */
+  MXG_ERR_CUDA = 7,        /* a CUDA runtime call failed */
+  MXG_ERR_TIMEOUT = 8,     /* device-side: a bounded wait ran out */
+  MXG_ERR_WORKSPACE = 9,   /* workspace missing or smaller than required */
+  MXG_ERR_CAPACITY = 10    /* device-side: padded rows exceed the output capacity */
+} mxg_status;
+
+typedef enum mxg_elem { MXG_E2M1 = 1, MXG_E4M3 = 2 } mxg_elem;
+typedef enum mxg_out_dtype { MXG_OUT_BF16 = 1, MXG_OUT_F32 = 2 } mxg_out_dtype;
+typedef enum mxg_pass { MXG_PASS_FWD = 0, MXG_PASS_DGRAD = 1, MXG_PASS_WGRAD = 2 } mxg_pass;
+
+/* One MX operand of a grouped GEMM, K-major: `rows` rows of `cols` elements,
+ * quantized along `cols` (the contraction dimension).
+ *   data   : codes, row r at (uint8*)data + r*ld  (ld >= cols or cols/2 bytes)
+ *   scale  : UE8M0 bytes, row r at scale + r*scale_ld, entries [0, cols/32)
+ *   elem   : MXG_E2M1 or MXG_E4M3
+ * Requirements: cols % 32 == 0; data 16-byte aligned (32 for E2M1 weights of
+ * the a8w4 forward); ld % 16 == 0 (32 for those weights). */
+typedef struct mxg_mx_operand {
+  const void* data;
+  const uint8_t* scale;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;
+  int64_t scale_ld;
+  int32_t elem;
+  int32_t reserved; /* must be 0 */
+} mxg_mx_operand;
+
+/* --------------------------------------------------------------------------
+ * MX quantization
+ * ------------------------------------------------------------------------ */
+
+/* Row-wise MX quantization (PR #723 `_row_operand`; PR #745 MXFP8 E4M3
+ * reference quantizer).  For each row and each block of 32 consecutive BF16
+ * values: e = clamp(floor(log2(amax)) - emax, -127, 127) (emax 2 for E2M1,
+ * 8 for E4M3; e = -127 for an all-zero block); scale byte = e + 127; element =
+ * x * 2^-e rounded to nearest, ties to even, saturating (6 / 448), sign kept.
+ *   x      : BF16 [rows, cols], row stride ld_x elements (ld_x % 8 == 0)
+ *   q      : codes [rows, cols/2] (E2M1) or [rows, cols] (E4M3), stride ld_q bytes
+ *   s      : scale bytes [rows, cols/32], stride ld_s bytes
+ * cols % 32 == 0; rows may be 0 (no launch).  Writes only q and s. */
+mxg_status mx_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                               int32_t elem, void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
+                               void* stream);
+
+/* Column-wise, segment-padded MX quantization: the wgrad operand of PR #723
+ * (`_col_operand_grouped_padded`).  x is BF16 [rows, cols] with the experts'
+ * rows concatenated in order.  Expert g's rows [off_g, off_g+m_g) are
+ * transposed and written to output columns [poff_g, poff_g + m_g), followed by
+ * zero columns up to p_g = ceil(m_g/pad)*pad; 32-blocks start at poff_g, so no
+ * block straddles two experts.  poff is the exclusive prefix sum of p_g.
+ *   d_m_splits   : int32[G] device
+ *   pad_multiple : positive multiple of 32
+ *   qT           : codes [cols, capacity(/2)], row stride ld_q bytes
+ *   sT           : scale bytes [cols, capacity/32], row stride ld_s bytes
+ *   capacity     : columns available in qT (e.g. mx_padded_rows_capacity)
+ *   d_pad_offsets: int64[G+1] device, receives poff (may be NULL)
+ * Columns beyond poff_G are left untouched.  Device errors: MXG_ERR_SPLITS,
+ * MXG_ERR_CAPACITY (poff_G > capacity). */
+mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64_t cols,
+                                              int64_t ld_x, const int32_t* d_m_splits,
+                                              int32_t G, int32_t pad_multiple, int32_t elem,
+                                              void* qT, int64_t ld_q, uint8_t* sT, int64_t ld_s,
+                                              int64_t capacity, int64_t* d_pad_offsets,
+                                              int32_t* d_status, void* stream);
+
+/* Upper bound of sum_g ceil(m_g/pad)*pad over all splits of `rows` into G
+ * experts: floor((rows + k*(pad-1)) / pad) * pad with k = min(G, rows), the
+ * most experts that can be non-empty.  -1 on invalid input. */
+int64_t mx_padded_rows_capacity(int64_t rows, int32_t G, int32_t pad);
+
+/* --------------------------------------------------------------------------
+ * Grouped MX GEMMs (single launch over all experts; tcgen05 block-scaled MMA)
+ *
+ * Supported element pairs: E2M1 x E2M1 (MXFP4, all passes), E4M3 x E2M1
+ * (a8w4: A = MXFP8 activations, W = MXFP4 weights; forward only, K % 128 == 0)
+ * and E4M3 x E4M3 (MXFP8, all passes).  Products are exact; accumulation is in
+ * fp32; the output is rounded to BF16 (nearest even) or stored as FP32.
+ * Only each expert's valid rows/columns are written.
+ *
+ * ws / ws_bytes: device scratch of at least mxg_gemm_workspace_size(...)
+ * bytes, 256-byte aligned; the UE8M0 scales are re-laid out there into the
+ * tensor-core staging order before the GEMM kernel runs.
+ * ------------------------------------------------------------------------ */
+
+/* Forward (TN).  A: rows = S (sum of m_splits), cols = K.  W: rows = G*N,
+ * cols = K (expert g's weight is rows [g*N, g*N+N)).  out: [S, N] with row
+ * stride ld_out elements (ld_out % 8 == 0).  N % 32 == 0. */
+mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
+                            const int32_t* d_m_splits, int32_t G, int64_t N, void* out,
+                            int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
+                            int32_t* d_status, void* stream);
+
+/* dgrad (NN).  dY: rows = S, cols = N.  Wt: rows = K, cols = G*N -- W
+ * transposed and quantized along N within each expert (mx_quantize_colwise_
+ * segment_padded of W [G*N, K] with m_splits = {N, ..., N}, pad 32).
+ * out: [S, K], row stride ld_out elements.  K % 32 == 0, N % 32 == 0. */
+mxg_status grouped_gemm_dgrad(const mxg_mx_operand* dY, const mxg_mx_operand* Wt,
+                              const int32_t* d_m_splits, int32_t G, void* out, int64_t ld_out,
+                              int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* d_status,
+                              void* stream);
+
+/* wgrad (NT, variable K per expert).  dYt: rows = N, Xt: rows = K, both
+ * column-wise segment-padded operands (mx_quantize_colwise_segment_padded with
+ * the same m_splits and pad_multiple); cols = their capacity.  The padded
+ * offsets are recomputed from d_m_splits and pad_multiple.  total_rows = S
+ * (validated against sum(m_splits)).  out: [G, N, K] contiguous; with
+ * accumulate != 0 (FP32 only) the result is added in place (fp32 main_grad),
+ * otherwise stored.  An empty expert stores zeros (or leaves out unchanged
+ * when accumulating). */
+mxg_status grouped_gemm_wgrad(const mxg_mx_operand* dYt, const mxg_mx_operand* Xt,
+                              const int32_t* d_m_splits, int32_t G, int64_t total_rows,
+                              int32_t pad_multiple, void* out, int32_t out_dtype,
+                              int32_t accumulate, void* ws, size_t ws_bytes, int32_t* d_status,
+                              void* stream);
+
+/* Scratch bytes needed by a grouped MX GEMM pass (an upper bound valid for
+ * every split of S rows into G experts).  For MXG_PASS_FWD and DGRAD the
+ * arguments are (G, S, N, K); for MXG_PASS_WGRAD, S is the operands' column
+ * capacity.  Returns 0 on invalid input. */
+size_t mxg_gemm_workspace_size(int32_t pass, int32_t G, int64_t S, int64_t N, int64_t K,
+                               int32_t pad_multiple);
+
+/* --------------------------------------------------------------------------
+ * Status and configuration
+ * ------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, reads *d_status, resets it to 0 and returns it (the
+ * only call that blocks the host). */
+mxg_status mxg_check_status(int32_t* d_status, void* stream);
+
+/* Static English description of a status code. */
+const char* mxg_status_string(mxg_status s);
+
+/* Time limit for every bounded wait inside the kernels (default 2 s). */
+void mxg_set_wait_timeout_ns(uint64_t ns);
+uint64_t mxg_get_wait_timeout_ns(void);
+
+/* Diagnostic for the bounded-wait machinery: launches one CTA that waits on
+ * an mbarrier nothing ever arrives at, with the same bounded wait the GEMM
+ * kernels use and limit `timeout_ns`.  The wait runs out, MXG_ERR_TIMEOUT is
+ * recorded in *d_status and the kernel returns; the CUDA context stays
+ * usable.  Returns the launch status (enqueue only). */
+mxg_status mxg_diag_bounded_wait(int32_t* d_status, uint64_t timeout_ns, void* stream);
+
+/* ABI version: major*10000 + minor*100 + patch. */
+int32_t mxg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXG_H_ */

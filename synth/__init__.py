@@ -55,6 +55,8 @@ def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0,
     host memory used for large tensors."""
     shape = tuple(int(s) for s in shape)
     out = np.empty(shape, dtype=np.uint16)
+    if out.size == 0:
+        return out
     rows = shape[0] if shape else 1
     flat = out.reshape(rows, -1) if shape else out.reshape(1, 1)
     cols = flat.shape[1]
@@ -127,8 +129,10 @@ def splits_uniform_rows(rng: np.random.Generator, G: int, rows: int) -> np.ndarr
 
 
 def padded_rows_capacity(rows: int, G: int, pad: int) -> int:
-    """Upper bound on sum_g ceil(m_g/pad)*pad over all splits of ``rows``."""
-    return ((rows + G * (pad - 1)) // pad) * pad
+    """Upper bound on sum_g ceil(m_g/pad)*pad over all splits of ``rows``
+    (at most min(G, rows) experts are non-empty and each adds < pad)."""
+    k = min(G, rows)
+    return ((rows + k * (pad - 1)) // pad) * pad
 
 
 @dataclasses.dataclass(frozen=True)

@@ -1,0 +1,140 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+declared in include/*.h, and its host-side argument checks return the
+documented codes without touching the device (fake, never dereferenced
+pointers are used; every call here fails before any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_bf16_mxfp4_gb300 import build, _lib
+    build.build()
+    return _lib.load()
+
+
+def header_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        txt = open(os.path.join(inc, f)).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        txt = re.sub(r"//[^\n]*", "", txt)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(", txt, flags=re.M):
+            name = m.group(1)
+            if name not in ("if", "sizeof"):
+                names.append(name)
+    return sorted(set(names))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = header_functions()
+    for must in ("mx_quantize_rowwise", "mx_quantize_colwise_segment_padded", "grouped_gemm_fwd",
+                 "grouped_gemm_dgrad", "grouped_gemm_wgrad", "mxg_check_status"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from fp8_bf16_mxfp4_gb300 import _lib
+    names = header_functions()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_pure_host_functions(lib):
+    assert lib.mxg_version() == 100
+    assert lib.mx_padded_rows_capacity(131072, 32, 32) == ((131072 + 32 * 31) // 32) * 32
+    assert lib.mx_padded_rows_capacity(3, 8, 32) == 96
+    assert lib.mx_padded_rows_capacity(0, 4, 128) == 0
+    assert lib.mx_padded_rows_capacity(-1, 4, 32) == -1
+    assert lib.mxg_status_string(0) == b"ok"
+    assert b"m_splits" in lib.mxg_status_string(4)
+    old = lib.mxg_get_wait_timeout_ns()
+    lib.mxg_set_wait_timeout_ns(12345)
+    assert lib.mxg_get_wait_timeout_ns() == 12345
+    lib.mxg_set_wait_timeout_ns(old)
+    assert lib.mxg_gemm_workspace_size(0, 0, 10, 32, 32, 32) == 0      # G < 1
+    assert lib.mxg_gemm_workspace_size(2, 4, 1024, 256, 512, 48) == 0  # pad % 32
+    assert lib.mxg_gemm_workspace_size(0, 4, 512, 256, 512, 32) > 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced
+
+
+def test_quantize_host_checks(lib):
+    vp = ctypes.c_void_p
+    q = lib.mx_quantize_rowwise
+    assert q(None, 4, 64, 64, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 1           # NULL x
+    assert q(vp(FAKE), 4, 48, 64, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 2       # cols % 32
+    assert q(vp(FAKE), 4, 64, 32, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 2       # ld_x < cols
+    assert q(vp(FAKE), 4, 64, 64, 3, vp(FAKE), 32, vp(FAKE), 2, None) == 5       # bad elem
+    assert q(vp(FAKE + 2), 4, 64, 64, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 3   # x misaligned
+    assert q(vp(FAKE), 4, 64, 68, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 3       # ld_x % 8
+    c = lib.mx_quantize_colwise_segment_padded
+    args = [vp(FAKE), 64, 64, 64, vp(FAKE), 4, 32, 1, vp(FAKE), 96, vp(FAKE), 4, 192, vp(FAKE),
+            vp(FAKE), None]
+    bad = list(args); bad[14] = None
+    assert c(*bad) == 1                                                           # NULL status
+    bad = list(args); bad[5] = 0
+    assert c(*bad) == 2                                                           # G < 1
+    bad = list(args); bad[5] = 513
+    assert c(*bad) == 2                                                           # G > 512
+    bad = list(args); bad[6] = 48
+    assert c(*bad) == 2                                                           # pad % 32
+    bad = list(args); bad[12] = 100
+    assert c(*bad) == 2                                                           # capacity % 32
+
+
+def _op(rows, cols, elem, data=FAKE, ld=None, scale_ld=None):
+    from fp8_bf16_mxfp4_gb300 import _lib
+    cb = cols // 2 if elem == 1 else cols
+    return _lib.MxOperandC(data, FAKE, rows, cols, ld if ld is not None else cb,
+                           scale_ld if scale_ld is not None else cols // 32, elem, 0)
+
+
+def test_gemm_host_checks(lib):
+    vp = ctypes.c_void_p
+    f = lib.grouped_gemm_fwd
+    ws = 1 << 30
+    A, W = _op(512, 512, 1), _op(4 * 256, 512, 1)
+    call = lambda A, W, G=4, N=256, ldo=256, dt=1, ws_bytes=ws, status=vp(FAKE): f(
+        ctypes.byref(A), ctypes.byref(W), vp(FAKE), G, N, vp(FAKE), ldo, dt, vp(FAKE), ws_bytes, status, None)
+    assert call(A, W, status=None) == 1                       # NULL status
+    assert call(A, _op(4 * 256, 480, 1)) == 2                  # K mismatch
+    assert call(A, _op(3 * 256, 512, 1)) == 2                  # W rows != G*N
+    assert call(A, W, G=0) == 2 and call(A, W, G=513) == 2     # G range
+    assert call(A, W, N=250, ldo=256) == 2                     # N % 32
+    assert call(A, W, ldo=200) == 2                            # ld_out < N
+    assert call(A, W, dt=3) == 5                               # bad out dtype
+    assert call(_op(512, 512, 1, data=FAKE + 8), W) == 3       # misaligned data
+    assert call(A, W, ws_bytes=16) == 9                        # workspace too small
+    assert call(_op(512, 512, 1), _op(1024, 512, 2)) == 5      # E2M1 x E4M3 not provided
+    assert call(_op(512, 96, 2), _op(1024, 96, 1)) == 2        # a8w4 needs K % 128
+    bad = _op(512, 512, 1); bad.reserved = 7
+    assert call(bad, W) == 5
+    d = lib.grouped_gemm_dgrad
+    dY, Wt = _op(512, 256, 2), _op(512, 4 * 256, 1)
+    assert d(ctypes.byref(dY), ctypes.byref(Wt), vp(FAKE), 4, vp(FAKE), 512, 1, vp(FAKE), ws,
+             vp(FAKE), None) == 5                              # a8w4 is forward-only
+    w = lib.grouped_gemm_wgrad
+    dYt, Xt = _op(256, 1024, 1), _op(512, 1024, 1)
+    assert w(ctypes.byref(dYt), ctypes.byref(Xt), vp(FAKE), 4, 900, 32, vp(FAKE), 1, 1, vp(FAKE),
+             ws, vp(FAKE), None) == 5                          # accumulate needs FP32
+    assert w(ctypes.byref(dYt), ctypes.byref(Xt), vp(FAKE), 4, 900, 48, vp(FAKE), 2, 1, vp(FAKE),
+             ws, vp(FAKE), None) == 2                          # pad % 32
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import fp8_bf16_mxfp4_gb300 as mxg
+    with pytest.raises(ValueError):
+        mxg.mx_quantize_rowwise(torch.zeros((4, 64), dtype=torch.bfloat16), "e2m1")
