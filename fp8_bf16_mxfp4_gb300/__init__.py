@@ -75,7 +75,16 @@ class MXOperand:
 
     def c(self) -> _lib.MxOperandC:
         return _lib.MxOperandC(self.data.data_ptr(), self.scale.data_ptr(), self.rows, self.cols,
-                               self.data.stride(0), self.scale.stride(0), ELEM[self.elem], 0)
+                               _ld(self.data, _codes_cols(self.elem, self.cols)),
+                               _ld(self.scale, self.cols // 32), ELEM[self.elem], 0)
+
+
+def _ld(t: torch.Tensor, row_elems: int) -> int:
+    """Row stride in elements; zero-size tensors report degenerate strides,
+    so their logical (contiguous) stride is used."""
+    if t.numel() == 0:
+        return max(row_elems, 16)
+    return t.stride(0)
 
 
 _status = {}
@@ -122,8 +131,9 @@ def mx_quantize_rowwise(x: torch.Tensor, elem: str, q: torch.Tensor | None = Non
     if s is None:
         s = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
     lib = _lib.load()
-    _ok(lib.mx_quantize_rowwise(_ptr(x), rows, cols, x.stride(0), ELEM[elem], _ptr(q), q.stride(0),
-                                _ptr(s), s.stride(0), _stream(x.device)), "mx_quantize_rowwise")
+    _ok(lib.mx_quantize_rowwise(_ptr(x), rows, cols, _ld(x, cols), ELEM[elem], _ptr(q),
+                                _ld(q, _codes_cols(elem, cols)), _ptr(s), _ld(s, cols // 32),
+                                _stream(x.device)), "mx_quantize_rowwise")
     return MXOperand(q, s, elem, cols)
 
 
@@ -144,8 +154,9 @@ def mx_quantize_colwise_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, 
     st = status if status is not None else status_tensor(x.device)
     lib = _lib.load()
     _ok(lib.mx_quantize_colwise_segment_padded(
-        _ptr(x), S, C, x.stride(0), _ptr(m_splits), G, pad_multiple, ELEM[elem], _ptr(qT),
-        qT.stride(0), _ptr(sT), sT.stride(0), capacity, _ptr(poff), _ptr(st), _stream(x.device)),
+        _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, pad_multiple, ELEM[elem], _ptr(qT),
+        _ld(qT, _codes_cols(elem, capacity)), _ptr(sT), _ld(sT, capacity // 32), capacity,
+        _ptr(poff), _ptr(st), _stream(x.device)),
         "mx_quantize_colwise_segment_padded")
     if check:
         check_status(st)
@@ -177,7 +188,7 @@ def grouped_gemm_fwd(A: MXOperand, W: MXOperand, m_splits: torch.Tensor, N: int,
     st = status if status is not None else status_tensor(dev)
     a, w = A.c(), W.c()
     _ok(_lib.load().grouped_gemm_fwd(ctypes.byref(a), ctypes.byref(w), _ptr(m_splits), G, N,
-                                     _ptr(out), out.stride(0), _OUT[out.dtype], _ptr(ws),
+                                     _ptr(out), _ld(out, N), _OUT[out.dtype], _ptr(ws),
                                      ws.numel(), _ptr(st), _stream(dev)), "grouped_gemm_fwd")
     if check:
         check_status(st)
@@ -200,7 +211,7 @@ def grouped_gemm_dgrad(dY: MXOperand, Wt: MXOperand, m_splits: torch.Tensor,
     st = status if status is not None else status_tensor(dev)
     a, b = dY.c(), Wt.c()
     _ok(_lib.load().grouped_gemm_dgrad(ctypes.byref(a), ctypes.byref(b), _ptr(m_splits), G,
-                                       _ptr(out), out.stride(0), _OUT[out.dtype], _ptr(ws),
+                                       _ptr(out), _ld(out, K), _OUT[out.dtype], _ptr(ws),
                                        ws.numel(), _ptr(st), _stream(dev)), "grouped_gemm_dgrad")
     if check:
         check_status(st)
