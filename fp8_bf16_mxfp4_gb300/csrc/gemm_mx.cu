@@ -234,15 +234,20 @@ MXG_DEVINL int find_prefix(const int32_t* pre, int G, int x) {  // last g with p
   return lo;
 }
 
+constexpr int kPackKc = 8;  // k-chunks per CTA
+
+// grid = (row tiles, k-chunk groups of kPackKc, operand); one thread per row
+// of the 128-row tile.  The expert is looked up once per CTA (row-segmented
+// operands) or advanced incrementally along the k-chunks (contraction-
+// segmented operands), so the per-chunk work is a few byte loads and one
+// 4-byte store.
 __global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, PackSrc sb) {
-  const int32_t* plan = p.plan;
-  const PlanView pv = plan_view(const_cast<int32_t*>(plan), p.G);
+  const PlanView pv = plan_view(const_cast<int32_t*>(p.plan), p.G);
   if (pv.hdr[0] == 0) return;
-  const bool isA = blockIdx.y == 0;
+  const bool isA = blockIdx.z == 0;
   const PackSrc ps = isA ? sa : sb;
   const int G = p.G;
   const int nrt = (int)((p.N + 127) / 128);
-  // totals for this operand
   int RT, KC;
   if (p.pass == MXG_PASS_FWD) {
     RT = isA ? pv.rt[G] : p.rtB;
@@ -254,57 +259,73 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, 
     RT = isA ? p.rtA_fixed : p.rtB;
     KC = pv.kc[G];
   }
-  const int64_t total = (int64_t)RT * KC;
+  const int rt = blockIdx.x;
+  const int kc0 = blockIdx.y * kPackKc;
+  if (rt >= RT || kc0 >= KC) return;
+  const bool wg = p.pass == MXG_PASS_WGRAD;
+  const bool kseg = wg || (p.pass == MXG_PASS_DGRAD && !isA);
+  __shared__ int32_t pre[kMaxExperts + 1];
+  __shared__ int32_t pof[kMaxExperts + 1];
+  if ((isA && !kseg) || wg) {
+    for (int i = threadIdx.x; i <= G; i += blockDim.x) {
+      pre[i] = wg ? pv.kc[i] : pv.rt[i];
+      if (wg) pof[i] = pv.poff[i];
+    }
+    __syncthreads();
+  }
+  int t, R;
+  int64_t row0;
+  int g = 0;
+  if (!kseg) {
+    if (isA) {
+      g = find_prefix(pre, G, rt);
+      t = rt - pre[g];
+      row0 = pv.off[g];
+      R = pv.off[g + 1] - pv.off[g];
+    } else {  // forward weights: G blocks of N rows
+      g = rt / nrt;
+      t = rt - g * nrt;
+      row0 = (int64_t)g * p.N;
+      R = (int)p.N;
+    }
+  } else {
+    t = rt;
+    row0 = 0;
+    R = (int)(isA ? p.N : p.K);
+    if (wg) g = find_prefix(pre, G, kc0);
+  }
+  const int KBrow = (int)((p.pass == MXG_PASS_FWD ? p.K : p.N) / 32);  // row-segmented only
   const int r = threadIdx.x;
-  for (int64_t id = blockIdx.x; id < total; id += gridDim.x) {
-    const int kcg = (int)(id / RT), rtg = (int)(id % RT);
-    int g, t, c;
-    int64_t row0, k0;
-    int R, KB;
-    if (p.pass == MXG_PASS_WGRAD || (p.pass == MXG_PASS_DGRAD && !isA)) {
-      // rows shared, contraction segmented per expert
-      if (p.pass == MXG_PASS_WGRAD) {
-        g = find_prefix(pv.kc, G, kcg);
-        c = kcg - pv.kc[g];
-        k0 = pv.poff[g];
-        KB = (pv.poff[g + 1] - pv.poff[g]) / 32;
-      } else {
-        g = kcg / nrt;
-        c = kcg - g * nrt;
-        k0 = (int64_t)g * p.N;
-        KB = (int)(p.N / 32);
-      }
-      t = rtg;
-      row0 = 0;
-      R = (int)(isA ? p.N : p.K);
-    } else {
-      // rows segmented per expert, contraction shared
-      if (isA) {
-        g = find_prefix(pv.rt, G, rtg);
-        t = rtg - pv.rt[g];
-        row0 = pv.off[g];
-        R = pv.off[g + 1] - pv.off[g];
-      } else {  // fwd B: G blocks of N rows
-        g = rtg / nrt;
-        t = rtg - g * nrt;
-        row0 = (int64_t)g * p.N;
-        R = (int)p.N;
-      }
-      c = kcg;
-      k0 = 0;
-      KB = (int)((p.pass == MXG_PASS_FWD ? p.K : p.N) / 32);
+  const int rr = t * 128 + r;
+  const bool row_ok = rr < R;
+  const uint8_t* srow = ps.src + (row0 + (row_ok ? rr : 0)) * ps.ld;
+  uint8_t* dst = ps.dst + (r & 31) * 16 + (r >> 5) * 4;
+  const int kc_end = min(KC, kc0 + kPackKc);
+  for (int kcg = kc0; kcg < kc_end; ++kcg) {
+    int c, KB;
+    int64_t kb0;
+    if (!kseg) {
+      c = kcg; kb0 = 0; KB = KBrow;
+    } else if (wg) {
+      while (pre[g + 1] <= kcg) ++g;
+      c = kcg - pre[g];
+      kb0 = pof[g] >> 5;
+      KB = (pof[g + 1] - pof[g]) >> 5;
+    } else {  // dgrad weights: expert g's contraction is columns [g*N, g*N+N)
+      g = kcg / nrt;
+      c = kcg - g * nrt;
+      kb0 = (int64_t)g * (p.N >> 5);
+      KB = (int)(p.N >> 5);
     }
     uint32_t w = 0;
-    const int rr = t * 128 + r;
-    if (rr < R) {
-      const uint8_t* srow = ps.src + (row0 + rr) * ps.ld + (k0 >> 5);
+    if (row_ok) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int kb = c * 4 + j;
-        if (kb < KB) w |= (uint32_t)__ldg(srow + kb) << (8 * j);
+        if (kb < KB) w |= (uint32_t)__ldg(srow + kb0 + kb) << (8 * j);
       }
     }
-    *reinterpret_cast<uint32_t*>(ps.dst + id * kChunkBytes + (r & 31) * 16 + (r >> 5) * 4) = w;
+    *reinterpret_cast<uint32_t*>(dst + ((int64_t)kcg * RT + rt) * kChunkBytes) = w;
   }
 }
 
@@ -712,10 +733,10 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   // 2. scale packing (both operands in one launch)
   PackSrc sa{a.a_scale, a.a_scale_ld, packA};
   PackSrc sb{a.b_scale, a.b_scale_ld, packB};
-  const int64_t chunks = std::max(ps.rtA * ps.kcA, ps.rtB * ps.kcB);
-  int64_t gx = std::min<int64_t>(chunks, (int64_t)num_sms * 16);
-  if (gx < 1) gx = 1;
-  pack_scales_kernel<<<dim3((unsigned)gx, 2), 128, 0, stream>>>(p, sa, sb);
+  const int64_t gx = std::max<int64_t>(1, std::max(ps.rtA, ps.rtB));
+  const int64_t gy = std::max<int64_t>(1, cdiv(std::max(ps.kcA, ps.kcB), kPackKc));
+  if (gy > 65535) return MXG_ERR_SHAPE;
+  pack_scales_kernel<<<dim3((unsigned)gx, (unsigned)gy, 2), 128, 0, stream>>>(p, sa, sb);
   if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
 
   // 3. tensor maps + GEMM

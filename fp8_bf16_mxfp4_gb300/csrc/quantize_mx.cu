@@ -7,10 +7,9 @@
 // with the exponent floor at -127 required by the PR #745 review ("Clamp tiny
 // block scales to preserve nonzero values").
 //
-// Both kernels are HBM-bound.  Row-wise: one 16-byte load of 8 BF16 values per
-// thread per step, a 32-block spread over 4 adjacent lanes (amax by two
-// shuffles), outputs written as 4-byte (E2M1) / 8-byte (E4M3) coalesced
-// stores.  Column-wise: a CTA stages a 128-token x 128-column BF16 tile in
+// Both kernels are HBM-bound.  Row-wise: one 32-element block per thread
+// (four 16-byte loads, the exponent computed once per block), coalesced
+// 16-byte stores.  Column-wise: a CTA stages a 128-token x 128-column BF16 tile in
 // shared memory with 16-byte loads, then each thread quantizes columns down
 // the token axis and writes 64 (E2M1) / 128 (E4M3) contiguous bytes of a
 // transposed output row.
@@ -51,47 +50,51 @@ MXG_DEVINL void quantize8(const uint32_t* w, float sinv, uint32_t* out) {
 }
 
 constexpr int kRowThreads = 256;
-constexpr int kRowUnroll = 4;  // 16-byte loads in flight per thread
 
+// One 32-element block per thread: four 16-byte loads (the block's 64 bytes),
+// amax and exponent computed once, 16 (E2M1) or 32 (E4M3) output bytes and
+// one scale byte.  Consecutive threads take consecutive blocks of a row, so
+// a warp reads 2 KB and writes 512 B / 1 KB contiguous.
 template <int kElem>
 __global__ void __launch_bounds__(kRowThreads) mx_rowwise_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
     uint8_t* __restrict__ q, int64_t ld_q, uint8_t* __restrict__ s, int64_t ld_s) {
-  const int64_t chunks_per_row = cols >> 3;  // 8 elements per chunk
-  const int64_t total = rows * chunks_per_row;
-  const int64_t step = (int64_t)gridDim.x * kRowThreads * kRowUnroll;
-  // Chunk ids t = base + u*kRowThreads + threadIdx.x.  The loop bound is
-  // block-uniform so the shuffles see full warps; chunks_per_row is a multiple
-  // of 4, so the 4 lanes of a 32-block always share a row.
-  for (int64_t base = (int64_t)blockIdx.x * kRowThreads * kRowUnroll; base < total; base += step) {
-    uint32_t w[kRowUnroll][4];
-    int64_t r[kRowUnroll], c8[kRowUnroll];
+  const int64_t blocks_per_row = cols >> 5;
+  const int64_t total = rows * blocks_per_row;
+  const int64_t step = (int64_t)gridDim.x * kRowThreads;
+  for (int64_t t = (int64_t)blockIdx.x * kRowThreads + threadIdx.x; t < total; t += step) {
+    const int64_t r = t / blocks_per_row;
+    const int64_t b = t - r * blocks_per_row;
+    const uint4* src = reinterpret_cast<const uint4*>(x + r * ld_x + b * 32);
+    uint32_t w[16];
 #pragma unroll
-    for (int u = 0; u < kRowUnroll; ++u) {
-      const int64_t t = base + u * kRowThreads + threadIdx.x;
-      r[u] = t < total ? t / chunks_per_row : -1;
-      c8[u] = t < total ? t - r[u] * chunks_per_row : 0;
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (r[u] >= 0) raw = __ldcs(reinterpret_cast<const uint4*>(x + r[u] * ld_x + c8[u] * 8));
-      w[u][0] = raw.x; w[u][1] = raw.y; w[u][2] = raw.z; w[u][3] = raw.w;
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldcs(src + i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
     }
+    uint32_t am = 0;
 #pragma unroll
-    for (int u = 0; u < kRowUnroll; ++u) {
-      uint32_t am = max(max(bf16x2_absmax_bits(w[u][0]), bf16x2_absmax_bits(w[u][1])),
-                        max(bf16x2_absmax_bits(w[u][2]), bf16x2_absmax_bits(w[u][3])));
-      am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
-      am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
-      if (r[u] < 0) continue;
-      const int e = mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax);
-      uint32_t o[2];
-      quantize8<kElem>(w[u], pow2_neg(e), o);
-      if constexpr (kElem == MXG_E2M1) {
-        *reinterpret_cast<uint32_t*>(q + r[u] * ld_q + c8[u] * 4) = o[0];
-      } else {
-        *reinterpret_cast<uint2*>(q + r[u] * ld_q + c8[u] * 8) = make_uint2(o[0], o[1]);
-      }
-      if ((threadIdx.x & 3) == 0) s[r[u] * ld_s + (c8[u] >> 2)] = (uint8_t)(e + 127);
+    for (int i = 0; i < 16; ++i) am = max(am, bf16x2_absmax_bits(w[i]));
+    const int e = mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax);
+    const float sinv = pow2_neg(e);
+    if constexpr (kElem == MXG_E2M1) {
+      uint4 o;
+      quantize8<kElem>(&w[0], sinv, &o.x);
+      quantize8<kElem>(&w[4], sinv, &o.y);
+      quantize8<kElem>(&w[8], sinv, &o.z);
+      quantize8<kElem>(&w[12], sinv, &o.w);
+      __stcs(reinterpret_cast<uint4*>(q + r * ld_q + b * 16), o);
+    } else {
+      uint4 o0, o1;
+      quantize8<kElem>(&w[0], sinv, &o0.x);
+      quantize8<kElem>(&w[4], sinv, &o0.z);
+      quantize8<kElem>(&w[8], sinv, &o1.x);
+      quantize8<kElem>(&w[12], sinv, &o1.z);
+      uint4* dst = reinterpret_cast<uint4*>(q + r * ld_q + b * 32);
+      __stcs(dst, o0);
+      __stcs(dst + 1, o1);
     }
+    s[r * ld_s + b] = (uint8_t)(e + 127);
   }
 }
 
@@ -244,10 +247,10 @@ __global__ void __launch_bounds__(kColThreads) mx_colwise_kernel(
 cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int elem,
                               void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
                               cudaStream_t stream, int num_sms) {
-  const int64_t total = rows * (cols / 8);
+  const int64_t total = rows * (cols / 32);
   const int threads = kRowThreads;
-  int64_t blocks = (total + threads * kRowUnroll - 1) / (threads * kRowUnroll);
-  const int64_t cap = (int64_t)num_sms * 8 * 2;  // two full waves, then grid-stride
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms * 8 * 4;  // a few full waves, then grid-stride
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   auto* xp = static_cast<const uint16_t*>(x);
