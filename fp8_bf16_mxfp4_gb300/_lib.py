@@ -50,6 +50,9 @@ SIGNATURES = {
     "grouped_gemm_wgrad": (
         c_i32, [ctypes.POINTER(MxOperandC), ctypes.POINTER(MxOperandC), c_vp, c_i32, c_i64, c_i32,
                 c_vp, c_i32, c_i32, c_vp, c_size, c_vp, c_vp]),
+    "grouped_gemm_fwd_noalloc": (
+        c_i32, [ctypes.POINTER(MxOperandC), ctypes.POINTER(MxOperandC), c_vp, c_i32, c_i64, c_vp,
+                c_i64, c_i32, c_vp, c_vp]),
     "mxg_gemm_workspace_size": (c_size, [c_i32, c_i32, c_i64, c_i64, c_i64, c_i32]),
     "mxg_check_status": (c_i32, [c_vp, c_vp]),
     "mxg_status_string": (ctypes.c_char_p, [c_i32]),

@@ -179,6 +179,31 @@ mxg_status grouped_gemm_wgrad(const mxg_mx_operand* dYt, const mxg_mx_operand* X
                               int32_t accumulate, void* ws, size_t ws_bytes, int32_t* d_status,
                               void* stream);
 
+/* grouped_gemm_fwd for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for code that must not
+ * call cudaMalloc at GEMM time -- work recorded inside a CUDA stream capture,
+ * an inference-engine plugin whose device memory is budgeted by its host, or a
+ * latency-critical path that never enters an allocator.
+ *
+ * Same arguments and results as grouped_gemm_fwd minus the workspace: the
+ * scratch is a file-scope device array of 32 MiB (33554432 bytes) inside
+ * libmxg.so, held on every GPU that loads the library until the process exits.
+ * A problem whose workspace (mxg_gemm_workspace_size(MXG_PASS_FWD, ...))
+ * exceeds 32 MiB is rejected with MXG_ERR_WORKSPACE before anything is
+ * enqueued.  Nothing is allocated: no cudaMalloc / cudaFree and no allocating
+ * library routine.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device made current); make that first call before any stream
+ *     capture begins.
+ *   - Every call shares the one array; each call fully rewrites the parts it
+ *     reads, so nothing has to be cleared between calls, but calls that may
+ *     overlap on the GPU (different streams without ordering) race on it and
+ *     must be serialised by the caller. */
+mxg_status grouped_gemm_fwd_noalloc(const mxg_mx_operand* A, const mxg_mx_operand* W,
+                                    const int32_t* d_m_splits, int32_t G, int64_t N, void* out,
+                                    int64_t ld_out, int32_t out_dtype, int32_t* d_status,
+                                    void* stream);
+
 /* Scratch bytes needed by a grouped MX GEMM pass (an upper bound valid for
  * every split of S rows into G experts).  For MXG_PASS_FWD and DGRAD the
  * arguments are (G, S, N, K); for MXG_PASS_WGRAD, S is the operands' column
