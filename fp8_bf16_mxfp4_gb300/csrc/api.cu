@@ -107,11 +107,12 @@ mxg_status check_operand(const mxg_mx_operand* op, bool allow_no_cols = false) {
 mxg_status check_out(const void* out, int64_t rows, int64_t ld_out, int64_t ncols, int32_t dtype) {
   if (dtype != MXG_OUT_BF16 && dtype != MXG_OUT_F32) return MXG_ERR_UNSUPPORTED;
   if (ld_out < ncols) return MXG_ERR_SHAPE;
+  // the epilogue writes whole 32-byte sectors
   const int64_t esz = dtype == MXG_OUT_BF16 ? 2 : 4;
-  if ((ld_out * esz) % 16 != 0) return MXG_ERR_ALIGN;
+  if ((ld_out * esz) % 32 != 0) return MXG_ERR_ALIGN;
   if (rows == 0) return MXG_OK;
   if (out == nullptr) return MXG_ERR_NULL;
-  if (!aligned16(out)) return MXG_ERR_ALIGN;
+  if (!aligned(out, 32)) return MXG_ERR_ALIGN;
   return MXG_OK;
 }
 

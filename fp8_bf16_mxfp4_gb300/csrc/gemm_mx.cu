@@ -345,36 +345,27 @@ struct Smem {
   static constexpr int kTotal = kTabOff + kTabBytes + 1024;  // + alignment slack
 };
 
-MXG_DEVINL void store_row_chunk(const Params& p, int64_t row, int64_t col, const uint32_t* r) {
-  if (p.out_dtype == MXG_OUT_BF16) {
-    uint32_t h[16];
+// FP32 output: one 32-column chunk of a row, stored (or added) with 32-byte
+// accesses.
+MXG_DEVINL void store_row_chunk_f32(const Params& p, int64_t row, int64_t col, uint32_t* r) {
+  float* dst = static_cast<float*>(p.out) + row * p.ld_out + col;
+  if (p.accumulate) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-      h[i] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * p.ld_out + col);
+    for (int i = 0; i < 4; ++i) {
+      uint32_t o[8];
+      ptx::ld_global_v8(dst + 8 * i, o);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-  } else {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.ld_out + col);
-    if (p.accumulate) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float4 o = dst[i];
-        o.x += __uint_as_float(r[4 * i]);
-        o.y += __uint_as_float(r[4 * i + 1]);
-        o.z += __uint_as_float(r[4 * i + 2]);
-        o.w += __uint_as_float(r[4 * i + 3]);
-        dst[i] = o;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                             __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+      for (int j = 0; j < 8; ++j)
+        r[8 * i + j] = __float_as_uint(__uint_as_float(o[j]) + __uint_as_float(r[8 * i + j]));
     }
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) ptx::st_global_v8(dst + 8 * i, r + 8 * i);
+}
+
+MXG_DEVINL uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<const uint32_t*>(&b);
 }
 
 template <int kKind>
@@ -566,7 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // BF16: the whole 128x256 tile is read from TMEM into registers (128
+    // packed words per thread), TMEM is handed back to the MMA warp, and only
+    // then are the rows stored -- the next tile's MMAs overlap the stores.
+    // FP32: 32-column chunks are read and stored in turn, TMEM released after.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int g, mt, nt;
@@ -577,24 +573,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = mt * BM + quarter * 32 + lane;
       const bool row_ok = row < e.M;
       const int64_t orow = e.out_row0 + row;
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col = nt * BN + c * 32;
-        if (col >= e.Nn) break;  // warp-uniform
-        uint32_t r[32];
-        if (e.Kc > 0) {
-          __syncwarp();
-          ptx::tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(c * 32), r);
-          ptx::tmem_ld_wait();
-        } else {
+      const int ncols = min(BN, e.Nn - nt * BN);  // multiple of 32
+      const int64_t col0 = (int64_t)nt * BN;
+      if (p.out_dtype == MXG_OUT_BF16) {
+        uint32_t h[BN / 2];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0;
-          if (p.accumulate) continue;  // empty expert, accumulating: leave untouched
+        for (int c = 0; c < BN / 32; ++c) {
+          if (c * 32 < ncols) {
+            uint32_t r[32];
+            if (e.Kc > 0) {
+              __syncwarp();
+              ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(c * 32), r);
+              ptx::tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = 0;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) h[c * 16 + i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
+          }
         }
-        if (row_ok) store_row_chunk(p, orow, col, r);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tmem_empty);
+        if (row_ok && !(e.Kc == 0 && p.accumulate)) {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * p.ld_out + col0;
+#pragma unroll
+          for (int c = 0; c < BN / 32; ++c) {
+            if (c * 32 < ncols) {
+              ptx::st_global_v8(dst + c * 32, &h[c * 16]);
+              ptx::st_global_v8(dst + c * 32 + 16, &h[c * 16 + 8]);
+            }
+          }
+        }
+      } else {
+        for (int c = 0; c < BN / 32; ++c) {
+          if (c * 32 >= ncols) break;  // warp-uniform
+          uint32_t r[32];
+          if (e.Kc > 0) {
+            __syncwarp();
+            ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(c * 32), r);
+            ptx::tmem_ld_wait();
+          } else {
+            if (p.accumulate) continue;  // empty expert, accumulating: leave untouched
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0;
+          }
+          if (row_ok) store_row_chunk_f32(p, orow, col0 + c * 32, r);
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tmem_empty);
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tmem_empty);
       acc_phase ^= 1u;
     }
   }

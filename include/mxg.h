@@ -150,7 +150,9 @@ int64_t mx_padded_rows_capacity(int64_t rows, int32_t G, int32_t pad);
 
 /* Forward (TN).  A: rows = S (sum of m_splits), cols = K.  W: rows = G*N,
  * cols = K (expert g's weight is rows [g*N, g*N+N)).  out: [S, N] with row
- * stride ld_out elements (ld_out % 8 == 0).  N % 32 == 0. */
+ * stride ld_out elements; out is 32-byte aligned and ld_out * element size is
+ * a multiple of 32 bytes (the same holds for every GEMM output below).
+ * N % 32 == 0. */
 mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
                             const int32_t* d_m_splits, int32_t G, int64_t N, void* out,
                             int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
