@@ -24,7 +24,9 @@ __all__ = [
     "MXOperand", "MXGError", "mx_quantize_rowwise", "mx_quantize_colwise_segment_padded",
     "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "gemm_workspace_size",
     "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns",
-    "library_path",
+    "library_path", "BWOperand", "bw_quantize_1x128", "bw_quantize_128x128",
+    "bw_quantize_colwise_padded", "bw_grouped_gemm_fwd", "bw_grouped_gemm_dgrad",
+    "bw_grouped_gemm_wgrad",
 ]
 
 ELEM = {"e2m1": 1, "e4m3": 2}
@@ -80,9 +82,10 @@ class MXOperand:
 
 
 def _ld(t: torch.Tensor, row_elems: int) -> int:
-    """Row stride in elements; zero-size tensors report degenerate strides,
-    so their logical (contiguous) stride is used."""
-    if t.numel() == 0:
+    """Row stride in elements.  Zero-size tensors and tensors with a single
+    row report arbitrary strides (the stride is never used for them), so their
+    logical contiguous stride is passed instead."""
+    if t.numel() == 0 or t.shape[0] <= 1:
         return max(row_elems, 16)
     return t.stride(0)
 
@@ -241,6 +244,150 @@ def grouped_gemm_wgrad(dYt: MXOperand, Xt: MXOperand, m_splits: torch.Tensor, to
                                        total_rows, pad_multiple, _ptr(out), _OUT[out.dtype],
                                        1 if accumulate else 0, _ptr(ws), ws.numel(), _ptr(st),
                                        _stream(dev)), "grouped_gemm_wgrad")
+    if check:
+        check_status(st)
+    return out
+
+
+# ----------------------------------------------------------------------------- blockwise FP8
+
+
+@dataclass
+class BWOperand:
+    """Blockwise-FP8 K-major operand: E4M3 codes [rows, cols] and fp32 scales
+    (activation-type [cols/128, >= rows] or weight-type [rows/128, cols/128])."""
+    data: torch.Tensor
+    scale: torch.Tensor
+
+    @property
+    def rows(self) -> int:
+        return self.data.shape[0]
+
+    @property
+    def cols(self) -> int:
+        return self.data.shape[1]
+
+    def c(self) -> _lib.BwOperandC:
+        return _lib.BwOperandC(self.data.data_ptr(), self.scale.data_ptr(), self.rows, self.cols,
+                               _ld(self.data, self.cols), _ld(self.scale, self.scale.shape[-1]),
+                               0, 0)
+
+
+def bw_quantize_1x128(x: torch.Tensor) -> BWOperand:
+    """BF16 [rows, cols] -> E4M3 [rows, cols] + activation-type scales [cols/128, rows]."""
+    _need_cuda(x)
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    s = torch.empty((C // 128, R), dtype=torch.float32, device=x.device)
+    _ok(_lib.load().bw_quantize_1x128(_ptr(x), R, C, _ld(x, C), _ptr(q), _ld(q, C), _ptr(s),
+                                      _ld(s, R), _stream(x.device)), "bw_quantize_1x128")
+    return BWOperand(q, s)
+
+
+def bw_quantize_128x128(w: torch.Tensor, transposed: bool = True):
+    """BF16 weights [rows, cols] -> (operand with weight-type scales, and when
+    `transposed` the dgrad copy [cols, rows] with its scales)."""
+    _need_cuda(w)
+    R, C = w.shape
+    dev = w.device
+    q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    s = torch.empty((R // 128, C // 128), dtype=torch.float32, device=dev)
+    qT = torch.empty((C, R), dtype=torch.uint8, device=dev) if transposed else None
+    sT = torch.empty((C // 128, R // 128), dtype=torch.float32, device=dev) if transposed else None
+    _ok(_lib.load().bw_quantize_128x128(_ptr(w), R, C, _ld(w, C), _ptr(q), _ld(q, C), _ptr(s),
+                                        _ptr(qT), _ld(qT, R) if transposed else 0, _ptr(sT),
+                                        _stream(dev)), "bw_quantize_128x128")
+    return BWOperand(q, s), (BWOperand(qT, sT) if transposed else None)
+
+
+def bw_quantize_colwise_padded(x: torch.Tensor, m_splits: torch.Tensor, capacity: int | None = None,
+                               status: torch.Tensor | None = None, check: bool = False):
+    """BF16 [S, C] -> (operand [C, capacity] with activation-type scales
+    [capacity/128, C], int64 padded offsets [G+1]); segments padded to 128."""
+    _need_cuda(x, m_splits)
+    S, C = x.shape
+    G = m_splits.numel()
+    if capacity is None:
+        capacity = mx_padded_rows_capacity(S, G, 128)
+    qT = torch.empty((C, capacity), dtype=torch.uint8, device=x.device)
+    sT = torch.empty((capacity // 128, C), dtype=torch.float32, device=x.device)
+    poff = torch.empty(G + 1, dtype=torch.int64, device=x.device)
+    st = status if status is not None else status_tensor(x.device)
+    _ok(_lib.load().bw_quantize_colwise_padded(
+        _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, _ptr(qT), _ld(qT, capacity), _ptr(sT),
+        _ld(sT, C), capacity, _ptr(poff), _ptr(st), _stream(x.device)), "bw_quantize_colwise_padded")
+    if check:
+        check_status(st)
+    return BWOperand(qT, sT), poff
+
+
+def _bw_ws(G, device, ws):
+    if ws is not None:
+        return ws
+    return torch.empty(max(int(_lib.load().bw_gemm_workspace_size(G)), 256), dtype=torch.uint8,
+                       device=device)
+
+
+def bw_grouped_gemm_fwd(A: BWOperand, W: BWOperand, m_splits: torch.Tensor, N: int,
+                        out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                        check: bool = False) -> torch.Tensor:
+    _need_cuda(A.data, W.data, m_splits)
+    G = m_splits.numel()
+    dev = A.data.device
+    if out is None:
+        out = torch.empty((A.rows, N), dtype=out_dtype, device=dev)
+    ws = _bw_ws(G, dev, workspace)
+    st = status if status is not None else status_tensor(dev)
+    a, w = A.c(), W.c()
+    _ok(_lib.load().bw_grouped_gemm_fwd(ctypes.byref(a), ctypes.byref(w), _ptr(m_splits), G, N,
+                                        _ptr(out), _ld(out, N), _OUT[out.dtype], _ptr(ws),
+                                        ws.numel(), _ptr(st), _stream(dev)), "bw_grouped_gemm_fwd")
+    if check:
+        check_status(st)
+    return out
+
+
+def bw_grouped_gemm_dgrad(dY: BWOperand, Wt: BWOperand, m_splits: torch.Tensor,
+                          out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+                          workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                          check: bool = False) -> torch.Tensor:
+    _need_cuda(dY.data, Wt.data, m_splits)
+    G = m_splits.numel()
+    dev = dY.data.device
+    K = Wt.rows
+    if out is None:
+        out = torch.empty((dY.rows, K), dtype=out_dtype, device=dev)
+    ws = _bw_ws(G, dev, workspace)
+    st = status if status is not None else status_tensor(dev)
+    a, b = dY.c(), Wt.c()
+    _ok(_lib.load().bw_grouped_gemm_dgrad(ctypes.byref(a), ctypes.byref(b), _ptr(m_splits), G,
+                                          _ptr(out), _ld(out, K), _OUT[out.dtype], _ptr(ws),
+                                          ws.numel(), _ptr(st), _stream(dev)), "bw_grouped_gemm_dgrad")
+    if check:
+        check_status(st)
+    return out
+
+
+def bw_grouped_gemm_wgrad(dYt: BWOperand, Xt: BWOperand, m_splits: torch.Tensor, total_rows: int,
+                          out: torch.Tensor | None = None, out_dtype=torch.float32,
+                          accumulate: bool = False, workspace: torch.Tensor | None = None,
+                          status: torch.Tensor | None = None, check: bool = False) -> torch.Tensor:
+    _need_cuda(dYt.data, Xt.data, m_splits)
+    G = m_splits.numel()
+    dev = dYt.data.device
+    N, K = dYt.rows, Xt.rows
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate needs an existing out tensor")
+        out = torch.empty((G, N, K), dtype=out_dtype, device=dev)
+    ws = _bw_ws(G, dev, workspace)
+    st = status if status is not None else status_tensor(dev)
+    a, b = dYt.c(), Xt.c()
+    _ok(_lib.load().bw_grouped_gemm_wgrad(ctypes.byref(a), ctypes.byref(b), _ptr(m_splits), G,
+                                          total_rows, _ptr(out), _OUT[out.dtype],
+                                          1 if accumulate else 0, _ptr(ws), ws.numel(), _ptr(st),
+                                          _stream(dev)), "bw_grouped_gemm_wgrad")
     if check:
         check_status(st)
     return out

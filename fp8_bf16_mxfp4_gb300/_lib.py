@@ -34,6 +34,20 @@ class MxOperandC(ctypes.Structure):
     ]
 
 
+class BwOperandC(ctypes.Structure):
+    """Mirror of ``mxg_bw_operand``."""
+    _fields_ = [
+        ("data", c_vp),
+        ("scale", c_vp),
+        ("rows", c_i64),
+        ("cols", c_i64),
+        ("ld", c_i64),
+        ("scale_ld", c_i64),
+        ("reserved0", c_i32),
+        ("reserved1", c_i32),
+    ]
+
+
 # name -> (restype, argtypes); exactly the functions declared in include/mxg.h
 SIGNATURES = {
     "mx_quantize_rowwise": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp]),
@@ -54,6 +68,22 @@ SIGNATURES = {
         c_i32, [ctypes.POINTER(MxOperandC), ctypes.POINTER(MxOperandC), c_vp, c_i32, c_i64, c_vp,
                 c_i64, c_i32, c_vp, c_vp]),
     "mxg_gemm_workspace_size": (c_size, [c_i32, c_i32, c_i64, c_i64, c_i64, c_i32]),
+    "bw_quantize_1x128": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_vp, c_i64, c_vp]),
+    "bw_quantize_128x128": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i64, c_vp, c_vp, c_i64, c_vp,
+                                    c_vp]),
+    "bw_quantize_colwise_padded": (
+        c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_vp, c_i64, c_vp, c_i64, c_i64, c_vp, c_vp,
+                c_vp]),
+    "bw_grouped_gemm_fwd": (
+        c_i32, [ctypes.POINTER(BwOperandC), ctypes.POINTER(BwOperandC), c_vp, c_i32, c_i64, c_vp,
+                c_i64, c_i32, c_vp, c_size, c_vp, c_vp]),
+    "bw_grouped_gemm_dgrad": (
+        c_i32, [ctypes.POINTER(BwOperandC), ctypes.POINTER(BwOperandC), c_vp, c_i32, c_vp, c_i64,
+                c_i32, c_vp, c_size, c_vp, c_vp]),
+    "bw_grouped_gemm_wgrad": (
+        c_i32, [ctypes.POINTER(BwOperandC), ctypes.POINTER(BwOperandC), c_vp, c_i32, c_i64, c_vp,
+                c_i32, c_i32, c_vp, c_size, c_vp, c_vp]),
+    "bw_gemm_workspace_size": (c_size, [c_i32]),
     "mxg_check_status": (c_i32, [c_vp, c_vp]),
     "mxg_status_string": (ctypes.c_char_p, [c_i32]),
     "mxg_set_wait_timeout_ns": (None, [c_u64]),

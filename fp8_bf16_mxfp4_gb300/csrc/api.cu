@@ -116,6 +116,40 @@ mxg_status check_out(const void* out, int64_t rows, int64_t ld_out, int64_t ncol
   return MXG_OK;
 }
 
+// Host checks of one blockwise operand (rows may be 0; cols a multiple of
+// 128, 0 only where allowed).
+mxg_status check_bw_operand(const mxg_bw_operand* op, bool allow_no_cols = false) {
+  if (op == nullptr) return MXG_ERR_NULL;
+  if (op->reserved0 != 0 || op->reserved1 != 0) return MXG_ERR_UNSUPPORTED;
+  if (op->rows < 0 || op->cols < 0 || op->cols % 128 != 0) return MXG_ERR_SHAPE;
+  if (op->cols == 0 && !allow_no_cols) return MXG_ERR_SHAPE;
+  if (op->ld < op->cols || op->ld % 16 != 0 || op->scale_ld < 0) return op->ld % 16 ? MXG_ERR_ALIGN : MXG_ERR_SHAPE;
+  if (op->rows == 0 || op->cols == 0) return MXG_OK;
+  if (op->data == nullptr || op->scale == nullptr) return MXG_ERR_NULL;
+  if (!aligned16(op->data) || !aligned(op->scale, 4)) return MXG_ERR_ALIGN;
+  return MXG_OK;
+}
+
+BwGemmArgs bw_args(int pass, int G, const mxg_bw_operand* A, const mxg_bw_operand* B,
+                   const int32_t* splits, int64_t S, int64_t N, int64_t K, void* out,
+                   int64_t ld_out, int32_t dtype, int acc, void* ws, int32_t* st) {
+  BwGemmArgs a{};
+  a.pass = pass;
+  a.G = G;
+  a.a_data = static_cast<const uint8_t*>(A->data); a.a_ld = A->ld;
+  a.a_scale = A->scale; a.a_scale_ld = A->scale_ld;
+  a.a_rows = A->rows; a.a_cols = A->cols;
+  a.b_data = static_cast<const uint8_t*>(B->data); a.b_ld = B->ld;
+  a.b_scale = B->scale; a.b_scale_ld = B->scale_ld;
+  a.b_rows = B->rows; a.b_cols = B->cols;
+  a.splits = splits;
+  a.total_rows = S;
+  a.N = N; a.K = K;
+  a.out = out; a.ld_out = ld_out; a.out_dtype = dtype; a.accumulate = acc;
+  a.ws = ws; a.status = st;
+  return a;
+}
+
 }  // namespace
 }  // namespace mxg
 
@@ -342,6 +376,154 @@ mxg_status grouped_gemm_wgrad(const mxg_mx_operand* dYt, const mxg_mx_operand* X
   a.out = out; a.ld_out = K; a.out_dtype = out_dtype; a.accumulate = accumulate ? 1 : 0;
   a.ws = ws; a.ws_bytes = ws_bytes; a.status = d_status;
   return launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), sms);
+}
+
+
+// ------------------------------------------------------------------ blockwise FP8
+
+mxg_status bw_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
+                             int64_t ld_q, float* s, int64_t ld_s, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 128 != 0) return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < cols || ld_s < rows) return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 8 != 0) return MXG_ERR_ALIGN;
+  if (rows == 0) return MXG_OK;
+  if (x == nullptr || q == nullptr || s == nullptr) return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned(q, 8) || !aligned(s, 4)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, q, s}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_bw_rowwise(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+                                       static_cast<cudaStream_t>(stream), sms));
+}
+
+mxg_status bw_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w, void* q,
+                               int64_t ld_q, float* s, void* qT, int64_t ld_qT, float* sT,
+                               void* stream) {
+  if ((qT == nullptr) != (sT == nullptr)) return MXG_ERR_NULL;
+  if (rows < 0 || cols <= 0 || rows % 128 != 0 || cols % 128 != 0) return MXG_ERR_SHAPE;
+  if (ld_w < cols || ld_q < cols || (qT != nullptr && ld_qT < rows)) return MXG_ERR_SHAPE;
+  if (rows / 128 > 65535 || cols / 128 > 0x7FFFFFFF) return MXG_ERR_SHAPE;
+  if (ld_w % 8 != 0 || ld_q % 16 != 0 || (qT != nullptr && ld_qT % 16 != 0)) return MXG_ERR_ALIGN;
+  if (rows == 0) return MXG_OK;
+  if (w == nullptr || q == nullptr || s == nullptr) return MXG_ERR_NULL;
+  if (!aligned16(w) || !aligned16(q) || !aligned16(qT) || !aligned(s, 4) || !aligned(sT, 4))
+    return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({w, q, s, qT, sT}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_bw_weight(w, rows, cols, ld_w, q, ld_q, s, qT, ld_qT, sT,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+mxg_status bw_quantize_colwise_padded(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                      const int32_t* d_m_splits, int32_t G, void* qT,
+                                      int64_t ld_q, float* sT, int64_t ld_s, int64_t capacity,
+                                      int64_t* d_pad_offsets, int32_t* d_status, void* stream) {
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0 || capacity < 0 || capacity % 128 != 0)
+    return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < capacity || ld_s < cols) return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 16 != 0) return MXG_ERR_ALIGN;
+  if ((rows > 0 && x == nullptr) || (capacity > 0 && (qT == nullptr || sT == nullptr)))
+    return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned16(qT) || !aligned(sT, 4) || !aligned(d_pad_offsets, 8))
+    return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, d_m_splits, qT, sT, d_pad_offsets, d_status}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_bw_colwise(x, rows, cols, ld_x, d_m_splits, G, qT, ld_q, sT, ld_s,
+                                       capacity, d_pad_offsets, d_status,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t bw_gemm_workspace_size(int32_t G) {
+  if (G < 1 || G > kMaxExperts) return 0;
+  return bw_gemm_workspace_bytes(G);
+}
+
+mxg_status bw_grouped_gemm_fwd(const mxg_bw_operand* A, const mxg_bw_operand* W,
+                               const int32_t* d_m_splits, int32_t G, int64_t N, void* out,
+                               int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
+                               int32_t* d_status, void* stream) {
+  mxg_status st;
+  if ((st = check_bw_operand(A)) != MXG_OK || (st = check_bw_operand(W)) != MXG_OK) return st;
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (G < 1 || G > kMaxExperts || N <= 0 || N % 128 != 0) return MXG_ERR_SHAPE;
+  if ((st = check_out(out, A->rows, ld_out, N, out_dtype)) != MXG_OK) return st;
+  if (A->cols != W->cols || W->rows != (int64_t)G * N) return MXG_ERR_SHAPE;
+  if (A->scale_ld < A->rows || W->scale_ld < W->cols / 128) return MXG_ERR_SHAPE;
+  if (ws_bytes < bw_gemm_workspace_bytes(G) || ws == nullptr) return MXG_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if ((st = check_device({A->data, A->scale, W->data, W->scale, d_m_splits, out, ws, d_status},
+                         &dev, &sms)) != MXG_OK)
+    return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return launch_grouped_bw_gemm(bw_args(MXG_PASS_FWD, G, A, W, d_m_splits, A->rows, N, A->cols,
+                                        out, ld_out, out_dtype, 0, ws, d_status),
+                                static_cast<cudaStream_t>(stream), sms);
+}
+
+mxg_status bw_grouped_gemm_dgrad(const mxg_bw_operand* dY, const mxg_bw_operand* Wt,
+                                 const int32_t* d_m_splits, int32_t G, void* out, int64_t ld_out,
+                                 int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* d_status,
+                                 void* stream) {
+  mxg_status st;
+  if ((st = check_bw_operand(dY)) != MXG_OK || (st = check_bw_operand(Wt)) != MXG_OK) return st;
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  const int64_t N = dY->cols, K = Wt->rows;
+  if (K <= 0 || K % 128 != 0 || Wt->cols != (int64_t)G * N) return MXG_ERR_SHAPE;
+  if ((st = check_out(out, dY->rows, ld_out, K, out_dtype)) != MXG_OK) return st;
+  if (dY->scale_ld < dY->rows || Wt->scale_ld < Wt->cols / 128) return MXG_ERR_SHAPE;
+  if (ws_bytes < bw_gemm_workspace_bytes(G) || ws == nullptr) return MXG_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if ((st = check_device({dY->data, dY->scale, Wt->data, Wt->scale, d_m_splits, out, ws, d_status},
+                         &dev, &sms)) != MXG_OK)
+    return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return launch_grouped_bw_gemm(bw_args(MXG_PASS_DGRAD, G, dY, Wt, d_m_splits, dY->rows, N, K,
+                                        out, ld_out, out_dtype, 0, ws, d_status),
+                                static_cast<cudaStream_t>(stream), sms);
+}
+
+mxg_status bw_grouped_gemm_wgrad(const mxg_bw_operand* dYt, const mxg_bw_operand* Xt,
+                                 const int32_t* d_m_splits, int32_t G, int64_t total_rows,
+                                 void* out, int32_t out_dtype, int32_t accumulate, void* ws,
+                                 size_t ws_bytes, int32_t* d_status, void* stream) {
+  mxg_status st;
+  if ((st = check_bw_operand(dYt, true)) != MXG_OK || (st = check_bw_operand(Xt, true)) != MXG_OK)
+    return st;
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (G < 1 || G > kMaxExperts || total_rows < 0) return MXG_ERR_SHAPE;
+  const int64_t N = dYt->rows, K = Xt->rows;
+  if (N <= 0 || K <= 0 || N % 128 != 0 || K % 128 != 0 || dYt->cols != Xt->cols) return MXG_ERR_SHAPE;
+  if ((st = check_out(out, 1, K, K, out_dtype)) != MXG_OK) return st;
+  if (accumulate && out_dtype != MXG_OUT_F32) return MXG_ERR_UNSUPPORTED;
+  if (dYt->scale_ld < N || Xt->scale_ld < K) return MXG_ERR_SHAPE;
+  if (Xt->cols > 0 && (!aligned16(Xt->scale) || Xt->scale_ld % 4 != 0)) return MXG_ERR_ALIGN;
+  if (ws_bytes < bw_gemm_workspace_bytes(G) || ws == nullptr) return MXG_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  if ((st = check_device({dYt->data, dYt->scale, Xt->data, Xt->scale, d_m_splits, out, ws,
+                          d_status},
+                         &dev, &sms)) != MXG_OK)
+    return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return launch_grouped_bw_gemm(bw_args(MXG_PASS_WGRAD, G, dYt, Xt, d_m_splits, total_rows, N, K,
+                                        out, K, out_dtype, accumulate ? 1 : 0, ws, d_status),
+                                static_cast<cudaStream_t>(stream), sms);
 }
 
 }  // extern "C"

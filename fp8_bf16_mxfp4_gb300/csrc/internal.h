@@ -20,6 +20,17 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
                               int64_t ld_q, uint8_t* sT, int64_t ld_s, int64_t capacity,
                               int64_t* pad_offsets, int32_t* status, cudaStream_t stream);
 
+cudaError_t launch_bw_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
+                              int64_t ld_q, float* s, int64_t ld_s, cudaStream_t stream,
+                              int num_sms);
+cudaError_t launch_bw_weight(const void* w, int64_t rows, int64_t K, int64_t ld_w, void* q,
+                             int64_t ld_q, float* s, void* qT, int64_t ld_qT, float* sT,
+                             cudaStream_t stream);
+cudaError_t launch_bw_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                              const int32_t* splits, int G, void* qT, int64_t ld_q, float* sT,
+                              int64_t ld_s, int64_t capacity, int64_t* pad_offsets,
+                              int32_t* status, cudaStream_t stream);
+
 // Grouped MX GEMM (tcgen05 block-scaled).  See gemm_mx.cu.
 struct GemmArgs {
   int pass;  // mxg_pass
@@ -52,5 +63,33 @@ struct GemmArgs {
 
 size_t gemm_workspace_bytes(int pass, int G, int64_t S, int64_t N, int64_t K, int pad);
 mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_sms);
+
+// Grouped blockwise-FP8 GEMM.  See gemm_bw.cu.
+struct BwGemmArgs {
+  int pass;
+  int G;
+  const uint8_t* a_data;
+  int64_t a_ld;
+  const float* a_scale;  // activation-type: (row, kb) at a_scale[kb * a_scale_ld + row]
+  int64_t a_scale_ld;
+  int64_t a_rows, a_cols;
+  const uint8_t* b_data;
+  int64_t b_ld;
+  const float* b_scale;  // fwd/dgrad: 128x128 at [rb * ld + kb]; wgrad: activation-type
+  int64_t b_scale_ld;
+  int64_t b_rows, b_cols;
+  const int32_t* splits;
+  int64_t total_rows;
+  int64_t N, K;
+  void* out;
+  int64_t ld_out;
+  int out_dtype;
+  int accumulate;
+  void* ws;
+  int32_t* status;
+};
+
+size_t bw_gemm_workspace_bytes(int G);
+mxg_status launch_grouped_bw_gemm(const BwGemmArgs& a, cudaStream_t stream, int num_sms);
 
 }  // namespace mxg

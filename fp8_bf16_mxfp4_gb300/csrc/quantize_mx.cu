@@ -242,6 +242,179 @@ __global__ void __launch_bounds__(kColThreads) mx_colwise_kernel(
   if (sc[1] != 0xFF) srow[1] = sc[1];
 }
 
+// ---------------------------------------------------------------------------
+// Blockwise FP8 ("Add ROCm Triton blockwise FP8 grouped GEMM", PR #716):
+// a = max(amax, 1e-4f), s = a / 448 (fp32, IEEE division), q = RNE_satfinite_
+// E4M3(x / s) with x / s an IEEE fp32 division; s is the dequant scale.
+// Activation-type scales are stored block-column-major: scale of (row r,
+// 128-block kb) at s[kb * ld_s + r], so a GEMM epilogue thread holding row r
+// reads its scales with coalesced loads.
+// ---------------------------------------------------------------------------
+constexpr float kBwAmaxFloor = 1e-4f;
+
+MXG_DEVINL float bw_scale(uint32_t amax_bits) {
+  const float a = fmaxf(__uint_as_float(amax_bits << 16), kBwAmaxFloor);
+  return __fdiv_rn(a, 448.0f);
+}
+
+// 8 bf16 (four words) / s -> 8 E4M3 codes (two words).
+MXG_DEVINL void bw_quantize8(const uint32_t* w, float s, uint32_t* o) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __fdiv_rn(bf16lo_to_f32(w[i]), s);
+    v[2 * i + 1] = __fdiv_rn(bf16hi_to_f32(w[i]), s);
+  }
+  o[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]);
+  o[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]);
+}
+
+// 1x128 along the row: 16 lanes per block, 8 values (16 bytes) per lane.
+__global__ void __launch_bounds__(kRowThreads) bw_rowwise_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
+    uint8_t* __restrict__ q, int64_t ld_q, float* __restrict__ s, int64_t ld_s) {
+  const int64_t chunks_per_row = cols >> 3;
+  const int64_t total = rows * chunks_per_row;
+  const int64_t step = (int64_t)gridDim.x * kRowThreads;
+  for (int64_t base = (int64_t)blockIdx.x * kRowThreads; base < total; base += step) {
+    const int64_t t = base + threadIdx.x;
+    const bool live = t < total;
+    const int64_t r = live ? t / chunks_per_row : 0;
+    const int64_t c8 = live ? t - r * chunks_per_row : 0;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (live) raw = __ldcs(reinterpret_cast<const uint4*>(x + r * ld_x + c8 * 8));
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t am = max(max(bf16x2_absmax_bits(w[0]), bf16x2_absmax_bits(w[1])),
+                      max(bf16x2_absmax_bits(w[2]), bf16x2_absmax_bits(w[3])));
+#pragma unroll
+    for (int d = 1; d < 16; d <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
+    if (!live) continue;
+    const float sc = bw_scale(am);
+    uint32_t o[2];
+    bw_quantize8(w, sc, o);
+    *reinterpret_cast<uint2*>(q + r * ld_q + c8 * 8) = make_uint2(o[0], o[1]);
+    if ((threadIdx.x & 15) == 0) s[(c8 >> 4) * ld_s + r] = sc;
+  }
+}
+
+// 128x128 weight tiles: one CTA of 256 threads per tile; thread t holds row
+// t/2, 64 columns.  Optionally writes the transposed codes (dgrad copy).
+constexpr int kBwTile = 128;
+__global__ void __launch_bounds__(256) bw_weight_kernel(
+    const uint16_t* __restrict__ w, int64_t rows, int64_t K, int64_t ld_w, uint8_t* __restrict__ q,
+    int64_t ld_q, float* __restrict__ s, uint8_t* __restrict__ qT, int64_t ld_qT,
+    float* __restrict__ sT) {
+  __shared__ uint32_t warp_max[8];
+  __shared__ float s_tile;
+  __shared__ __align__(16) uint8_t codes[kBwTile][kBwTile + 16];
+  const int kb = blockIdx.x, rb = blockIdx.y;
+  const int t = threadIdx.x, r = t >> 1, h = t & 1;
+  const uint4* src = reinterpret_cast<const uint4*>(w + ((int64_t)rb * kBwTile + r) * ld_w +
+                                                    (int64_t)kb * kBwTile + h * 64);
+  uint32_t v[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 u = __ldcs(src + i);
+    v[4 * i] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
+  }
+  uint32_t am = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) am = max(am, bf16x2_absmax_bits(v[i]));
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
+  if ((t & 31) == 0) warp_max[t >> 5] = am;
+  __syncthreads();
+  if (t == 0) {
+    uint32_t m = 0;
+    for (int i = 0; i < 8; ++i) m = max(m, warp_max[i]);
+    const float sc = bw_scale(m);
+    s_tile = sc;
+    s[(int64_t)rb * (K / kBwTile) + kb] = sc;
+    if (sT != nullptr) sT[(int64_t)kb * (rows / kBwTile) + rb] = sc;
+  }
+  __syncthreads();
+  const float sc = s_tile;
+  uint32_t o[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) bw_quantize8(&v[4 * i], sc, &o[2 * i]);
+  uint4* dst = reinterpret_cast<uint4*>(q + ((int64_t)rb * kBwTile + r) * ld_q + (int64_t)kb * kBwTile + h * 64);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  if (qT == nullptr) return;
+  uint4* crow = reinterpret_cast<uint4*>(&codes[r][h * 64]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) crow[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  __syncthreads();
+  // transposed: thread t writes row k = t/2 of the [K, rows] copy, 64 codes
+  const int k = t >> 1;
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int j = h * 64 + 4 * i;
+    pk[i] = (uint32_t)codes[j][k] | ((uint32_t)codes[j + 1][k] << 8) |
+            ((uint32_t)codes[j + 2][k] << 16) | ((uint32_t)codes[j + 3][k] << 24);
+  }
+  uint4* tdst = reinterpret_cast<uint4*>(qT + ((int64_t)kb * kBwTile + k) * ld_qT + (int64_t)rb * kBwTile + h * 64);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tdst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+// Column-wise, segment-padded to 128 (the variable-K wgrad operand): one CTA
+// per (128 padded token positions = one block, 128 columns); thread t owns
+// column t%128 and tokens [64*(t/128), +64).
+__global__ void __launch_bounds__(kColThreads) bw_colwise_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
+    const int32_t* __restrict__ splits, int G, uint8_t* __restrict__ qT, int64_t ld_q,
+    float* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
+    int32_t* status) {
+  __shared__ SegTable tab;
+  __shared__ __align__(16) uint16_t tile[kColTokens][kColCols + 8];
+  __shared__ uint32_t half_max[kColThreads];
+  const bool first = blockIdx.x == 0 && blockIdx.y == 0;
+  if (!build_seg_table(tab, splits, G, rows, kBwTile, capacity, status, first)) return;
+  if (first && pad_offsets != nullptr) {
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) pad_offsets[g] = tab.poff[g];
+  }
+  const int64_t j0 = (int64_t)blockIdx.x * kColTokens;
+  if (j0 >= tab.poff[G]) return;
+  const int64_t c0 = (int64_t)blockIdx.y * kColCols;
+  const int g = find_segment(tab, G, j0);  // the whole block belongs to one expert
+  const int64_t tok0 = j0 - tab.poff[g];
+  const int64_t mg = tab.off[g + 1] - tab.off[g];
+  for (int idx = threadIdx.x; idx < kColTokens * (kColCols / 8); idx += kColThreads) {
+    const int jr = idx / (kColCols / 8);
+    const int cc = (idx % (kColCols / 8)) * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tok0 + jr < mg && c0 + cc < cols)
+      v = __ldcs(reinterpret_cast<const uint4*>(x + (tab.off[g] + tok0 + jr) * ld_x + c0 + cc));
+    *reinterpret_cast<uint4*>(&tile[jr][cc]) = v;
+  }
+  __syncthreads();
+  const int col = threadIdx.x & (kColCols - 1);
+  const int half = threadIdx.x >> 7;
+  uint32_t w[32];
+  uint32_t am = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t lo = tile[64 * half + 2 * i][col];
+    const uint32_t hi = tile[64 * half + 2 * i + 1][col];
+    w[i] = lo | (hi << 16);
+    am = max(am, bf16x2_absmax_bits(w[i]));
+  }
+  half_max[threadIdx.x] = am;
+  __syncthreads();
+  am = max(am, half_max[threadIdx.x ^ 128]);
+  if (c0 + col >= cols) return;
+  const float sc = bw_scale(am);
+  uint32_t o[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) bw_quantize8(&w[4 * i], sc, &o[2 * i]);
+  uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + col) * ld_q + j0 + 64 * half);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  if (half == 0) sT[(j0 / kBwTile) * ld_s + c0 + col] = sc;
+}
+
 }  // namespace
 
 cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int elem,
@@ -279,6 +452,46 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
   else
     mx_colwise_kernel<MXG_E4M3><<<grid, kColThreads, 0, stream>>>(
         xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mxg
+
+namespace mxg {
+
+cudaError_t launch_bw_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
+                              int64_t ld_q, float* s, int64_t ld_s, cudaStream_t stream,
+                              int num_sms) {
+  const int64_t total = rows * (cols / 8);
+  int64_t blocks = (total + kRowThreads - 1) / kRowThreads;
+  const int64_t cap = (int64_t)num_sms * 8 * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  bw_rowwise_kernel<<<(unsigned)blocks, kRowThreads, 0, stream>>>(
+      static_cast<const uint16_t*>(x), rows, cols, ld_x, static_cast<uint8_t*>(q), ld_q, s, ld_s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bw_weight(const void* w, int64_t rows, int64_t K, int64_t ld_w, void* q,
+                             int64_t ld_q, float* s, void* qT, int64_t ld_qT, float* sT,
+                             cudaStream_t stream) {
+  dim3 grid((unsigned)(K / kBwTile), (unsigned)(rows / kBwTile));
+  bw_weight_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(w), rows, K, ld_w,
+                                             static_cast<uint8_t*>(q), ld_q, s,
+                                             static_cast<uint8_t*>(qT), ld_qT, sT);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bw_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                              const int32_t* splits, int G, void* qT, int64_t ld_q, float* sT,
+                              int64_t ld_s, int64_t capacity, int64_t* pad_offsets,
+                              int32_t* status, cudaStream_t stream) {
+  const int64_t gx = (capacity + kColTokens - 1) / kColTokens;
+  const int64_t gy = (cols + kColCols - 1) / kColCols;
+  dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)gy);
+  bw_colwise_kernel<<<grid, kColThreads, 0, stream>>>(
+      static_cast<const uint16_t*>(x), rows, cols, ld_x, splits, G, static_cast<uint8_t*>(qT), ld_q,
+      sT, ld_s, capacity, pad_offsets, status);
   return cudaGetLastError();
 }
 

@@ -131,6 +131,17 @@ MXG_DEVINL void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t id
       : "memory");
 }
 
+// D(tmem) (+)= A(smem) * B(smem), FP8/FP6/FP4 operands without block scales.
+MXG_DEVINL void mma_f8f6f4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Each thread of the warp reads 32 consecutive 32-bit columns of its lane.
 MXG_DEVINL void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
   asm volatile(

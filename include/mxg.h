@@ -214,6 +214,90 @@ size_t mxg_gemm_workspace_size(int32_t pass, int32_t G, int64_t S, int64_t N, in
                                int32_t pad_multiple);
 
 /* --------------------------------------------------------------------------
+ * Blockwise FP8 (DeepSeek-style; "Add ROCm Triton blockwise FP8 grouped GEMM",
+ * ROCm TransformerEngine PR #716)
+ *
+ * Per block: a = max(amax, 1e-4), s = a / 448 (fp32, correctly rounded), and
+ * each element q = x / s (fp32, correctly rounded) rounded to E4M3 (nearest,
+ * ties to even, saturating at 448).  s is the dequantization scale: x ~= q*s.
+ * Blocks are 1x128 along the contraction for activations / gradients and for
+ * the column-wise wgrad operands, and 128x128 for weights.  All sizes that
+ * are block dimensions must be multiples of 128.
+ *
+ * Scale layouts:
+ *   activation-type (1x128): block-column-major, (row r, block kb) at
+ *                            s[kb * ld_s + r], ld_s >= rows;
+ *   weight-type (128x128):   row-major [rows/128, cols/128], (rb, kb) at
+ *                            s[rb * ld_s + kb].
+ * ------------------------------------------------------------------------ */
+
+/* A blockwise-FP8 operand, K-major: E4M3 codes [rows, cols] (row r at
+ * (uint8*)data + r*ld, ld % 16 == 0) and fp32 scales in the layout the call
+ * states (stride scale_ld floats). */
+typedef struct mxg_bw_operand {
+  const void* data;
+  const float* scale;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;
+  int64_t scale_ld;
+  int32_t reserved0; /* must be 0 */
+  int32_t reserved1; /* must be 0 */
+} mxg_bw_operand;
+
+/* 1x128 row-wise quantization of BF16 x [rows, cols] (ld_x elements, % 8):
+ * codes q [rows, cols] (ld_q bytes, % 8), activation-type scales s
+ * (ld_s >= rows floats).  cols % 128 == 0. */
+mxg_status bw_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
+                             int64_t ld_q, float* s, int64_t ld_s, void* stream);
+
+/* 128x128 quantization of BF16 weights w [rows, cols] (rows = G*N stacked
+ * experts; ld_w elements): codes q [rows, cols] (ld_q bytes), weight-type
+ * scales s [rows/128, cols/128] (contiguous).  When qT and sT are given, also
+ * writes the dgrad copy: the same blocks transposed, codes qT [cols, rows]
+ * (ld_qT bytes) and scales sT [cols/128, rows/128] (contiguous).  rows and
+ * cols multiples of 128; qT and sT both NULL or both set. */
+mxg_status bw_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_t ld_w, void* q,
+                               int64_t ld_q, float* s, void* qT, int64_t ld_qT, float* sT,
+                               void* stream);
+
+/* Column-wise 1x128 quantization along tokens, each expert's segment padded
+ * to a multiple of 128 (the variable-K wgrad operand).  x BF16 [rows, cols]
+ * with experts concatenated; codes qT [cols, capacity] (ld_q bytes, % 16),
+ * activation-type scales sT of the transposed operand: (column c, token
+ * block jb) at sT[jb * ld_s + c], ld_s >= cols.  Columns past the last
+ * expert's padded end are left untouched.  Device errors as for
+ * mx_quantize_colwise_segment_padded. */
+mxg_status bw_quantize_colwise_padded(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                      const int32_t* d_m_splits, int32_t G, void* qT,
+                                      int64_t ld_q, float* sT, int64_t ld_s, int64_t capacity,
+                                      int64_t* d_pad_offsets, int32_t* d_status, void* stream);
+
+/* Grouped blockwise-FP8 GEMMs (tcgen05 kind::f8f6f4 + per-128-K promotion in
+ * fp32).  Same passes, split validation and output conventions as the MX
+ * GEMMs; N and K multiples of 128; the wgrad padding is 128.
+ *   fwd:   A [S, K] activation-type scales; W [G*N, K] weight-type scales.
+ *   dgrad: dY [S, N] activation-type; Wt [K, G*N] weight-type (the dgrad copy
+ *          from bw_quantize_128x128).
+ *   wgrad: dYt [N, capacity], Xt [K, capacity] from bw_quantize_colwise_padded
+ *          (activation-type scales; Xt's scale pointer 16-byte aligned and its
+ *          scale_ld a multiple of 4).
+ * ws: at least bw_gemm_workspace_size(G) bytes, 256-byte aligned. */
+mxg_status bw_grouped_gemm_fwd(const mxg_bw_operand* A, const mxg_bw_operand* W,
+                               const int32_t* d_m_splits, int32_t G, int64_t N, void* out,
+                               int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
+                               int32_t* d_status, void* stream);
+mxg_status bw_grouped_gemm_dgrad(const mxg_bw_operand* dY, const mxg_bw_operand* Wt,
+                                 const int32_t* d_m_splits, int32_t G, void* out, int64_t ld_out,
+                                 int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* d_status,
+                                 void* stream);
+mxg_status bw_grouped_gemm_wgrad(const mxg_bw_operand* dYt, const mxg_bw_operand* Xt,
+                                 const int32_t* d_m_splits, int32_t G, int64_t total_rows,
+                                 void* out, int32_t out_dtype, int32_t accumulate, void* ws,
+                                 size_t ws_bytes, int32_t* d_status, void* stream);
+size_t bw_gemm_workspace_size(int32_t G);
+
+/* --------------------------------------------------------------------------
  * Status and configuration
  * ------------------------------------------------------------------------ */
 

@@ -1,0 +1,171 @@
+"""Blockwise FP8 on the GPU vs the oracle: quantizers bit-exact (codes and
+fp32 scales), grouped GEMMs within |gpu - ref| <= 2^-8 |ref| + 1e-4 rms(ref)
+on oracle-quantized operands.
+
+Layout notes: the library stores activation-type scales block-column-major
+([cols/128, rows]); the oracle returns them [rows, cols/128], so the tests
+transpose.  The dgrad weight copy is [K, G*N] (experts side by side)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.blockwise import transpose_bw_128x128
+import synth
+
+pytestmark = pytest.mark.gpu
+
+from gpu_util import bf16_to_dev, i32_to_dev  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _mxg():
+    import fp8_bf16_mxfp4_gb300 as mxg
+    return mxg
+
+
+def _f32_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda:0")
+
+
+def _u8_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).to("cuda:0")
+
+
+@pytest.mark.parametrize("shape", [(1, 128), (37, 384), (1000, 4096)])
+def test_bw_1x128_bit_exact(shape):
+    rng = np.random.default_rng(shape[0])
+    x = synth.normal_bf16(rng, shape, std=2.0, outlier_frac=0.02)
+    if shape[0] > 4:
+        v = synth.bf16_bits_to_f32(x)
+        x[1] = synth.f32_to_bf16_bits(v[1] * np.float32(1e-7))   # below the 1e-4 amax floor
+        x[2, :128] = 0                                           # a zero block
+        x[3, :128] = synth.f32_to_bf16_bits(np.full(128, -2.0, np.float32))
+    op = _mxg().bw_quantize_1x128(bf16_to_dev(x))
+    torch.cuda.synchronize()
+    codes, s = oracle.quantize_bw_1x128(x)
+    assert np.array_equal(op.data.cpu().numpy(), codes)
+    assert np.array_equal(op.scale.cpu().numpy(), s.T)
+
+
+def test_bw_128x128_and_dgrad_copy_bit_exact():
+    rng = np.random.default_rng(3)
+    G, N, K = 2, 256, 384
+    w = synth.normal_bf16(rng, (G * N, K), outlier_frac=0.02)
+    op, opT = _mxg().bw_quantize_128x128(bf16_to_dev(w))
+    torch.cuda.synchronize()
+    codes, s = oracle.quantize_bw_128x128(w.reshape(G, N, K))
+    assert np.array_equal(op.data.cpu().numpy(), codes.reshape(G * N, K))
+    assert np.array_equal(op.scale.cpu().numpy(), s.reshape(G * N // 128, K // 128))
+    ct, st = transpose_bw_128x128(codes, s)
+    assert np.array_equal(opT.data.cpu().numpy(), np.concatenate(list(ct), axis=1))
+    assert np.array_equal(opT.scale.cpu().numpy(), np.concatenate(list(st), axis=1))
+
+
+@pytest.mark.parametrize("splits,cols", [([200, 0, 1, 128, 55], 128), ([0, 0, 300], 256),
+                                         ([1, 2, 3, 4], 160)])
+def test_bw_colwise_padded_bit_exact(splits, cols):
+    rng = np.random.default_rng(len(splits) + cols)
+    splits = np.array(splits, dtype=np.int32)
+    x = synth.normal_bf16(rng, (int(splits.sum()), cols), std=3.0, outlier_frac=0.02)
+    op, poff = _mxg().bw_quantize_colwise_padded(bf16_to_dev(x), i32_to_dev(splits), check=True)
+    codes, s, p = oracle.quantize_bw_colwise_padded(x, splits)
+    spad = int(p[-1])
+    assert np.array_equal(poff.cpu().numpy(), p)
+    assert np.array_equal(op.data.cpu().numpy()[:, :spad], codes)
+    assert np.array_equal(op.scale.cpu().numpy()[: spad // 128], s.T)
+
+
+# ------------------------------------------------------------------------------ GEMMs
+
+def _act_operand(bits):
+    """Oracle 1x128 quantization -> (device operand, dequantized float64)."""
+    codes, s = oracle.quantize_bw_1x128(bits)
+    return _mxg().BWOperand(_u8_dev(codes), _f32_dev(s.T)), oracle.dequantize_bw_1x128(codes, s)
+
+
+@pytest.mark.parametrize("splits,N,K", [([0, 130, 1, 300], 256, 384), ([512], 128, 128),
+                                        ([64, 64], 384, 1024)])
+def test_bw_fwd_parity(splits, N, K):
+    mxg = _mxg()
+    splits = np.asarray(splits, dtype=np.int32)
+    G, S = len(splits), int(splits.sum())
+    rng = np.random.default_rng(N + K)
+    x = synth.normal_bf16(rng, (S, K), outlier_frac=0.01)
+    w = synth.normal_bf16(rng, (G * N, K), outlier_frac=0.01)
+    A, Ad = _act_operand(x)
+    wc, ws = oracle.quantize_bw_128x128(w.reshape(G, N, K))
+    W = mxg.BWOperand(_u8_dev(wc.reshape(G * N, K)), _f32_dev(ws.reshape(G * N // 128, K // 128)))
+    Wd = oracle.dequantize_bw_128x128(wc, ws).reshape(G * N, K)
+    Y = mxg.bw_grouped_gemm_fwd(A, W, i32_to_dev(splits), N, check=True)
+    oracle.assert_gemm_close(Y.float().cpu().numpy(), oracle.grouped_fwd(Ad, Wd, splits, N), "bw fwd")
+
+
+@pytest.mark.parametrize("splits,N,K", [([0, 77, 300], 256, 384), ([128], 128, 256)])
+def test_bw_dgrad_parity(splits, N, K):
+    mxg = _mxg()
+    splits = np.asarray(splits, dtype=np.int32)
+    G, S = len(splits), int(splits.sum())
+    rng = np.random.default_rng(N * 3 + K)
+    dy = synth.normal_bf16(rng, (S, N), outlier_frac=0.01)
+    w = synth.normal_bf16(rng, (G * N, K), outlier_frac=0.01)
+    dY, dYd = _act_operand(dy)
+    wc, ws = oracle.quantize_bw_128x128(w.reshape(G, N, K))
+    ct, st = transpose_bw_128x128(wc, ws)
+    Wt = mxg.BWOperand(_u8_dev(np.concatenate(list(ct), axis=1)), _f32_dev(np.concatenate(list(st), axis=1)))
+    Wtd = np.concatenate(list(oracle.dequantize_bw_128x128(ct, st)), axis=1)
+    dX = mxg.bw_grouped_gemm_dgrad(dY, Wt, i32_to_dev(splits), check=True)
+    oracle.assert_gemm_close(dX.float().cpu().numpy(), oracle.grouped_dgrad(dYd, Wtd, splits), "bw dgrad")
+
+
+def _col_operand(bits, splits, capacity):
+    codes, s, poff = oracle.quantize_bw_colwise_padded(bits, splits)
+    C, spad = codes.shape
+    rng = np.random.default_rng(5)
+    full = rng.integers(0, 0x77, size=(C, capacity)).astype(np.uint8)   # finite junk slack
+    full[:, :spad] = codes
+    fs = np.full((capacity // 128, C), 7.0, dtype=np.float32)
+    fs[: spad // 128] = s.T
+    deq = codes.astype(np.float64)
+    deq = oracle.dequantize_bw_1x128(codes, s)
+    return _mxg().BWOperand(_u8_dev(full), _f32_dev(fs)), deq, poff
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_bw_wgrad_parity(accumulate):
+    mxg = _mxg()
+    splits = np.array([200, 0, 1, 300, 129], dtype=np.int32)
+    G, S, N, K = len(splits), int(splits.sum()), 256, 384
+    rng = np.random.default_rng(11 + accumulate)
+    dy = synth.normal_bf16(rng, (S, N), outlier_frac=0.01)
+    x = synth.normal_bf16(rng, (S, K), outlier_frac=0.01)
+    cap = synth.padded_rows_capacity(S, G, 128)
+    dYt, dYtd, poff = _col_operand(dy, splits, cap)
+    Xt, Xtd, _ = _col_operand(x, splits, cap)
+    init = (rng.standard_normal((G, N, K)) * 1e-3).astype(np.float32)
+    out = torch.from_numpy(init.copy()).to("cuda:0")
+    mxg.bw_grouped_gemm_wgrad(dYt, Xt, i32_to_dev(splits), S, out=out, accumulate=accumulate, check=True)
+    ref = oracle.grouped_wgrad(dYtd, Xtd, poff, out_init=init if accumulate else None)
+    got = out.cpu().numpy()
+    oracle.assert_gemm_close(got, ref, f"bw wgrad acc={accumulate}")
+    assert np.array_equal(got[1], init[1] if accumulate else np.zeros_like(init[1]))
+
+
+def test_bw_gemm_rejects_bad_splits():
+    mxg = _mxg()
+    rng = np.random.default_rng(2)
+    A, _ = _act_operand(synth.normal_bf16(rng, (128, 128)))
+    wc, ws = oracle.quantize_bw_128x128(synth.normal_bf16(rng, (256, 128)).reshape(2, 128, 128))
+    W = mxg.BWOperand(_u8_dev(wc.reshape(256, 128)), _f32_dev(ws.reshape(2, 1)))
+    out = torch.full((128, 128), 5.0, dtype=torch.bfloat16, device="cuda:0")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    mxg.bw_grouped_gemm_fwd(A, W, i32_to_dev([130, -2]), 128, out=out, status=st)
+    with pytest.raises(mxg.MXGError) as ei:
+        mxg.check_status(st)
+    assert ei.value.code == 4 and (out == 5.0).all()
