@@ -21,15 +21,22 @@
 //      per (row tile, 128-element k chunk) with every expert's rows (or k
 //      range) starting on a fresh chunk -- the "scale packing" step that the
 //      HipKittens grouped MXFP8 kernel (PR #661) also performs.
-//   3. the persistent GEMM kernel, one CTA per SM, 192 threads:
+//   3. the persistent GEMM kernel, one CTA per SM, 320 threads:
 //        warp 0    TMA producer: A/B data tiles (128-byte swizzle) and scale
 //                  chunks into a 4-stage shared-memory ring (mbarriers);
-//        warp 1    TMEM owner and MMA issuer (one thread): tcgen05.cp of the
-//                  stage's scales into TMEM, 4 tcgen05.mma per stage
-//                  (kind::mxf4 for MXFP4, kind::mxf8f6f4 for MXFP8 / a8w4)
-//                  accumulating a 128x256 fp32 tile in TMEM;
+//        warp 1    TMEM owner and MMA issuer (one thread): 4 tcgen05.mma per
+//                  stage (kind::mxf4 for MXFP4, kind::mxf8f6f4 for MXFP8 /
+//                  a8w4) accumulating a 128x256 fp32 tile in TMEM;
 //        warps 2-5 epilogue: tcgen05.ld, fp32 -> BF16/FP32 (optionally +=),
-//                  row/column-masked stores of the expert's valid region.
+//                  row/column-masked stores of the expert's valid region;
+//        warps 6-9 scale feeders, one per 32-lane quarter of TMEM: each
+//                  stage's scale chunks go from shared memory to registers
+//                  and on into that stage's TMEM scale slot (tcgen05.st),
+//                  then the stage is handed to the MMA issuer.
+//      The feeders keep every tcgen05.cp out of the MMA issuer's stream:
+//      measured on GB300, a scale copy issued between MMAs (3 per FP8 stage,
+//      6 per FP4 stage) slowed the MMA stream by a third to two thirds, and
+//      more again when the issuer also waited on an mbarrier.
 //      Tiles (expert, m-tile, n-tile) are enumerated expert-major, n fastest,
 //      and strided over the CTAs.
 #include <cuda.h>
@@ -50,7 +57,7 @@ namespace {
 constexpr int BM = 128;           // tile rows (TMEM lanes)
 constexpr int BN = 256;           // tile columns (TMEM fp32 columns)
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kATileBytes = BM * 128;  // 128 bytes of K per row per stage
 constexpr int kBTileBytes = BN * 128;
 constexpr int kChunkBytes = 512;       // 128 rows x 4 scale bytes
@@ -184,7 +191,7 @@ struct Smem {
   static constexpr int kDataBytes = kStages * kStageBytes;
   static constexpr int kSfOff = kDataBytes;
   static constexpr int kBarOff = kSfOff + kStages * KindCfg<kKind>::kSfBytes;
-  static constexpr int kNumBars = 2 * kStages + 3;  // full, empty, tmem_full, tmem_empty, drain
+  static constexpr int kNumBars = 3 * kStages + 3;  // full, empty, sready, tmem_full, tmem_empty, drain
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem addr, abort flag
   static constexpr int kTabOff = kMiscOff + 16;
   static constexpr int kTabBytes = 5 * (kMaxExperts + 1) * 4;
@@ -247,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sbase + L::kBarOff;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  const uint32_t tmem_full = bar0 + 8u * (2 * kStages);
+  auto sready_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); };  // scales in TMEM
+  const uint32_t tmem_full = bar0 + 8u * (3 * kStages);
   const uint32_t tmem_empty = tmem_full + 8;
   const uint32_t drain_bar = tmem_full + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -257,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
+      ptx::mbar_init(sready_bar(s), 4);
     }
     ptx::mbar_init(tmem_full, 1);
     ptx::mbar_init(tmem_empty, 4);
@@ -354,24 +363,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ptx::mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
         ptx::tc_fence_after();
         const int nk = cdiv_d(e.Kc, Cfg::kStageK);
-        const int nb_rows = min(2, cdiv_d(e.Nn - nt * BN, 128));
         for (int kb = 0; kb < nk; ++kb) {
-          if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          // the stage's data has landed and the feeders have put its scales in TMEM
+          if (!ptx::mbar_wait(sready_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           ptx::tc_fence_after();
           const int rem = e.Kc - kb * Cfg::kStageK;
-          const int kc_valid = min(Cfg::kKPS, cdiv_d(rem, 128));
           const int steps = min(4, cdiv_d(rem, Cfg::kMmaK));
           const uint32_t sA = sbase + stage * L::kStageBytes;
           const uint32_t sB = sA + kATileBytes;
-          const uint32_t sf = sbase + L::kSfOff + stage * Cfg::kSfBytes;
           const uint32_t tsf = tmem + kSfTmemCol0 + stage * Cfg::kSfCols;  // A: kKPS*4 cols, then B
-          for (int c = 0; c < kc_valid; ++c) {
-            ptx::tc_cp_32x128b_warpx4(tsf + 4 * c, ptx::smem_desc(sf + c * kChunkBytes, 0, 128, 0));
-            for (int rr = 0; rr < nb_rows; ++rr)
-              ptx::tc_cp_32x128b_warpx4(
-                  tsf + Cfg::kKPS * 4 + 8 * c + 4 * rr,
-                  ptx::smem_desc(sf + Cfg::kKPS * kChunkBytes + (2 * c + rr) * kChunkBytes, 0, 128, 0));
-          }
           const uint64_t adesc0 = ptx::smem_desc(sA, 16, 1024, 2);
           const uint64_t bdesc0 = ptx::smem_desc(sB, 16, 1024, 2);
           for (int j = 0; j < steps; ++j) {
@@ -401,6 +401,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_wait(drain_bar, 0, &no_abort, p.status, p.drain_ns);
       }
     }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ scale feeders
+    // Shared-memory chunk k of a stage (A chunks first, then B) goes to TMEM
+    // columns 4k..4k+3 of the stage's slot, every lane of this warp's quarter
+    // receiving the 16 bytes that tcgen05.cp 32x128b.warpx4 would have given
+    // it.  Chunks the producer skipped (k tail, short N tile) carry stale
+    // bytes into columns that no MMA of the stage reads.
+    const int quarter = warp & 3;
+    const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + kSfTmemCol0;
+    const uint8_t* sf_lane = smem + L::kSfOff + lane * 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int g, mt, nt;
+      Geo e;
+      locate(tile, g, mt, nt, e);
+      const int nk = cdiv_d(e.Kc, Cfg::kStageK);
+      bool ok = true;
+      for (int kb = 0; kb < nk; ++kb) {
+        const bool landed = ptx::mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
+        const uint8_t* src = sf_lane + stage * Cfg::kSfBytes;
+        const uint32_t dst = tq + stage * Cfg::kSfCols;
+#pragma unroll
+        for (int k = 0; k < 3 * Cfg::kKPS; ++k) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + k * kChunkBytes);
+          ptx::tmem_st_32x32b_x4(dst + 4 * k, v.x, v.y, v.z, v.w);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sready_bar(stage));
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     // BF16: the whole 128x256 tile is read from TMEM into registers (128
@@ -414,7 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g, mt, nt;
       Geo e;
       locate(tile, g, mt, nt, e);
-      if (!ptx::mbar_wait(tmem_full, acc_phase, abort_flag, p.status, p.timeout_ns)) break;
+      const bool ready = ptx::mbar_wait(tmem_full, acc_phase, abort_flag, p.status, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, ready)) break;  // the warp leaves together (.aligned TMEM loads)
       ptx::tc_fence_after();
       const int row = mt * BM + quarter * 32 + lane;
       const bool row_ok = row < e.M;
