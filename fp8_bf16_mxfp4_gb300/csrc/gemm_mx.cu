@@ -87,13 +87,16 @@ struct PackSrc {
   uint8_t* dst;
 };
 
-constexpr int kPackKc = 8;  // k-chunks per CTA
+constexpr int kPackKc = 8;  // k-chunks per CTA (eight 4-byte words per 32-byte row segment)
+static_assert(kPackKc == 8, "the pack kernel maps 8 threads to a row");
 
-// grid = (row tiles, k-chunk groups of kPackKc, operand); one thread per row
-// of the 128-row tile.  The expert is looked up once per CTA (row-segmented
-// operands) or advanced incrementally along the k-chunks (contraction-
-// segmented operands), so the per-chunk work is a few byte loads and one
-// 4-byte store.
+// grid = (row tiles, k-chunk groups of kPackKc, operand), 128 threads.  A CTA
+// repacks one 128-row tile over kPackKc chunks (32 scale bytes per row): the
+// rows are read as 4-byte words, eight threads per row (one chunk each), into
+// a shared-memory tile, and every 512-byte chunk is then written with one
+// coalesced 4-byte store per thread.  Words whose four blocks are not all
+// inside the expert's contraction range, or are not 4-byte aligned, are
+// assembled from byte loads; blocks outside the range are zero.
 __global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, PackSrc sb) {
   const PlanView pv = plan_view(const_cast<int32_t*>(p.plan), p.G);
   if (pv.hdr[0] == 0) return;
@@ -119,24 +122,26 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, 
   const bool kseg = wg || (p.pass == MXG_PASS_DGRAD && !isA);
   __shared__ int32_t pre[kMaxExperts + 1];
   __shared__ int32_t pof[kMaxExperts + 1];
+  __shared__ uint32_t tile[128][kPackKc + 1];
+  const int tid = threadIdx.x;
   if ((isA && !kseg) || wg) {
-    for (int i = threadIdx.x; i <= G; i += blockDim.x) {
+    for (int i = tid; i <= G; i += blockDim.x) {
       pre[i] = wg ? pv.kc[i] : pv.rt[i];
       if (wg) pof[i] = pv.poff[i];
     }
     __syncthreads();
   }
+  // rows of this tile: [row0 + t*128, row0 + min(R, t*128 + 128))
   int t, R;
   int64_t row0;
-  int g = 0;
   if (!kseg) {
     if (isA) {
-      g = find_prefix(pre, G, rt);
+      const int g = find_prefix(pre, G, rt);
       t = rt - pre[g];
       row0 = pv.off[g];
       R = pv.off[g + 1] - pv.off[g];
     } else {  // forward weights: G blocks of N rows
-      g = rt / nrt;
+      const int g = rt / nrt;
       t = rt - g * nrt;
       row0 = (int64_t)g * p.N;
       R = (int)p.N;
@@ -145,40 +150,56 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, 
     t = rt;
     row0 = 0;
     R = (int)(isA ? p.N : p.K);
-    if (wg) g = find_prefix(pre, G, kc0);
   }
-  const int KBrow = (int)((p.pass == MXG_PASS_FWD ? p.K : p.N) / 32);  // row-segmented only
-  const int r = threadIdx.x;
-  const int rr = t * 128 + r;
-  const bool row_ok = rr < R;
-  const uint8_t* srow = ps.src + (row0 + (row_ok ? rr : 0)) * ps.ld;
-  uint8_t* dst = ps.dst + (r & 31) * 16 + (r >> 5) * 4;
-  const int kc_end = min(KC, kc0 + kPackKc);
-  for (int kcg = kc0; kcg < kc_end; ++kcg) {
+  // load phase: thread -> (chunk j = tid % 8, rows tid / 8 + 16 i)
+  const int j = tid & (kPackKc - 1);
+  const int kcg = kc0 + j;
+  int nb = 0;        // valid blocks of the word (0..4)
+  int64_t boff = 0;  // byte offset of the word's first block in the row
+  if (kcg < KC) {
     int c, KB;
     int64_t kb0;
     if (!kseg) {
-      c = kcg; kb0 = 0; KB = KBrow;
+      c = kcg;
+      kb0 = 0;
+      KB = (int)((p.pass == MXG_PASS_FWD ? p.K : p.N) / 32);
     } else if (wg) {
-      while (pre[g + 1] <= kcg) ++g;
+      const int g = find_prefix(pre, G, kcg);
       c = kcg - pre[g];
       kb0 = pof[g] >> 5;
       KB = (pof[g + 1] - pof[g]) >> 5;
     } else {  // dgrad weights: expert g's contraction is columns [g*N, g*N+N)
-      g = kcg / nrt;
+      const int g = kcg / nrt;
       c = kcg - g * nrt;
       kb0 = (int64_t)g * (p.N >> 5);
       KB = (int)(p.N >> 5);
     }
+    nb = max(0, min(4, KB - 4 * c));
+    boff = kb0 + 4 * (int64_t)c;
+  }
+  const bool vec = nb == 4 && ((boff | ps.ld | (int64_t)reinterpret_cast<uintptr_t>(ps.src)) & 3) == 0;
+#pragma unroll 4
+  for (int i = 0; i < 128 / 16; ++i) {
+    const int r = i * 16 + (tid >> 3);
+    const int rr = t * 128 + r;
     uint32_t w = 0;
-    if (row_ok) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int kb = c * 4 + j;
-        if (kb < KB) w |= (uint32_t)__ldg(srow + kb0 + kb) << (8 * j);
+    if (rr < R && nb > 0) {
+      const uint8_t* src = ps.src + (row0 + rr) * ps.ld + boff;
+      if (vec) {
+        w = __ldg(reinterpret_cast<const uint32_t*>(src));
+      } else {
+        for (int b = 0; b < nb; ++b) w |= (uint32_t)__ldg(src + b) << (8 * b);
       }
     }
-    *reinterpret_cast<uint32_t*>(dst + ((int64_t)kcg * RT + rt) * kChunkBytes) = w;
+    tile[r][j] = w;
+  }
+  __syncthreads();
+  // store phase: chunk word tid holds rows 32*(tid%4) + tid/4 (byte (r%32)*16 + (r/32)*4 + block)
+  const int r_of = 32 * (tid & 3) + (tid >> 2);
+  const int kc_n = min(KC - kc0, kPackKc);
+  for (int jj = 0; jj < kc_n; ++jj) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(ps.dst + ((int64_t)(kc0 + jj) * RT + rt) * kChunkBytes);
+    dst[tid] = tile[r_of][jj];
   }
 }
 
