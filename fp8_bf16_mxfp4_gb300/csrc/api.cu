@@ -242,7 +242,7 @@ mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64
   if (!g.ok) return MXG_ERR_CUDA;
   return cuda_status(launch_mx_colwise(x, rows, cols, ld_x, d_m_splits, G, pad_multiple, elem, qT,
                                        ld_q, sT, ld_s, capacity, d_pad_offsets, d_status,
-                                       static_cast<cudaStream_t>(stream)));
+                                       static_cast<cudaStream_t>(stream), sms));
 }
 
 size_t mxg_gemm_workspace_size(int32_t pass, int32_t G, int64_t S, int64_t N, int64_t K,
