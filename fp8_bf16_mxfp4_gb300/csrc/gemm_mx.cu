@@ -219,19 +219,17 @@ struct Smem {
   static constexpr int kTotal = kTabOff + kTabBytes + 1024;  // + alignment slack
 };
 
-// FP32 output: one 32-column chunk of a row, stored (or added) with 32-byte
-// accesses.
+// FP32 output: one 32-column chunk of a row, stored with 32-byte accesses,
+// or added in place with 16-byte reductions at L2 (the thread does not wait
+// for the old values, so the accumulator is released sooner).
 MXG_DEVINL void store_row_chunk_f32(const Params& p, int64_t row, int64_t col, uint32_t* r) {
   float* dst = static_cast<float*>(p.out) + row * p.ld_out + col;
   if (p.accumulate) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t o[8];
-      ptx::ld_global_v8(dst + 8 * i, o);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        r[8 * i + j] = __float_as_uint(__uint_as_float(o[j]) + __uint_as_float(r[8 * i + j]));
-    }
+    for (int i = 0; i < 8; ++i)
+      ptx::red_add_v4_f32(dst + 4 * i, __uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                          __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+    return;
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) ptx::st_global_v8(dst + 8 * i, r + 8 * i);

@@ -179,6 +179,14 @@ MXG_DEVINL void ld_global_v8(const void* p, uint32_t* v) {
                : "memory");
 }
 
+// dst[0..3] += v[0..3] performed at L2 (no value returned to the thread):
+// one fp32 add per element, round to nearest even; subnormal sums are
+// flushed to zero.  dst must be 16-byte aligned.
+MXG_DEVINL void red_add_v4_f32(float* dst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 MXG_DEVINL void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
