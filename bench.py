@@ -342,6 +342,92 @@ class MXFP4Train:
         self.mxg.check_status(self.status)
 
 
+class DenseMXFP4:
+    """Dense MXFP4 per-pass GEMMs (G = 1), the largest point of the sweep:
+    seqlen 2048 x mbs 4 = 8192 tokens, hidden 8192, FFN 28672; fwd and dgrad
+    BF16 out, wgrad FP32 out (no accumulate)."""
+    name = "dense_mxfp4_m8192"
+
+    def __init__(self, dev):
+        import torch
+        import fp8_bf16_mxfp4_gb300 as mxg
+        self.mxg = mxg
+        w = synth.WORKLOADS["dense_mxfp4_m8192"]
+        self.splits = w.splits()
+        self.G, self.N, self.K, self.pad = w.G, w.N, w.K, w.pad
+        self.S = int(self.splits.sum())
+        G, N, K, S = self.G, self.N, self.K, self.S
+        self.x_host = _to_bf16(synth.normal_bf16(w.act_rng(0), (S, K), std=w.std)).pin_memory()
+        self.dy_host = _to_bf16(synth.normal_bf16(w.act_rng(1), (S, N), std=w.std)).pin_memory()
+        self.x = self.x_host.to(dev)
+        self.dy = self.dy_host.to(dev)
+        self.w = _to_bf16(synth.normal_bf16(w.weight_rng(), (N, K), std=w.std)).to(dev)
+        self.splits_host = torch.from_numpy(self.splits).pin_memory()
+        self.d_splits = self.splits_host.to(dev)
+        self.w_splits = torch.full((1,), N, dtype=torch.int32, device=dev)
+        self.cap = mxg.mx_padded_rows_capacity(S, G, self.pad)
+        self.dw = torch.empty((G, N, K), device=dev, dtype=torch.float32)
+        self.y = torch.empty((S, N), dtype=torch.bfloat16, device=dev)
+        self.dx = torch.empty((S, K), dtype=torch.bfloat16, device=dev)
+        self.y_host = torch.empty((S, N), dtype=torch.bfloat16).pin_memory()
+        self.dx_host = torch.empty((S, K), dtype=torch.bfloat16).pin_memory()
+        ws = max(mxg.gemm_workspace_size("fwd", G, S, N, K), mxg.gemm_workspace_size("dgrad", G, S, N, K),
+                 mxg.gemm_workspace_size("wgrad", G, self.cap, N, K, self.pad))
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        f = 2.0 * S * N * K
+        self.flops = 3 * f
+        self.launches_per_step = 6 + 3 * 3   # six quantizers; three GEMM calls of three kernels
+        self.timed = _Timed()
+        self.gemm_info = {p: (f, FP4_OVER_BF16, "mxf4") for p in ("fwd", "dgrad", "wgrad")}
+
+    def step(self, time_gemm=False):
+        mxg, N, pad = self.mxg, self.N, self.pad
+        Xq = mxg.mx_quantize_rowwise(self.x, "e2m1")
+        Wq = mxg.mx_quantize_rowwise(self.w, "e2m1")
+        self.timed.run("fwd", lambda: mxg.grouped_gemm_fwd(Xq, Wq, self.d_splits, N, out=self.y,
+                                                           workspace=self.ws, status=self.status), time_gemm)
+        dYq = mxg.mx_quantize_rowwise(self.dy, "e2m1")
+        Wt, _ = mxg.mx_quantize_colwise_segment_padded(self.w, self.w_splits, 32, "e2m1",
+                                                       capacity=N, status=self.status)
+        self.timed.run("dgrad", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx,
+                                                               workspace=self.ws, status=self.status), time_gemm)
+        dYt, _ = mxg.mx_quantize_colwise_segment_padded(self.dy, self.d_splits, pad, "e2m1",
+                                                        capacity=self.cap, status=self.status)
+        Xt, _ = mxg.mx_quantize_colwise_segment_padded(self.x, self.d_splits, pad, "e2m1",
+                                                       capacity=self.cap, status=self.status)
+        self.timed.run("wgrad", lambda: mxg.grouped_gemm_wgrad(dYt, Xt, self.d_splits, self.S, pad,
+                                                               out=self.dw, accumulate=False,
+                                                               workspace=self.ws, status=self.status), time_gemm)
+
+    def e2e_step(self):
+        self.x.copy_(self.x_host, non_blocking=True)
+        self.dy.copy_(self.dy_host, non_blocking=True)
+        self.d_splits.copy_(self.splits_host, non_blocking=True)
+        self.step()
+        self.y_host.copy_(self.y, non_blocking=True)
+        self.dx_host.copy_(self.dx, non_blocking=True)
+
+    def h2d_bytes(self):
+        return (self.x_host.numel() + self.dy_host.numel()) * 2 + self.splits_host.numel() * 4
+
+    def d2h_bytes(self):
+        return (self.y_host.numel() + self.dx_host.numel()) * 2
+
+    def config(self):
+        return {"workload": "dense MXFP4 per-pass GEMMs (G=1): M=8192 tokens (seqlen 2048 x mbs 4), "
+                            "hidden K=8192, FFN N=28672, inputs ~N(0,0.02); fwd TN and dgrad NN BF16 out, "
+                            "wgrad NT FP32 out",
+                "G": 1, "S": self.S, "N": self.N, "K": self.K,
+                "step": "6 quantizers + fwd + dgrad + wgrad",
+                "l2": "W 470 MB and dY 470 MB BF16 exceed L2, no flush"}
+
+    dtype = "mxf4 (e2m1 x e2m1, fp32 accumulate)"
+
+    def check(self):
+        self.mxg.check_status(self.status)
+
+
 class BlockwiseFP8:
     """Blockwise-FP8 grouped training step: fwd, dgrad, variable-K wgrad."""
     name = "blockwise_fp8"
@@ -408,7 +494,7 @@ class BlockwiseFP8:
         self.mxg.check_status(self.status)
 
 
-WORKLOAD_CLASSES = {c.name: c for c in (A8W4Forward, MXFP4Train, BlockwiseFP8)}
+WORKLOAD_CLASSES = {c.name: c for c in (A8W4Forward, MXFP4Train, BlockwiseFP8, DenseMXFP4)}
 
 
 def build_workload(name, dev):
@@ -423,6 +509,7 @@ ORACLE_SAMPLES = {
     "a8w4_fwd": (2048, 4096, "e4m3", "e2m1"),
     "mxfp4_moe_train": (1024, 7168, "e2m1", "e2m1"),
     "blockwise_fp8": (1024, 7168, "bw", "bw"),
+    "dense_mxfp4_m8192": (1024, 8192, "e2m1", "e2m1"),
 }
 
 

@@ -125,10 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto locate = [&](int tile, int& g, int& mt, int& nt, Geo& e) {
     g = find_prefix(t_tiles, G, tile);
     e = group_geo(p, t_off, t_rt, t_poff, t_kc, g);
-    const int local = tile - t_tiles[g];
     const int ntn = cdiv_d(e.Nn, BN);
-    mt = local / ntn;
-    nt = local - mt * ntn;
+    tile_mn(tile - t_tiles[g], t_tiles[g + 1] - t_tiles[g], ntn, p.group_m, mt, nt);
   };
 
   if (warp == 0) {
@@ -330,6 +328,8 @@ mxg_status launch_grouped_bw_gemm(const BwGemmArgs& a, cudaStream_t stream, int 
   p.status = a.status;
   p.timeout_ns = wait_timeout_ns();
   p.drain_ns = std::max<uint64_t>(p.timeout_ns, 200000000ull);
+  p.group_m = tile_group_m(a.pass == MXG_PASS_FWD ? (double)a.K
+                           : a.pass == MXG_PASS_DGRAD ? (double)a.N : (double)a.a_cols / a.G);
   // kind::f8f6f4 descriptor: fp32 accumulate, E4M3 x E4M3, K-major, N = 128, M = 128
   p.idesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
   bp.sA = a.a_scale;

@@ -63,6 +63,7 @@ struct Params {
   uint64_t timeout_ns;  // every wait of the main loops
   uint64_t drain_ns;    // teardown waits for copies / MMAs still in flight (>= 200 ms)
   uint32_t idesc;
+  int group_m;          // m-tiles per group of the tile order (see tile_mn)
 };
 
 // Per-expert geometry of one pass (see the table at the top of the file).
@@ -160,6 +161,29 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     pv.hdr[0] = bad ? 0 : 1;
     pv.hdr[1] = bad ? 0 : (int32_t)totals[4];
   }
+}
+
+// Tile order inside an expert: groups of `group_m` m-tiles; inside a group m
+// runs fastest and n outer, so CTAs running at the same time share a B tile
+// and the group's A rows stay in L2 across all of its n-tiles (B is then read
+// once per group instead of once per m-tile).
+MXG_DEVINL void tile_mn(int local, int expert_tiles, int ntn, int group_m, int& mt, int& nt) {
+  const int mtn = expert_tiles / ntn;
+  const int span = group_m * ntn;
+  const int grp = local / span;
+  const int first = grp * group_m;
+  const int rows = min(group_m, mtn - first);
+  const int idx = local - grp * span;
+  mt = first + idx % rows;
+  nt = idx / rows;
+}
+
+// Host: group size that keeps about 32 MiB of A rows (128-row strips of
+// `a_row_bytes` each) resident.
+inline int tile_group_m(double a_row_bytes) {
+  const double strip = 128.0 * (a_row_bytes > 1.0 ? a_row_bytes : 1.0);
+  const double g = (32.0 * 1024 * 1024) / strip;
+  return g < 1.0 ? 1 : (g > 4096.0 ? 4096 : (int)g);
 }
 
 MXG_DEVINL int find_prefix(const int32_t* pre, int G, int x) {  // last g with pre[g] <= x

@@ -306,10 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto locate = [&](int tile, int& g, int& mt, int& nt, Geo& e) {
     g = find_prefix(t_tiles, G, tile);
     e = group_geo(p, t_off, t_rt, t_poff, t_kc, g);
-    const int local = tile - t_tiles[g];
     const int ntn = cdiv_d(e.Nn, BN);
-    mt = local / ntn;
-    nt = local - mt * ntn;
+    tile_mn(tile - t_tiles[g], t_tiles[g + 1] - t_tiles[g], ntn, p.group_m, mt, nt);
   };
 
   if (warp == 0) {
@@ -612,6 +610,12 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   p.status = a.status;
   p.timeout_ns = wait_timeout_ns();
   p.drain_ns = std::max<uint64_t>(p.timeout_ns, 200000000ull);
+  {  // bytes of one A row along the contraction (wgrad: the mean expert's padded tokens)
+    const double eb = kind == KIND_MXF4 ? 0.5 : 1.0;
+    const double kc = a.pass == MXG_PASS_FWD ? (double)a.K
+                    : a.pass == MXG_PASS_DGRAD ? (double)a.N : (double)a.a_cols / a.G;
+    p.group_m = tile_group_m(kc * eb);
+  }
 
   // instruction descriptor: dense, K-major A and B, UE8M0 scales, M=128, N=256
   uint32_t at = kind == KIND_MXF4 ? 1u : 0u;
