@@ -9,11 +9,14 @@
 // (gemm_common.cuh).  Tile 128x128, one 128-element K block per stage:
 //   warp 0     TMA producer: A and B tiles (128-byte swizzle), and for wgrad the
 //              stage's 128 column scales of B (1-D bulk copy), 6-stage ring;
-//   warp 1     owns TMEM (256 columns) and issues 4 tcgen05.mma kind::f8f6f4
-//              (no block scaling) per stage into one of two 128-column
-//              partial accumulators, alternating, each started fresh;
+//   warp 1     owns TMEM (512 columns) and issues 4 tcgen05.mma kind::f8f6f4
+//              (no block scaling) per stage into one of four 128-column
+//              partial accumulators, in turn, each started fresh, and makes
+//              one commit per stage (to the partial's barrier);
 //   warps 2-9  promotion: each thread owns one row and 64 columns; it reads
-//              the stage's partial from TMEM, hands it back, and adds
+//              the stage's partial from TMEM, hands it back, frees the
+//              stage's shared memory for the producer (the partial being
+//              complete means its MMAs have read the stage), and adds
 //              partial * sa[row, kb] * sb[., kb] into fp32 registers; at the
 //              end of the tile the registers are stored (BF16, FP32 or +=).
 #include <cuda.h>
@@ -36,7 +39,8 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTileBytes = 128 * 128;  // one operand tile per stage: 128 rows x 128 B
 constexpr int kSbBytes = 128 * 4;      // wgrad: 128 fp32 column scales per stage
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;
+constexpr int kPBufs = 4;  // 128-column partial accumulators in TMEM
 
 struct BwParams {
   Params p;
@@ -51,7 +55,7 @@ struct BwSmem {
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kSbOff = kStages * kStageBytes;
   static constexpr int kBarOff = kSbOff + kStages * kSbBytes;
-  static constexpr int kNumBars = 2 * kStages + 5;  // full, empty, pfull[2], pempty[2], drain
+  static constexpr int kNumBars = 2 * kStages + 2 * kPBufs + 1;  // full, empty, pfull, pempty, drain
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kTabOff = kMiscOff + 16;
   static constexpr int kTabBytes = 5 * (kMaxExperts + 1) * 4;
@@ -91,19 +95,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto pfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-  auto pempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  auto pempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + kPBufs + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kPBufs);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      // wgrad: the column scales of a stage are read by the promotion warps,
-      // so the slot is free only after they (and the MMAs) are done with it
-      ptx::mbar_init(empty_bar(s), wg ? 1 + kEpiWarps : 1);
+      // freed by the promotion warps once the stage's partial is complete
+      // (and, for wgrad, once they have read its column scales)
+      ptx::mbar_init(empty_bar(s), kEpiWarps);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kPBufs; ++b) {
       ptx::mbar_init(pfull_bar(b), 1);
       ptx::mbar_init(pempty_bar(b), kEpiWarps);
     }
@@ -179,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         locate(tile, g, mt, nt, e);
         const int nk = e.Kc / 128;
         for (int kb = 0; kb < nk; ++kb, ++kcount) {
-          const uint32_t buf = kcount & 1u;
+          const uint32_t buf = kcount % kPBufs;
           if (!ptx::mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
-          if (!ptx::mbar_wait(pempty_bar(buf), ((kcount >> 1) & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          if (!ptx::mbar_wait(pempty_bar(buf), ((kcount / kPBufs) & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t sA = sbase + stage * L::kStageBytes;
           const uint64_t adesc0 = ptx::smem_desc(sA, 16, 1024, 2);
@@ -190,8 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j)
             ptx::mma_f8f6f4(tmem + buf * BN, adesc0 + 2 * j, bdesc0 + 2 * j, p.idesc, j != 0);
           issued = true;
-          ptx::tc_commit(empty_bar(stage));
-          ptx::tc_commit(pfull_bar(buf));
+          ptx::tc_commit(pfull_bar(buf));  // the promotion warps free the stage
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -231,9 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           sa_next = arow_ok ? __ldg(sa_col + (akb0 + kb + 1) * bp.sA_ld) : 0.f;
           if (!wg) sb_next = __ldg(sb_row + kb + 1);
         }
-        const uint32_t buf = kcount & 1u;
-        if (!ptx::mbar_wait(pfull_bar(buf), (kcount >> 1) & 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+        const uint32_t buf = kcount % kPBufs;
+        const bool landed = ptx::mbar_wait(pfull_bar(buf), (kcount / kPBufs) & 1u, abort_flag, p.status, p.timeout_ns);
+        if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }  // the warp leaves together
         ptx::tc_fence_after();
+        // every MMA of this stage has completed: its shared memory may be refilled
+        if (!wg && lane == 0) ptx::mbar_arrive(empty_bar((int)(kcount % kStages)));
         uint32_t r[64];
         __syncwarp();
         ptx::tmem_ld_32x32b_x32(tl + buf * BN, r);
@@ -249,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           const int st = (int)(kcount % kStages);
           // acquire the stage's bulk-copied column scales directly
-          if (!ptx::mbar_wait(full_bar(st), (kcount / kStages) & 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          const bool sb_ok = ptx::mbar_wait(full_bar(st), (kcount / kStages) & 1u, abort_flag, p.status, p.timeout_ns);
+          if (!__all_sync(0xffffffffu, sb_ok)) { ok = false; break; }
           const float4* sbv = reinterpret_cast<const float4*>(smem + L::kSbOff + st * kSbBytes) + chalf * 16;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
