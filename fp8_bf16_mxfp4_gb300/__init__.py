@@ -22,6 +22,7 @@ from . import _lib
 
 __all__ = [
     "MXOperand", "MXGError", "mx_quantize_rowwise", "mx_quantize_colwise_segment_padded",
+    "mx_quantize_dual_segment_padded",
     "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "gemm_workspace_size",
     "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns",
     "library_path", "BWOperand", "bw_quantize_1x128", "bw_quantize_128x128",
@@ -164,6 +165,40 @@ def mx_quantize_colwise_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, 
     if check:
         check_status(st)
     return MXOperand(qT, sT, elem, capacity), poff
+
+
+def mx_quantize_dual_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, pad_multiple: int,
+                                    elem: str, capacity: int | None = None,
+                                    q: torch.Tensor | None = None, s: torch.Tensor | None = None,
+                                    status: torch.Tensor | None = None, check: bool = False):
+    """BF16 [S, C] -> (row-wise operand [S, C], column-wise operand
+    [C, capacity], int64 padded offsets [G+1]) from one read of x; the same
+    bytes as mx_quantize_rowwise plus mx_quantize_colwise_segment_padded."""
+    _need_cuda(x, m_splits)
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bfloat16 tensor")
+    S, C = x.shape
+    G = m_splits.numel()
+    if capacity is None:
+        capacity = mx_padded_rows_capacity(S, G, pad_multiple)
+    if q is None:
+        q = torch.empty((S, _codes_cols(elem, C)), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((S, C // 32), dtype=torch.uint8, device=x.device)
+    qT = torch.empty((C, _codes_cols(elem, capacity)), dtype=torch.uint8, device=x.device)
+    sT = torch.empty((C, capacity // 32), dtype=torch.uint8, device=x.device)
+    poff = torch.empty(G + 1, dtype=torch.int64, device=x.device)
+    st = status if status is not None else status_tensor(x.device)
+    lib = _lib.load()
+    _ok(lib.mx_quantize_dual_segment_padded(
+        _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, pad_multiple, ELEM[elem], _ptr(q),
+        _ld(q, _codes_cols(elem, C)), _ptr(s), _ld(s, C // 32), _ptr(qT),
+        _ld(qT, _codes_cols(elem, capacity)), _ptr(sT), _ld(sT, capacity // 32), capacity,
+        _ptr(poff), _ptr(st), _stream(x.device)),
+        "mx_quantize_dual_segment_padded")
+    if check:
+        check_status(st)
+    return MXOperand(q, s, elem, C), MXOperand(qT, sT, elem, capacity), poff
 
 
 def gemm_workspace_size(pass_: str, G: int, S: int, N: int, K: int, pad: int = 32) -> int:

@@ -54,6 +54,9 @@ SIGNATURES = {
     "mx_quantize_colwise_segment_padded": (
         c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp, c_i64,
                 c_i64, c_vp, c_vp, c_vp]),
+    "mx_quantize_dual_segment_padded": (
+        c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp, c_i64,
+                c_vp, c_i64, c_vp, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "mx_padded_rows_capacity": (c_i64, [c_i64, c_i32, c_i32]),
     "grouped_gemm_fwd": (
         c_i32, [ctypes.POINTER(MxOperandC), ctypes.POINTER(MxOperandC), c_vp, c_i32, c_i64, c_vp,

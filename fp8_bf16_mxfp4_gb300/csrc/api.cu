@@ -204,10 +204,11 @@ mxg_status mx_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_
   if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
   if (rows < 0 || cols <= 0 || cols % 32 != 0) return MXG_ERR_SHAPE;
   if (ld_x < cols || ld_q < code_bytes(elem, cols) || ld_s < cols / 32) return MXG_ERR_SHAPE;
-  if (ld_x % 8 != 0 || ld_q % (elem == MXG_E2M1 ? 4 : 8) != 0) return MXG_ERR_ALIGN;
+  // codes are written 16 bytes per block (E2M1) or two 16-byte halves (E4M3)
+  if (ld_x % 8 != 0 || ld_q % 16 != 0) return MXG_ERR_ALIGN;
   if (rows == 0) return MXG_OK;  // nothing to read or write; pointers may be NULL
   if (x == nullptr || q == nullptr || s == nullptr) return MXG_ERR_NULL;
-  if (!aligned16(x) || !aligned(q, elem == MXG_E2M1 ? 4 : 8)) return MXG_ERR_ALIGN;
+  if (!aligned16(x) || !aligned16(q)) return MXG_ERR_ALIGN;
   int dev = 0, sms = 0;
   mxg_status st = check_device({x, q, s}, &dev, &sms);
   if (st != MXG_OK) return st;
@@ -243,6 +244,42 @@ mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64
   return cuda_status(launch_mx_colwise(x, rows, cols, ld_x, d_m_splits, G, pad_multiple, elem, qT,
                                        ld_q, sT, ld_s, capacity, d_pad_offsets, d_status,
                                        static_cast<cudaStream_t>(stream), sms));
+}
+
+mxg_status mx_quantize_dual_segment_padded(const void* x, int64_t rows, int64_t cols,
+                                           int64_t ld_x, const int32_t* d_m_splits, int32_t G,
+                                           int32_t pad_multiple, int32_t elem, void* q,
+                                           int64_t ld_q, uint8_t* s, int64_t ld_s, void* qT,
+                                           int64_t ld_qT, uint8_t* sT, int64_t ld_sT,
+                                           int64_t capacity, int64_t* d_pad_offsets,
+                                           int32_t* d_status, void* stream) {
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  if (pad_multiple <= 0 || pad_multiple % 32 != 0) return MXG_ERR_SHAPE;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0 || capacity < 0 || capacity % 32 != 0)
+    return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < code_bytes(elem, cols) || ld_s < cols / 32 ||
+      ld_qT < code_bytes(elem, capacity) || ld_sT < capacity / 32)
+    return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 16 != 0 || ld_qT % 16 != 0) return MXG_ERR_ALIGN;
+  // x, q, s may be NULL when there are no rows; qT / sT when there is no capacity
+  if ((rows > 0 && (x == nullptr || q == nullptr || s == nullptr)) ||
+      (capacity > 0 && (qT == nullptr || sT == nullptr)))
+    return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(qT) || !aligned(d_pad_offsets, 8))
+    return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, q, s, d_m_splits, qT, sT, d_pad_offsets, d_status}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  // with no rows the row-wise half has nothing to write; the launch still
+  // validates the splits and fills the padded offsets
+  return cuda_status(launch_mx_colwise(x, rows, cols, ld_x, d_m_splits, G, pad_multiple, elem, qT,
+                                       ld_qT, sT, ld_sT, capacity, d_pad_offsets, d_status,
+                                       static_cast<cudaStream_t>(stream), sms,
+                                       rows > 0 ? q : nullptr, ld_q, s, ld_s));
 }
 
 size_t mxg_gemm_workspace_size(int32_t pass, int32_t G, int64_t S, int64_t N, int64_t K,

@@ -88,22 +88,4 @@ MXG_DEVINL uint32_t cvt_e4m3x4(float a0, float a1, float a2, float a3) {
   return r;
 }
 
-// Sign bits of eight bf16 values (in four 32-bit words) moved to bit 3 of
-// each nibble: keeps the sign of values that round to zero.
-MXG_DEVINL uint32_t e2m1x8_signs(const uint32_t* w) {
-  uint32_t s = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    s |= ((w[i] >> 15) & 1u) << (8 * i + 3);
-    s |= ((w[i] >> 31) & 1u) << (8 * i + 7);
-  }
-  return s;
-}
-
-// Same for E4M3 (bit 7 of each byte) for four bf16 values in two words.
-MXG_DEVINL uint32_t e4m3x4_signs(uint32_t w0, uint32_t w1) {
-  return ((w0 >> 8) & 0x80u) | ((w0 >> 16) & 0x8000u) | ((w1 << 8) & 0x800000u) |
-         (w1 & 0x80000000u);
-}
-
 }  // namespace mxg

@@ -44,11 +44,13 @@ MXG_DEVINL void quantize8(const uint32_t* w, float sinv, uint32_t* out) {
     v[2 * i] = bf16lo_to_f32(w[i]) * sinv;
     v[2 * i + 1] = bf16hi_to_f32(w[i]) * sinv;
   }
+  // The hardware conversions keep the sign of a value that rounds to zero
+  // (E2M1 0x8, E4M3 0x80), as the OCP rule and the oracle do.
   if constexpr (kElem == MXG_E2M1) {
-    out[0] = cvt_e2m1x8(v) | e2m1x8_signs(w);
+    out[0] = cvt_e2m1x8(v);
   } else {
-    out[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]) | e4m3x4_signs(w[0], w[1]);
-    out[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]) | e4m3x4_signs(w[2], w[3]);
+    out[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]);
+    out[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]);
   }
 }
 
@@ -164,8 +166,8 @@ __device__ int find_segment(const SegTable& t, int G, int64_t j) {
   return lo;  // the last such g is non-empty since poff[g+1] > j
 }
 
-// Quantizes the 32 tokens of one column (16 words of bf16 pairs, token 2i in
-// the low half) and writes its codes and scale.
+// Quantizes one 32-element block (16 words of bf16 pairs, element 2i in the
+// low half) and writes its codes and scale.
 template <int kElem>
 MXG_DEVINL void emit_col_block(const uint32_t* w, uint8_t* qrow, uint8_t* srow) {
   uint32_t am = 0;
@@ -204,14 +206,20 @@ MXG_DEVINL void emit_col_block(const uint32_t* w, uint8_t* qrow, uint8_t* srow) 
 // so each transposed output row is written as 64 (E2M1) / 128 (E4M3)
 // contiguous bytes by four lanes.  (A three-buffer cp.async pipeline of the
 // same tiles measured ~20% slower on GB300 than this register prefetch.)
+//
+// kDual: the same pass also writes the row-wise operand (the fused dual
+// quantizer, one HBM read of x for both): each real token row of the staged
+// tile is quantized along the columns, four 32-blocks per row and tile, and
+// written at its source row; padding positions write nothing.
 constexpr int kColCtasPerSm = 2;
 
-template <int kElem>
+template <int kElem, bool kDual>
 __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
     const int32_t* __restrict__ splits, int G, int pad, uint8_t* __restrict__ qT, int64_t ld_q,
     uint8_t* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
-    int32_t* status) {
+    int32_t* status, uint8_t* __restrict__ q_row, int64_t ld_qr, uint8_t* __restrict__ s_row,
+    int64_t ld_sr) {
   static_assert(kColTokens == 128 && kColCols == 128 && kColThreads == 256, "thread mapping");
   __shared__ SegTable tab;
   __shared__ __align__(16) uint32_t tile[kColTokens * (kColCols / 2) + 4 * 8];
@@ -287,6 +295,29 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
       emit_col_block<kElem>(wa, qT + col * ld_q + qoff, sT + col * ld_s + (jb >> 5));
       if (col + 1 < cols)
         emit_col_block<kElem>(wb, qT + (col + 1) * ld_q + qoff, sT + (col + 1) * ld_s + (jb >> 5));
+    }
+    if constexpr (kDual) {
+      // row-wise blocks: thread -> token row tid/2, 32-blocks 2*(tid%2) and +1
+      const int rr = threadIdx.x >> 1;
+      const int64_t sr = src_row[buf][rr];
+      if (sr >= 0) {
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const int b = 2 * (threadIdx.x & 1) + bb;
+          const int64_t colb = (tile_id % ntc) * kColCols + 32 * b;
+          if (colb < cols) {
+            const uint4* rp = reinterpret_cast<const uint4*>(tile + rr * 64 + (rr >> 5) * 8 + 16 * b);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 v4 = rp[i];
+              w[4 * i] = v4.x; w[4 * i + 1] = v4.y; w[4 * i + 2] = v4.z; w[4 * i + 3] = v4.w;
+            }
+            emit_col_block<kElem>(w, q_row + sr * ld_qr + (colb >> 5) * kBytesPerBlock,
+                                  s_row + sr * ld_sr + (colb >> 5));
+          }
+        }
+      }
     }
     __syncthreads();  // the tile buffer is rewritten next iteration
     buf ^= 1;
@@ -492,7 +523,8 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
                               const int32_t* splits, int G, int pad, int elem, void* qT,
                               int64_t ld_q, uint8_t* sT, int64_t ld_s, int64_t capacity,
                               int64_t* pad_offsets, int32_t* status, cudaStream_t stream,
-                              int num_sms) {
+                              int num_sms, void* q_row, int64_t ld_qr, uint8_t* s_row,
+                              int64_t ld_sr) {
   // persistent: at most kColCtasPerSm CTAs per SM, never more than the tiles
   const int64_t tiles = (capacity + kColTokens - 1) / kColTokens * ((cols + kColCols - 1) / kColCols);
   int64_t ctas = std::min<int64_t>(tiles, (int64_t)num_sms * kColCtasPerSm);
@@ -500,12 +532,27 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
   dim3 grid((unsigned)ctas);
   auto* xp = static_cast<const uint16_t*>(x);
   auto* qp = static_cast<uint8_t*>(qT);
-  if (elem == MXG_E2M1)
-    mx_colwise_kernel<MXG_E2M1><<<grid, kColThreads, 0, stream>>>(
-        xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status);
-  else
-    mx_colwise_kernel<MXG_E4M3><<<grid, kColThreads, 0, stream>>>(
-        xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status);
+  auto* qr = static_cast<uint8_t*>(q_row);
+  const bool dual = q_row != nullptr;
+  if (elem == MXG_E2M1) {
+    if (dual)
+      mx_colwise_kernel<MXG_E2M1, true><<<grid, kColThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, qr, ld_qr,
+          s_row, ld_sr);
+    else
+      mx_colwise_kernel<MXG_E2M1, false><<<grid, kColThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr,
+          0, nullptr, 0);
+  } else {
+    if (dual)
+      mx_colwise_kernel<MXG_E4M3, true><<<grid, kColThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, qr, ld_qr,
+          s_row, ld_sr);
+    else
+      mx_colwise_kernel<MXG_E4M3, false><<<grid, kColThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr,
+          0, nullptr, 0);
+  }
   return cudaGetLastError();
 }
 

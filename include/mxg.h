@@ -101,7 +101,8 @@ typedef struct mxg_mx_operand {
  * 8 for E4M3; e = -127 for an all-zero block); scale byte = e + 127; element =
  * x * 2^-e rounded to nearest, ties to even, saturating (6 / 448), sign kept.
  *   x      : BF16 [rows, cols], row stride ld_x elements (ld_x % 8 == 0)
- *   q      : codes [rows, cols/2] (E2M1) or [rows, cols] (E4M3), stride ld_q bytes
+ *   q      : codes [rows, cols/2] (E2M1) or [rows, cols] (E4M3), stride ld_q bytes;
+ *            q 16-byte aligned and ld_q % 16 == 0 (MXG_ERR_ALIGN otherwise)
  *   s      : scale bytes [rows, cols/32], stride ld_s bytes
  * cols % 32 == 0; rows may be 0 (no launch).  Writes only q and s. */
 mxg_status mx_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -128,6 +129,28 @@ mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64
                                               void* qT, int64_t ld_q, uint8_t* sT, int64_t ld_s,
                                               int64_t capacity, int64_t* d_pad_offsets,
                                               int32_t* d_status, void* stream);
+
+/* Fused dual MX quantization: one read of x yields both operands of a
+ * training step -- the row-wise operand (fwd / dgrad) and the column-wise
+ * segment-padded operand (wgrad) -- as the dual activation quantizer of "Add
+ * ROCm Triton blockwise FP8 grouped GEMM" (PR #716,
+ * `quantize_fp8_blockwise_act_operands`) does for blockwise FP8.  The bytes
+ * are identical to mx_quantize_rowwise(x) -> (q, s) followed by
+ * mx_quantize_colwise_segment_padded(x, ...) -> (qT, sT, d_pad_offsets).
+ *   q, ld_q, s, ld_s      : as in mx_quantize_rowwise (q 16-byte aligned,
+ *                           ld_q % 16 == 0)
+ *   qT, ld_qT, sT, ld_sT  : as qT, ld_q, sT, ld_s of the column-wise call
+ *   other arguments       : as in mx_quantize_colwise_segment_padded
+ * Host errors as for the two calls; device errors as for the column-wise call
+ * (MXG_ERR_SPLITS, MXG_ERR_CAPACITY), in which case neither operand is
+ * written. */
+mxg_status mx_quantize_dual_segment_padded(const void* x, int64_t rows, int64_t cols,
+                                           int64_t ld_x, const int32_t* d_m_splits, int32_t G,
+                                           int32_t pad_multiple, int32_t elem, void* q,
+                                           int64_t ld_q, uint8_t* s, int64_t ld_s, void* qT,
+                                           int64_t ld_qT, uint8_t* sT, int64_t ld_sT,
+                                           int64_t capacity, int64_t* d_pad_offsets,
+                                           int32_t* d_status, void* stream);
 
 /* Upper bound of sum_g ceil(m_g/pad)*pad over all splits of `rows` into G
  * experts: floor((rows + k*(pad-1)) / pad) * pad with k = min(G, rows), the

@@ -79,6 +79,8 @@ def test_quantize_host_checks(lib):
     assert q(vp(FAKE), 4, 64, 64, 3, vp(FAKE), 32, vp(FAKE), 2, None) == 5       # bad elem
     assert q(vp(FAKE + 2), 4, 64, 64, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 3   # x misaligned
     assert q(vp(FAKE), 4, 64, 68, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 3       # ld_x % 8
+    assert q(vp(FAKE), 4, 64, 64, 1, vp(FAKE + 4), 32, vp(FAKE), 2, None) == 3   # q not 16-B aligned
+    assert q(vp(FAKE), 4, 64, 64, 1, vp(FAKE), 36, vp(FAKE), 2, None) == 3       # ld_q % 16
     c = lib.mx_quantize_colwise_segment_padded
     args = [vp(FAKE), 64, 64, 64, vp(FAKE), 4, 32, 1, vp(FAKE), 96, vp(FAKE), 4, 192, vp(FAKE),
             vp(FAKE), None]
@@ -92,6 +94,24 @@ def test_quantize_host_checks(lib):
     assert c(*bad) == 2                                                           # pad % 32
     bad = list(args); bad[12] = 100
     assert c(*bad) == 2                                                           # capacity % 32
+    d = lib.mx_quantize_dual_segment_padded
+    #        x        rows cols ld_x splits    G  pad elem q        ld_q s        ld_s qT       ld_qT sT
+    dargs = [vp(FAKE), 64, 64, 64, vp(FAKE), 4, 32, 1, vp(FAKE), 32, vp(FAKE), 2, vp(FAKE), 96, vp(FAKE),
+             6, 192, vp(FAKE), vp(FAKE), None]
+    bad = list(dargs); bad[18] = None
+    assert d(*bad) == 1                                                           # NULL status
+    bad = list(dargs); bad[8] = None
+    assert d(*bad) == 1                                                           # NULL row-wise codes
+    bad = list(dargs); bad[9] = 16
+    assert d(*bad) == 2                                                           # ld_q < cols/2
+    bad = list(dargs); bad[9] = 36
+    assert d(*bad) == 3                                                           # ld_q % 16
+    bad = list(dargs); bad[8] = vp(FAKE + 4)
+    assert d(*bad) == 3                                                           # q misaligned
+    bad = list(dargs); bad[15] = 4
+    assert d(*bad) == 2                                                           # ld_sT < capacity/32
+    bad = list(dargs); bad[7] = 3
+    assert d(*bad) == 5                                                           # bad elem
 
 
 def _op(rows, cols, elem, data=FAKE, ld=None, scale_ld=None):

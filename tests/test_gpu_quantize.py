@@ -141,3 +141,53 @@ def test_colwise_rejects_bad_splits_on_device(bad, code):
         mxg.check_status(st)
     assert ei.value.code == code
     assert (q == 0xAB).all() and (sc == 0xCD).all() and (poff == -7).all()
+
+
+# ------------------------------------------------------------------ fused dual quantizer
+
+DUAL_CASES = COL_CASES + [([2000, 0, 1, 700, 129], 32, 4128)]   # > one column tile, ragged
+
+
+@pytest.mark.parametrize("elem", ["e2m1", "e4m3"])
+@pytest.mark.parametrize("splits,pad,cols", DUAL_CASES)
+def test_dual_matches_rowwise_and_colwise_oracles(elem, splits, pad, cols):
+    """One read of x: the row-wise operand and the column-wise segment-padded
+    operand, each bit-exact against its own oracle."""
+    rng = np.random.default_rng(len(splits) * 17 + pad + cols)
+    splits = np.array(splits, dtype=np.int32)
+    S = int(splits.sum())
+    x = synth.normal_bf16(rng, (S, cols), std=3.0, outlier_frac=0.03)
+    mxg = _mxg()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    row, col, poff = mxg.mx_quantize_dual_segment_padded(bf16_to_dev(x), i32_to_dev(splits), pad, elem,
+                                                         status=st, check=True)
+    rd, rs = oracle.quantize_mx_rowwise(x, elem)
+    assert np.array_equal(row.data.cpu().numpy(), rd)
+    assert np.array_equal(row.scale.cpu().numpy(), rs)
+    d, s, p = oracle.quantize_mx_colwise_segment_padded(x, splits, pad, elem)
+    spad = int(p[-1])
+    assert np.array_equal(poff.cpu().numpy(), p)
+    cb = spad // 2 if elem == "e2m1" else spad
+    assert np.array_equal(col.data.cpu().numpy()[:, :cb], d)
+    assert np.array_equal(col.scale.cpu().numpy()[:, : spad // 32], s)
+
+
+def test_dual_rejects_bad_splits_and_writes_nothing():
+    mxg = _mxg()
+    x = bf16_to_dev(synth.normal_bf16(np.random.default_rng(2), (14, 64)))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    q = torch.full((14, 32), 0xAB, dtype=torch.uint8, device="cuda:0")
+    s = torch.full((14, 2), 0xCD, dtype=torch.uint8, device="cuda:0")
+    qT = torch.full((64, 48), 0xAB, dtype=torch.uint8, device="cuda:0")
+    sT = torch.full((64, 3), 0xCD, dtype=torch.uint8, device="cuda:0")
+    poff = torch.full((4,), -7, dtype=torch.int64, device="cuda:0")
+    rc = mxg._lib.load().mx_quantize_dual_segment_padded(
+        mxg._ptr(x), 14, 64, 64, mxg._ptr(i32_to_dev([10, -1, 5])), 3, 32, 1, mxg._ptr(q), 32,
+        mxg._ptr(s), 2, mxg._ptr(qT), 48, mxg._ptr(sT), 3, 96, mxg._ptr(poff), mxg._ptr(st),
+        mxg._stream(x.device))
+    assert rc == 0
+    with pytest.raises(mxg.MXGError) as ei:
+        mxg.check_status(st)
+    assert ei.value.code == 4
+    assert (q == 0xAB).all() and (s == 0xCD).all() and (qT == 0xAB).all() and (sT == 0xCD).all()
+    assert (poff == -7).all()
