@@ -253,6 +253,10 @@ class A8W4Forward:
                 "l2": "inputs larger than L2 (X 67 MB + W 940 MB BF16), no flush"}
 
     dtype = "mxf8f6f4 (e4m3 x e2m1, fp32 accumulate)"
+    # DRAM bytes (read + write) of one forward call -- plan, scale pack and GEMM
+    # kernels -- counted by ncu on GB300 (dram__bytes_read.sum +
+    # dram__bytes_write.sum); algorithmic bytes of the call: 519,045,120.
+    traffic_bytes = 506477312
 
     def check(self):
         self.mxg.check_status(self.status)
@@ -430,6 +434,7 @@ class DenseMXFP4:
 
 class BlockwiseFP8:
     """Blockwise-FP8 grouped training step: fwd, dgrad, variable-K wgrad."""
+    call_kernels = "plan + tcgen05 GEMM with CUDA-core promotion"
     name = "blockwise_fp8"
 
     def __init__(self, dev):
@@ -660,8 +665,8 @@ def run_gpu(args):
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": wl.config(),
         "roofline": {"bound": "tensor", "achieved": d["tflops"], "peak": d["peak"], "unit": "TFLOP/s",
-                     "frac": d["frac"], "traffic": None,
-                     "kernel": f"grouped GEMM {dom} call (plan + scale pack + tcgen05 GEMM)",
+                     "frac": d["frac"], "traffic": getattr(wl, "traffic_bytes", None),
+                     "kernel": f"grouped GEMM {dom} call ({getattr(wl, 'call_kernels', 'plan + scale pack + tcgen05 GEMM')})",
                      "peak_source": f"{src}: bf16_tflops_sustained x {wl.gemm_info[dom][1]:g} "
                                     f"(nominal {wl.gemm_info[dom][2]}/bf16 dense ratio)",
                      "gemm_ms": d["ms"]},
