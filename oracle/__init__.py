@@ -49,6 +49,7 @@ from .blockwise import (  # noqa: F401
     dequantize_bw_1x128,
     dequantize_bw_128x128,
     transpose_bw_128x128,
+    pow2_scale,
 )
 from .gemm import (  # noqa: F401
     check_splits,

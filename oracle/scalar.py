@@ -136,13 +136,22 @@ def round_to_f32(v: Fraction) -> Fraction:
 F32_1EM4 = round_to_f32(Fraction(1, 10000))
 
 
-def quantize_block_bw(block_bits):
+def quantize_block_bw(block_bits, pow2: bool = False):
     """One blockwise-FP8 block (any number of BF16 values sharing one scale)
-    -> (fp32 scale as a Fraction, list of E4M3 codes)."""
+    -> (fp32 scale as a Fraction, list of E4M3 codes).  pow2: the scale is
+    the smallest power of two s with 448 * s >= a, found by walking exact
+    powers of two."""
     vals = [bf16_value(b) for b in block_bits]
     amax = max(abs(v) for v in vals)
     a = max(amax, F32_1EM4)
-    s = round_to_f32(a / 448)
+    if pow2:
+        s = Fraction(1)
+        while 448 * s < a:
+            s *= 2
+        while 448 * (s / 2) >= a:
+            s /= 2
+    else:
+        s = round_to_f32(a / 448)
     codes = []
     for b, v in zip(block_bits, vals):
         q = round_to_f32(v / s)

@@ -86,3 +86,71 @@ def test_colwise_padded_segments():
         seg = codes[:, j0: j0 + m]
         assert (seg == (0xFE if c < 0 else 0x7E)).all()
         assert (codes[:, j0 + m: int(poff[g + 1])] == 0).all()
+
+
+# ---------------------------------------------------------------- power-of-two scales
+
+def test_pow2_scale_hand_worked_values():
+    """s = the smallest power of two with 448 * s >= max(amax, 1e-4), worked by hand:
+    448 -> 1 (exact fit), 449 -> 2, 447.99 -> 1, 896 -> 2, 0.875 = 448 * 2^-9 -> 2^-9,
+    3 -> 2^-7 (448/128 = 3.5 >= 3 > 1.75), 1e-4 (the floor) -> 2^-22 (448 * 2^-22 =
+    1.07e-4 >= 1e-4 > 5.3e-5)."""
+    a = np.array([448.0, 449.0, 447.99, 896.0, 0.875, 3.0, 1e-4], dtype=np.float32)
+    want = [1.0, 2.0, 1.0, 2.0, 2.0 ** -9, 2.0 ** -7, 2.0 ** -22]
+    assert oracle.pow2_scale(a).tolist() == want
+
+
+def test_pow2_block_codes_hand_worked():
+    """A 1x128 block with amax 3: s = 2^-7, so 3 -> 384 = 1.5 * 2^8 (E4M3 0x7C),
+    -1 -> -128 = -2^7 (0xF0), 0.5 -> 64 = 2^6 (0x68), 0 -> 0x00."""
+    row = np.zeros(128, dtype=np.float32)
+    row[:4] = [3.0, -1.0, 0.5, 0.0]
+    codes, s = oracle.quantize_bw_1x128(synth.f32_to_bf16_bits(row[None, :]), pow2=True)
+    assert s.tolist() == [[2.0 ** -7]]
+    assert codes[0, :4].tolist() == [0x7C, 0xF0, 0x68, 0x00]
+
+
+def test_pow2_matches_exact_rational_formulation():
+    rng = np.random.default_rng(23)
+    x = synth.normal_bf16(rng, (6, 256), std=3.0, outlier_frac=0.02)
+    v = synth.bf16_bits_to_f32(x)
+    x[4] = synth.f32_to_bf16_bits(v[4] * np.float32(1e-7))   # below the floor
+    x[5, :128] = 0                                           # zero block
+    x[5, 128] = synth.f32_to_bf16_bits(np.array([448.0], dtype=np.float32))[0]  # exact fit
+    codes, s = oracle.quantize_bw_1x128(x, pow2=True)
+    for r in range(x.shape[0]):
+        for b in range(2):
+            blk = [int(t) for t in x[r, 128 * b: 128 * b + 128]]
+            sf, cs = scalar.quantize_block_bw(blk, pow2=True)
+            assert float(sf) == float(s[r, b]), (r, b)
+            assert list(codes[r, 128 * b: 128 * b + 128]) == cs, (r, b)
+
+
+def test_pow2_scale_brackets_the_fp32_scale():
+    """The power-of-two scale is the fp32 scale a/448 rounded up to a power of
+    two: s_fp32 <= s_pow2 < 2 s_fp32 (up to the rounding of s_fp32), blockwise."""
+    rng = np.random.default_rng(24)
+    w = synth.normal_bf16(rng, (3, 256, 384), std=5.0, outlier_frac=0.05)
+    _, s32 = oracle.quantize_bw_128x128(w)
+    _, s2 = oracle.quantize_bw_128x128(w, pow2=True)
+    m, _ = np.frexp(s2.astype(np.float64))
+    assert (m == 0.5).all()                                   # powers of two
+    r = s2.astype(np.float64) / s32.astype(np.float64)
+    assert (r >= 1.0 - 2.0 ** -23).all() and (r < 2.0).all()
+
+
+def test_pow2_colwise_segments_match_rowwise_of_each_expert():
+    rng = np.random.default_rng(25)
+    splits = np.array([130, 0, 5, 256], dtype=np.int32)
+    x = synth.normal_bf16(rng, (int(splits.sum()), 96), std=2.0, outlier_frac=0.02)
+    codes, s, poff = oracle.quantize_bw_colwise_padded(x, splits, pow2=True)
+    off = np.concatenate([[0], np.cumsum(splits)])
+    for g in range(len(splits)):
+        p_g = int(poff[g + 1] - poff[g])
+        if p_g == 0:
+            continue
+        seg = np.zeros((96, p_g), dtype=np.uint16)
+        seg[:, : splits[g]] = x[off[g]: off[g + 1]].T
+        cg, sg = oracle.quantize_bw_1x128(seg, pow2=True)
+        assert np.array_equal(codes[:, poff[g]: poff[g + 1]], cg)
+        assert np.array_equal(s[:, poff[g] // 128: poff[g + 1] // 128], sg)
