@@ -499,7 +499,55 @@ class BlockwiseFP8:
         self.mxg.check_status(self.status)
 
 
-WORKLOAD_CLASSES = {c.name: c for c in (A8W4Forward, MXFP4Train, BlockwiseFP8, DenseMXFP4)}
+class BlockwiseFP8Pow2(BlockwiseFP8):
+    """The blockwise-FP8 step with power-of-two scales: the quantizers write
+    MXFP8 operands (UE8M0 bytes repeated over each 128-block) and the three
+    passes run on the block-scaled MX GEMMs, with no promotion."""
+    call_kernels = "plan + scale pack + tcgen05 GEMM"
+    name = "blockwise_fp8_pow2"
+
+    def __init__(self, dev):
+        import torch
+        super().__init__(dev)
+        mxg, G, N, K, S = self.mxg, self.G, self.N, self.K, self.S
+        ws = max(mxg.gemm_workspace_size("fwd", G, S, N, K), mxg.gemm_workspace_size("dgrad", G, S, N, K),
+                 mxg.gemm_workspace_size("wgrad", G, self.cap, N, K, 128))
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.launches_per_step = 5 + 3 * 3   # five quantizers; three GEMM calls of three kernels
+        f = 2.0 * S * N * K
+        self.gemm_info = {p: (f, FP8_OVER_BF16, "mxf8f6f4 (pow2 blockwise)") for p in ("fwd", "dgrad", "wgrad")}
+
+    def step(self, time_gemm=False):
+        mxg, N = self.mxg, self.N
+        Xq = mxg.bw_quantize_1x128_pow2(self.x)
+        Wq, Wt = mxg.bw_quantize_128x128_pow2(self.w)
+        self.timed.run("fwd", lambda: mxg.grouped_gemm_fwd(Xq, Wq, self.d_splits, N, out=self.y,
+                                                           workspace=self.ws, status=self.status), time_gemm)
+        dYq = mxg.bw_quantize_1x128_pow2(self.dy)
+        self.timed.run("dgrad", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx,
+                                                               workspace=self.ws, status=self.status), time_gemm)
+        dYt, _ = mxg.bw_quantize_colwise_padded_pow2(self.dy, self.d_splits, capacity=self.cap, status=self.status)
+        Xt, _ = mxg.bw_quantize_colwise_padded_pow2(self.x, self.d_splits, capacity=self.cap, status=self.status)
+        self.timed.run("wgrad", lambda: mxg.grouped_gemm_wgrad(dYt, Xt, self.d_splits, self.S, 128, out=self.dw,
+                                                               out_dtype=torch_bf16(), workspace=self.ws,
+                                                               status=self.status), time_gemm)
+
+    def config(self):
+        c = super().config()
+        c["workload"] = ("blockwise FP8 grouped step, power-of-two scales: G=16, 32768 rows uniform "
+                         "routing, K=7168, N=4096; E4M3 with 1x128 activation / 128x128 weight pow2 scales "
+                         "as UE8M0 per 32; fwd, dgrad, variable-K wgrad (pad 128) on the MXFP8 GEMMs, BF16 out")
+        return c
+
+    dtype = "mxf8f6f4 (e4m3 x e4m3, pow2 block scales, fp32 accumulate)"
+
+
+def torch_bf16():
+    import torch
+    return torch.bfloat16
+
+
+WORKLOAD_CLASSES = {c.name: c for c in (A8W4Forward, MXFP4Train, BlockwiseFP8, DenseMXFP4, BlockwiseFP8Pow2)}
 
 
 def build_workload(name, dev):
@@ -514,6 +562,7 @@ ORACLE_SAMPLES = {
     "a8w4_fwd": (2048, 4096, "e4m3", "e2m1"),
     "mxfp4_moe_train": (1024, 7168, "e2m1", "e2m1"),
     "blockwise_fp8": (1024, 7168, "bw", "bw"),
+    "blockwise_fp8_pow2": (1024, 7168, "bw_pow2", "bw_pow2"),
     "dense_mxfp4_m8192": (1024, 8192, "e2m1", "e2m1"),
 }
 
@@ -530,9 +579,10 @@ def oracle_sample(workload="a8w4_fwd", rows=None):
     x = synth.normal_bf16(rng, (rows, K), outlier_frac=0.01)
     wt = synth.normal_bf16(rng, (rows, K), outlier_frac=0.01)
     t0 = time.perf_counter()
-    if ea == "bw":
-        xc, xs = oracle.quantize_bw_1x128(x)
-        wc, ws = oracle.quantize_bw_128x128(wt.reshape(1, rows, K))
+    if ea in ("bw", "bw_pow2"):
+        p2 = ea == "bw_pow2"
+        xc, xs = oracle.quantize_bw_1x128(x, pow2=p2)
+        wc, ws = oracle.quantize_bw_128x128(wt.reshape(1, rows, K), pow2=p2)
         A = oracle.dequantize_bw_1x128(xc, xs)
         W = oracle.dequantize_bw_128x128(wc, ws)[0]
     else:

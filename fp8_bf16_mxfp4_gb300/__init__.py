@@ -27,7 +27,8 @@ __all__ = [
     "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns",
     "library_path", "BWOperand", "bw_quantize_1x128", "bw_quantize_128x128",
     "bw_quantize_colwise_padded", "bw_grouped_gemm_fwd", "bw_grouped_gemm_dgrad",
-    "bw_grouped_gemm_wgrad",
+    "bw_grouped_gemm_wgrad", "bw_quantize_1x128_pow2", "bw_quantize_128x128_pow2",
+    "bw_quantize_colwise_padded_pow2",
 ]
 
 ELEM = {"e2m1": 1, "e4m3": 2}
@@ -354,6 +355,57 @@ def bw_quantize_colwise_padded(x: torch.Tensor, m_splits: torch.Tensor, capacity
     if check:
         check_status(st)
     return BWOperand(qT, sT), poff
+
+
+def bw_quantize_1x128_pow2(x: torch.Tensor) -> MXOperand:
+    """BF16 [rows, cols] -> blockwise FP8 (1x128, power-of-two scales) as an
+    MXFP8 operand: E4M3 [rows, cols] + UE8M0 [rows, cols/32]."""
+    _need_cuda(x)
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    s = torch.empty((R, C // 32), dtype=torch.uint8, device=x.device)
+    _ok(_lib.load().bw_quantize_1x128_pow2(_ptr(x), R, C, _ld(x, C), _ptr(q), _ld(q, C), _ptr(s),
+                                           _ld(s, C // 32), _stream(x.device)), "bw_quantize_1x128_pow2")
+    return MXOperand(q, s, "e4m3", C)
+
+
+def bw_quantize_128x128_pow2(w: torch.Tensor, transposed: bool = True):
+    """BF16 weights [rows, cols] -> (MXFP8 operand with 128x128 power-of-two
+    scales, and when `transposed` the dgrad copy [cols, rows])."""
+    _need_cuda(w)
+    R, C = w.shape
+    dev = w.device
+    q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    s = torch.empty((R, C // 32), dtype=torch.uint8, device=dev)
+    qT = torch.empty((C, R), dtype=torch.uint8, device=dev) if transposed else None
+    sT = torch.empty((C, R // 32), dtype=torch.uint8, device=dev) if transposed else None
+    _ok(_lib.load().bw_quantize_128x128_pow2(
+        _ptr(w), R, C, _ld(w, C), _ptr(q), _ld(q, C), _ptr(s), _ld(s, C // 32), _ptr(qT),
+        _ld(qT, R) if transposed else 0, _ptr(sT), _ld(sT, R // 32) if transposed else 0, _stream(dev)),
+        "bw_quantize_128x128_pow2")
+    return MXOperand(q, s, "e4m3", C), (MXOperand(qT, sT, "e4m3", R) if transposed else None)
+
+
+def bw_quantize_colwise_padded_pow2(x: torch.Tensor, m_splits: torch.Tensor, capacity: int | None = None,
+                                    status: torch.Tensor | None = None, check: bool = False):
+    """BF16 [S, C] -> (MXFP8 operand [C, capacity], segments padded to 128,
+    power-of-two 1x128 scales as UE8M0 [C, capacity/32]; int64 padded offsets)."""
+    _need_cuda(x, m_splits)
+    S, C = x.shape
+    G = m_splits.numel()
+    if capacity is None:
+        capacity = mx_padded_rows_capacity(S, G, 128)
+    qT = torch.empty((C, capacity), dtype=torch.uint8, device=x.device)
+    sT = torch.empty((C, capacity // 32), dtype=torch.uint8, device=x.device)
+    poff = torch.empty(G + 1, dtype=torch.int64, device=x.device)
+    st = status if status is not None else status_tensor(x.device)
+    _ok(_lib.load().bw_quantize_colwise_padded_pow2(
+        _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, _ptr(qT), _ld(qT, capacity), _ptr(sT),
+        _ld(sT, capacity // 32), capacity, _ptr(poff), _ptr(st), _stream(x.device)),
+        "bw_quantize_colwise_padded_pow2")
+    if check:
+        check_status(st)
+    return MXOperand(qT, sT, "e4m3", capacity), poff
 
 
 def _bw_ws(G, device, ws):

@@ -431,7 +431,7 @@ mxg_status bw_quantize_1x128(const void* x, int64_t rows, int64_t cols, int64_t 
   if (st != MXG_OK) return st;
   DeviceGuard g(dev);
   if (!g.ok) return MXG_ERR_CUDA;
-  return cuda_status(launch_bw_rowwise(x, rows, cols, ld_x, q, ld_q, s, ld_s,
+  return cuda_status(launch_bw_rowwise(x, rows, cols, ld_x, q, ld_q, s, ld_s, false,
                                        static_cast<cudaStream_t>(stream), sms));
 }
 
@@ -452,7 +452,7 @@ mxg_status bw_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_
   if (st != MXG_OK) return st;
   DeviceGuard g(dev);
   if (!g.ok) return MXG_ERR_CUDA;
-  return cuda_status(launch_bw_weight(w, rows, cols, ld_w, q, ld_q, s, qT, ld_qT, sT,
+  return cuda_status(launch_bw_weight(w, rows, cols, ld_w, q, ld_q, s, 0, qT, ld_qT, sT, 0, false,
                                       static_cast<cudaStream_t>(stream)));
 }
 
@@ -476,7 +476,74 @@ mxg_status bw_quantize_colwise_padded(const void* x, int64_t rows, int64_t cols,
   DeviceGuard g(dev);
   if (!g.ok) return MXG_ERR_CUDA;
   return cuda_status(launch_bw_colwise(x, rows, cols, ld_x, d_m_splits, G, qT, ld_q, sT, ld_s,
-                                       capacity, d_pad_offsets, d_status,
+                                       capacity, d_pad_offsets, d_status, false,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+// ---- power-of-two blockwise scales, written as MX (UE8M0 per 32) operands
+
+mxg_status bw_quantize_1x128_pow2(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                  void* q, int64_t ld_q, uint8_t* s, int64_t ld_s, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 128 != 0) return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < cols || ld_s < cols / 32) return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 8 != 0 || ld_s % 4 != 0) return MXG_ERR_ALIGN;
+  if (rows == 0) return MXG_OK;
+  if (x == nullptr || q == nullptr || s == nullptr) return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned(q, 8) || !aligned(s, 4)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, q, s}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_bw_rowwise(x, rows, cols, ld_x, q, ld_q, s, ld_s, true,
+                                       static_cast<cudaStream_t>(stream), sms));
+}
+
+mxg_status bw_quantize_128x128_pow2(const void* w, int64_t rows, int64_t cols, int64_t ld_w,
+                                    void* q, int64_t ld_q, uint8_t* s, int64_t ld_s, void* qT,
+                                    int64_t ld_qT, uint8_t* sT, int64_t ld_sT, void* stream) {
+  if ((qT == nullptr) != (sT == nullptr)) return MXG_ERR_NULL;
+  if (rows < 0 || cols <= 0 || rows % 128 != 0 || cols % 128 != 0) return MXG_ERR_SHAPE;
+  if (ld_w < cols || ld_q < cols || ld_s < cols / 32) return MXG_ERR_SHAPE;
+  if (qT != nullptr && (ld_qT < rows || ld_sT < rows / 32)) return MXG_ERR_SHAPE;
+  if (rows / 128 > 65535 || cols / 128 > 0x7FFFFFFF) return MXG_ERR_SHAPE;
+  if (ld_w % 8 != 0 || ld_q % 16 != 0 || ld_s % 4 != 0) return MXG_ERR_ALIGN;
+  if (qT != nullptr && (ld_qT % 16 != 0 || ld_sT % 4 != 0)) return MXG_ERR_ALIGN;
+  if (rows == 0) return MXG_OK;
+  if (w == nullptr || q == nullptr || s == nullptr) return MXG_ERR_NULL;
+  if (!aligned16(w) || !aligned16(q) || !aligned16(qT) || !aligned(s, 4) || !aligned(sT, 4))
+    return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({w, q, s, qT, sT}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_bw_weight(w, rows, cols, ld_w, q, ld_q, s, ld_s, qT, ld_qT, sT, ld_sT,
+                                      true, static_cast<cudaStream_t>(stream)));
+}
+
+mxg_status bw_quantize_colwise_padded_pow2(const void* x, int64_t rows, int64_t cols,
+                                           int64_t ld_x, const int32_t* d_m_splits, int32_t G,
+                                           void* qT, int64_t ld_q, uint8_t* sT, int64_t ld_s,
+                                           int64_t capacity, int64_t* d_pad_offsets,
+                                           int32_t* d_status, void* stream) {
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0 || capacity < 0 || capacity % 128 != 0)
+    return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < capacity || ld_s < capacity / 32) return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 16 != 0 || ld_s % 4 != 0) return MXG_ERR_ALIGN;
+  if ((rows > 0 && x == nullptr) || (capacity > 0 && (qT == nullptr || sT == nullptr)))
+    return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned16(qT) || !aligned(sT, 4) || !aligned(d_pad_offsets, 8))
+    return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, d_m_splits, qT, sT, d_pad_offsets, d_status}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_bw_colwise(x, rows, cols, ld_x, d_m_splits, G, qT, ld_q, sT, ld_s,
+                                       capacity, d_pad_offsets, d_status, true,
                                        static_cast<cudaStream_t>(stream)));
 }
 

@@ -339,6 +339,29 @@ MXG_DEVINL float bw_scale(uint32_t amax_bits) {
   return __fdiv_rn(a, 448.0f);
 }
 
+// Power-of-two form: s = 2^k, the smallest power of two with 448 * s >= a,
+// a = max(amax, 1e-4f) = m * 2^e with m in [1, 2).  Since 448 = 1.75 * 2^8,
+// k = e - 8, plus one when m > 1.75.  k is in [-22, 120] for finite BF16
+// input, so the UE8M0 byte k + 127 is an MX scale and x / s = x * 2^-k exactly.
+MXG_DEVINL int bw_pow2_exponent(uint32_t amax_bits) {
+  const float a = fmaxf(__uint_as_float(amax_bits << 16), kBwAmaxFloor);
+  const uint32_t b = __float_as_uint(a);
+  return (int)((b >> 23) & 0xFFu) - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+}
+MXG_DEVINL uint32_t ue8m0x4(int k) { return (uint32_t)(k + 127) * 0x01010101u; }
+
+// 8 bf16 (four words) * m (a power of two) -> 8 E4M3 codes (two words).
+MXG_DEVINL void bw_quantize8_mul(const uint32_t* w, float m, uint32_t* o) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16lo_to_f32(w[i]) * m;
+    v[2 * i + 1] = bf16hi_to_f32(w[i]) * m;
+  }
+  o[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]);
+  o[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]);
+}
+
 // 8 bf16 (four words) / s -> 8 E4M3 codes (two words).
 MXG_DEVINL void bw_quantize8(const uint32_t* w, float s, uint32_t* o) {
   float v[8];
@@ -352,9 +375,12 @@ MXG_DEVINL void bw_quantize8(const uint32_t* w, float s, uint32_t* o) {
 }
 
 // 1x128 along the row: 16 lanes per block, 8 values (16 bytes) per lane.
+// kPow2: power-of-two scales written as UE8M0 bytes [rows, cols/32], each
+// block's byte repeated over its four 32-blocks (an MXFP8 operand).
+template <bool kPow2>
 __global__ void __launch_bounds__(kRowThreads) bw_rowwise_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
-    uint8_t* __restrict__ q, int64_t ld_q, float* __restrict__ s, int64_t ld_s) {
+    uint8_t* __restrict__ q, int64_t ld_q, void* __restrict__ s, int64_t ld_s) {
   const int64_t chunks_per_row = cols >> 3;
   const int64_t total = rows * chunks_per_row;
   const int64_t step = (int64_t)gridDim.x * kRowThreads;
@@ -371,23 +397,35 @@ __global__ void __launch_bounds__(kRowThreads) bw_rowwise_kernel(
 #pragma unroll
     for (int d = 1; d < 16; d <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
     if (!live) continue;
-    const float sc = bw_scale(am);
     uint32_t o[2];
-    bw_quantize8(w, sc, o);
+    if constexpr (kPow2) {
+      const int k = bw_pow2_exponent(am);
+      bw_quantize8_mul(w, pow2_neg(k), o);
+      if ((threadIdx.x & 15) == 0)
+        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s) + r * ld_s + (c8 >> 4) * 4) = ue8m0x4(k);
+    } else {
+      const float sc = bw_scale(am);
+      bw_quantize8(w, sc, o);
+      if ((threadIdx.x & 15) == 0) static_cast<float*>(s)[(c8 >> 4) * ld_s + r] = sc;
+    }
     *reinterpret_cast<uint2*>(q + r * ld_q + c8 * 8) = make_uint2(o[0], o[1]);
-    if ((threadIdx.x & 15) == 0) s[(c8 >> 4) * ld_s + r] = sc;
   }
 }
 
 // 128x128 weight tiles: one CTA of 256 threads per tile; thread t holds row
 // t/2, 64 columns.  Optionally writes the transposed codes (dgrad copy).
+// fp32 scales: s [rows/128, K/128], sT [K/128, rows/128] (ld_s, ld_sT unused).
+// kPow2: UE8M0 bytes s [rows, K/32] and sT [K, rows/32], the tile's byte in
+// every 32-block of its rows (an MXFP8 operand and its transposed copy).
 constexpr int kBwTile = 128;
+template <bool kPow2>
 __global__ void __launch_bounds__(256) bw_weight_kernel(
     const uint16_t* __restrict__ w, int64_t rows, int64_t K, int64_t ld_w, uint8_t* __restrict__ q,
-    int64_t ld_q, float* __restrict__ s, uint8_t* __restrict__ qT, int64_t ld_qT,
-    float* __restrict__ sT) {
+    int64_t ld_q, void* __restrict__ s, int64_t ld_s, uint8_t* __restrict__ qT, int64_t ld_qT,
+    void* __restrict__ sT, int64_t ld_sT) {
   __shared__ uint32_t warp_max[8];
   __shared__ float s_tile;
+  __shared__ int k_tile;
   __shared__ __align__(16) uint8_t codes[kBwTile][kBwTile + 16];
   const int kb = blockIdx.x, rb = blockIdx.y;
   const int t = threadIdx.x, r = t >> 1, h = t & 1;
@@ -409,16 +447,30 @@ __global__ void __launch_bounds__(256) bw_weight_kernel(
   if (t == 0) {
     uint32_t m = 0;
     for (int i = 0; i < 8; ++i) m = max(m, warp_max[i]);
-    const float sc = bw_scale(m);
-    s_tile = sc;
-    s[(int64_t)rb * (K / kBwTile) + kb] = sc;
-    if (sT != nullptr) sT[(int64_t)kb * (rows / kBwTile) + rb] = sc;
+    if constexpr (kPow2) {
+      k_tile = bw_pow2_exponent(m);
+    } else {
+      const float sc = bw_scale(m);
+      s_tile = sc;
+      static_cast<float*>(s)[(int64_t)rb * (K / kBwTile) + kb] = sc;
+      if (sT != nullptr) static_cast<float*>(sT)[(int64_t)kb * (rows / kBwTile) + rb] = sc;
+    }
   }
   __syncthreads();
-  const float sc = s_tile;
   uint32_t o[16];
+  if constexpr (kPow2) {
+    const int k = k_tile;
+    const float m = pow2_neg(k);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) bw_quantize8(&v[4 * i], sc, &o[2 * i]);
+    for (int i = 0; i < 8; ++i) bw_quantize8_mul(&v[4 * i], m, &o[2 * i]);
+    if (h == 0)
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s) + ((int64_t)rb * kBwTile + r) * ld_s + kb * 4) =
+          ue8m0x4(k);
+  } else {
+    const float sc = s_tile;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bw_quantize8(&v[4 * i], sc, &o[2 * i]);
+  }
   uint4* dst = reinterpret_cast<uint4*>(q + ((int64_t)rb * kBwTile + r) * ld_q + (int64_t)kb * kBwTile + h * 64);
 #pragma unroll
   for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
@@ -439,15 +491,23 @@ __global__ void __launch_bounds__(256) bw_weight_kernel(
   uint4* tdst = reinterpret_cast<uint4*>(qT + ((int64_t)kb * kBwTile + k) * ld_qT + (int64_t)rb * kBwTile + h * 64);
 #pragma unroll
   for (int i = 0; i < 4; ++i) tdst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  if constexpr (kPow2) {
+    if (h == 0)
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(sT) + ((int64_t)kb * kBwTile + k) * ld_sT + rb * 4) =
+          ue8m0x4(k_tile);
+  }
 }
 
 // Column-wise, segment-padded to 128 (the variable-K wgrad operand): one CTA
 // per (128 padded token positions = one block, 128 columns); thread t owns
 // column t%128 and tokens [64*(t/128), +64).
+// fp32 scales: sT [capacity/128, cols] (block-column-major); kPow2: UE8M0
+// bytes sT [cols, capacity/32], each block's byte in its four 32-blocks.
+template <bool kPow2>
 __global__ void __launch_bounds__(kColThreads) bw_colwise_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
     const int32_t* __restrict__ splits, int G, uint8_t* __restrict__ qT, int64_t ld_q,
-    float* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
+    void* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
     int32_t* status) {
   __shared__ SegTable tab;
   __shared__ __align__(16) uint16_t tile[kColTokens][kColCols + 8];
@@ -487,14 +547,23 @@ __global__ void __launch_bounds__(kColThreads) bw_colwise_kernel(
   __syncthreads();
   am = max(am, half_max[threadIdx.x ^ 128]);
   if (c0 + col >= cols) return;
-  const float sc = bw_scale(am);
   uint32_t o[16];
+  if constexpr (kPow2) {
+    const int k = bw_pow2_exponent(am);
+    const float m = pow2_neg(k);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) bw_quantize8(&w[4 * i], sc, &o[2 * i]);
+    for (int i = 0; i < 8; ++i) bw_quantize8_mul(&w[4 * i], m, &o[2 * i]);
+    if (half == 0)
+      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(sT) + (c0 + col) * ld_s + j0 / 32) = ue8m0x4(k);
+  } else {
+    const float sc = bw_scale(am);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bw_quantize8(&w[4 * i], sc, &o[2 * i]);
+    if (half == 0) static_cast<float*>(sT)[(j0 / kBwTile) * ld_s + c0 + col] = sc;
+  }
   uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + col) * ld_q + j0 + 64 * half);
 #pragma unroll
   for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-  if (half == 0) sT[(j0 / kBwTile) * ld_s + c0 + col] = sc;
 }
 
 }  // namespace
@@ -561,38 +630,51 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
 namespace mxg {
 
 cudaError_t launch_bw_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
-                              int64_t ld_q, float* s, int64_t ld_s, cudaStream_t stream,
+                              int64_t ld_q, void* s, int64_t ld_s, bool pow2, cudaStream_t stream,
                               int num_sms) {
   const int64_t total = rows * (cols / 8);
   int64_t blocks = (total + kRowThreads - 1) / kRowThreads;
   const int64_t cap = (int64_t)num_sms * 8 * 4;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  bw_rowwise_kernel<<<(unsigned)blocks, kRowThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(x), rows, cols, ld_x, static_cast<uint8_t*>(q), ld_q, s, ld_s);
+  auto* xp = static_cast<const uint16_t*>(x);
+  auto* qp = static_cast<uint8_t*>(q);
+  if (pow2)
+    bw_rowwise_kernel<true><<<(unsigned)blocks, kRowThreads, 0, stream>>>(xp, rows, cols, ld_x, qp, ld_q, s, ld_s);
+  else
+    bw_rowwise_kernel<false><<<(unsigned)blocks, kRowThreads, 0, stream>>>(xp, rows, cols, ld_x, qp, ld_q, s, ld_s);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bw_weight(const void* w, int64_t rows, int64_t K, int64_t ld_w, void* q,
-                             int64_t ld_q, float* s, void* qT, int64_t ld_qT, float* sT,
-                             cudaStream_t stream) {
+                             int64_t ld_q, void* s, int64_t ld_s, void* qT, int64_t ld_qT, void* sT,
+                             int64_t ld_sT, bool pow2, cudaStream_t stream) {
   dim3 grid((unsigned)(K / kBwTile), (unsigned)(rows / kBwTile));
-  bw_weight_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(w), rows, K, ld_w,
-                                             static_cast<uint8_t*>(q), ld_q, s,
-                                             static_cast<uint8_t*>(qT), ld_qT, sT);
+  auto* wp = static_cast<const uint16_t*>(w);
+  auto* qp = static_cast<uint8_t*>(q);
+  auto* qTp = static_cast<uint8_t*>(qT);
+  if (pow2)
+    bw_weight_kernel<true><<<grid, 256, 0, stream>>>(wp, rows, K, ld_w, qp, ld_q, s, ld_s, qTp, ld_qT, sT, ld_sT);
+  else
+    bw_weight_kernel<false><<<grid, 256, 0, stream>>>(wp, rows, K, ld_w, qp, ld_q, s, ld_s, qTp, ld_qT, sT, ld_sT);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bw_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
-                              const int32_t* splits, int G, void* qT, int64_t ld_q, float* sT,
+                              const int32_t* splits, int G, void* qT, int64_t ld_q, void* sT,
                               int64_t ld_s, int64_t capacity, int64_t* pad_offsets,
-                              int32_t* status, cudaStream_t stream) {
+                              int32_t* status, bool pow2, cudaStream_t stream) {
   const int64_t gx = (capacity + kColTokens - 1) / kColTokens;
   const int64_t gy = (cols + kColCols - 1) / kColCols;
   dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)gy);
-  bw_colwise_kernel<<<grid, kColThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(x), rows, cols, ld_x, splits, G, static_cast<uint8_t*>(qT), ld_q,
-      sT, ld_s, capacity, pad_offsets, status);
+  auto* xp = static_cast<const uint16_t*>(x);
+  auto* qp = static_cast<uint8_t*>(qT);
+  if (pow2)
+    bw_colwise_kernel<true><<<grid, kColThreads, 0, stream>>>(xp, rows, cols, ld_x, splits, G, qp, ld_q, sT, ld_s,
+                                                             capacity, pad_offsets, status);
+  else
+    bw_colwise_kernel<false><<<grid, kColThreads, 0, stream>>>(xp, rows, cols, ld_x, splits, G, qp, ld_q, sT, ld_s,
+                                                              capacity, pad_offsets, status);
   return cudaGetLastError();
 }
 

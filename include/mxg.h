@@ -296,6 +296,33 @@ mxg_status bw_quantize_colwise_padded(const void* x, int64_t rows, int64_t cols,
                                       int64_t ld_q, float* sT, int64_t ld_s, int64_t capacity,
                                       int64_t* d_pad_offsets, int32_t* d_status, void* stream);
 
+/* Blockwise FP8 with power-of-two scales (the `pow2` option of the PR #716
+ * quantizers; TE's `power_2_scale` default of its blockwise recipe): for each
+ * block, a = max(amax, 1e-4) and s = 2^k, the smallest power of two with
+ * 448 * s >= a; codes q = RNE_satfinite_E4M3(x * 2^-k) (exact scaling).  A
+ * power-of-two scale is a UE8M0 byte (k + 127), so these quantizers write MX
+ * operands: E4M3 codes plus UE8M0 bytes per 32-block, each 128-block's byte
+ * repeated over its four 32-blocks.  The results feed grouped_gemm_fwd /
+ * _dgrad / _wgrad directly (MXFP8 x MXFP8, elem MXG_E4M3), which compute the
+ * same products as the blockwise promotion without it.
+ *   1x128:   x [rows, cols] -> q [rows, cols] (ld_q % 8), s [rows, cols/32]
+ *            (ld_s % 4, s 4-byte aligned); cols % 128 == 0.
+ *   128x128: w [rows, cols] -> q [rows, cols], s [rows, cols/32] and, when
+ *            qT != NULL, the dgrad copy qT [cols, rows] (ld_qT % 16), sT
+ *            [cols, rows/32]; rows, cols % 128 == 0; ld_q % 16, ld_s % 4.
+ *   colwise: as bw_quantize_colwise_padded (segments padded to 128) with
+ *            sT [cols, capacity/32] UE8M0 (ld_s % 4). */
+mxg_status bw_quantize_1x128_pow2(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                  void* q, int64_t ld_q, uint8_t* s, int64_t ld_s, void* stream);
+mxg_status bw_quantize_128x128_pow2(const void* w, int64_t rows, int64_t cols, int64_t ld_w,
+                                    void* q, int64_t ld_q, uint8_t* s, int64_t ld_s, void* qT,
+                                    int64_t ld_qT, uint8_t* sT, int64_t ld_sT, void* stream);
+mxg_status bw_quantize_colwise_padded_pow2(const void* x, int64_t rows, int64_t cols,
+                                           int64_t ld_x, const int32_t* d_m_splits, int32_t G,
+                                           void* qT, int64_t ld_q, uint8_t* sT, int64_t ld_s,
+                                           int64_t capacity, int64_t* d_pad_offsets,
+                                           int32_t* d_status, void* stream);
+
 /* Grouped blockwise-FP8 GEMMs (tcgen05 kind::f8f6f4 + per-128-K promotion in
  * fp32).  Same passes, split validation and output conventions as the MX
  * GEMMs; N and K multiples of 128; the wgrad padding is 128.

@@ -169,3 +169,107 @@ def test_bw_gemm_rejects_bad_splits():
     with pytest.raises(mxg.MXGError) as ei:
         mxg.check_status(st)
     assert ei.value.code == 4 and (out == 5.0).all()
+
+
+# ------------------------------------------------------------- power-of-two scales (MX operands)
+
+def _ue8m0(s, rep_rows=1, rep_cols=4):
+    """UE8M0 bytes of power-of-two fp32 scales, each repeated over its rows and
+    its four 32-blocks (the MX layout the pow2 quantizers write)."""
+    k = np.frexp(np.asarray(s, dtype=np.float64))[1] - 1
+    b = (k + 127).astype(np.uint8)
+    return np.repeat(np.repeat(b, rep_rows, axis=-2), rep_cols, axis=-1)
+
+
+@pytest.mark.parametrize("shape", [(1, 128), (37, 384), (1000, 4096)])
+def test_bw_1x128_pow2_bit_exact(shape):
+    rng = np.random.default_rng(shape[0] + 7)
+    x = synth.normal_bf16(rng, shape, std=4.0, outlier_frac=0.02)
+    if shape[0] > 4:
+        v = synth.bf16_bits_to_f32(x)
+        x[1] = synth.f32_to_bf16_bits(v[1] * np.float32(1e-7))   # below the 1e-4 floor
+        x[2, :128] = 0
+        x[3, :128] = synth.f32_to_bf16_bits(np.full(128, -448.0, np.float32))   # exact fit, s = 1
+    op = _mxg().bw_quantize_1x128_pow2(bf16_to_dev(x))
+    torch.cuda.synchronize()
+    codes, s = oracle.quantize_bw_1x128(x, pow2=True)
+    assert np.array_equal(op.data.cpu().numpy(), codes)
+    assert np.array_equal(op.scale.cpu().numpy(), _ue8m0(s))
+
+
+def test_bw_128x128_pow2_and_dgrad_copy_bit_exact():
+    rng = np.random.default_rng(4)
+    G, N, K = 2, 256, 384
+    w = synth.normal_bf16(rng, (G * N, K), std=3.0, outlier_frac=0.02)
+    op, opT = _mxg().bw_quantize_128x128_pow2(bf16_to_dev(w))
+    torch.cuda.synchronize()
+    codes, s = oracle.quantize_bw_128x128(w.reshape(G, N, K), pow2=True)
+    assert np.array_equal(op.data.cpu().numpy(), codes.reshape(G * N, K))
+    assert np.array_equal(op.scale.cpu().numpy(), _ue8m0(s.reshape(G * N // 128, K // 128), 128, 4))
+    ct, st = transpose_bw_128x128(codes, s)
+    assert np.array_equal(opT.data.cpu().numpy(), np.concatenate(list(ct), axis=1))
+    assert np.array_equal(opT.scale.cpu().numpy(), _ue8m0(np.concatenate(list(st), axis=1), 128, 4))
+
+
+@pytest.mark.parametrize("splits,cols", [([200, 0, 1, 128, 55], 128), ([0, 0, 300], 256)])
+def test_bw_colwise_padded_pow2_bit_exact(splits, cols):
+    rng = np.random.default_rng(len(splits) + cols + 1)
+    splits = np.array(splits, dtype=np.int32)
+    x = synth.normal_bf16(rng, (int(splits.sum()), cols), std=3.0, outlier_frac=0.02)
+    op, poff = _mxg().bw_quantize_colwise_padded_pow2(bf16_to_dev(x), i32_to_dev(splits), check=True)
+    codes, s, p = oracle.quantize_bw_colwise_padded(x, splits, pow2=True)
+    spad = int(p[-1])
+    assert np.array_equal(poff.cpu().numpy(), p)
+    assert np.array_equal(op.data.cpu().numpy()[:, :spad], codes)
+    assert np.array_equal(op.scale.cpu().numpy()[:, : spad // 32], _ue8m0(s))
+
+
+def _mx_dev(codes, ue8m0, cols):
+    return _mxg().MXOperand(_u8_dev(codes), _u8_dev(ue8m0), "e4m3", cols)
+
+
+def test_pow2_blockwise_step_on_the_mx_gemms():
+    """The pow2 blockwise recipe runs on the MXFP8 GEMMs: fwd, dgrad and wgrad
+    against the oracle's per-expert contraction of the dequantized blockwise
+    operands."""
+    mxg = _mxg()
+    splits = np.array([200, 0, 77, 300, 129], dtype=np.int32)
+    G, S, N, K = len(splits), int(splits.sum()), 256, 384
+    rng = np.random.default_rng(31)
+    x = synth.normal_bf16(rng, (S, K), outlier_frac=0.01)
+    dy = synth.normal_bf16(rng, (S, N), outlier_frac=0.01)
+    w = synth.normal_bf16(rng, (G * N, K), outlier_frac=0.01)
+    d_splits = i32_to_dev(splits)
+    # operands quantized by the oracle
+    xc, xs = oracle.quantize_bw_1x128(x, pow2=True)
+    dyc, dys = oracle.quantize_bw_1x128(dy, pow2=True)
+    wc, ws = oracle.quantize_bw_128x128(w.reshape(G, N, K), pow2=True)
+    ct, st = transpose_bw_128x128(wc, ws)
+    Xd, dYd = oracle.dequantize_bw_1x128(xc, xs), oracle.dequantize_bw_1x128(dyc, dys)
+    Wd = oracle.dequantize_bw_128x128(wc, ws).reshape(G * N, K)
+    Wtd = np.concatenate(list(oracle.dequantize_bw_128x128(ct, st)), axis=1)
+    A = _mx_dev(xc, _ue8m0(xs), K)
+    Wm = _mx_dev(wc.reshape(G * N, K), _ue8m0(ws.reshape(G * N // 128, K // 128), 128, 4), K)
+    dYm = _mx_dev(dyc, _ue8m0(dys), N)
+    Wt = _mx_dev(np.concatenate(list(ct), axis=1), _ue8m0(np.concatenate(list(st), axis=1), 128, 4), G * N)
+    Y = mxg.grouped_gemm_fwd(A, Wm, d_splits, N, check=True)
+    oracle.assert_gemm_close(Y.float().cpu().numpy(), oracle.grouped_fwd(Xd, Wd, splits, N), "pow2 fwd")
+    dX = mxg.grouped_gemm_dgrad(dYm, Wt, d_splits, check=True)
+    oracle.assert_gemm_close(dX.float().cpu().numpy(), oracle.grouped_dgrad(dYd, Wtd, splits), "pow2 dgrad")
+    # wgrad on the column-wise operands (segments padded to 128)
+    cap = synth.padded_rows_capacity(S, G, 128)
+    dytc, dyts, poff = oracle.quantize_bw_colwise_padded(dy, splits, pow2=True)
+    xtc, xts, _ = oracle.quantize_bw_colwise_padded(x, splits, pow2=True)
+    spad = int(poff[-1])
+
+    def full(codes, s, C):
+        fc = np.zeros((C, cap), dtype=np.uint8)
+        fc[:, :spad] = codes
+        fs = np.full((C, cap // 32), 127, dtype=np.uint8)
+        fs[:, : spad // 32] = _ue8m0(s)
+        return _mx_dev(fc, fs, cap)
+
+    out = torch.zeros((G, N, K), dtype=torch.float32, device="cuda:0")
+    mxg.grouped_gemm_wgrad(full(dytc, dyts, N), full(xtc, xts, K), d_splits, S, 128, out=out, check=True)
+    ref = oracle.grouped_wgrad(oracle.dequantize_bw_1x128(dytc, dyts), oracle.dequantize_bw_1x128(xtc, xts), poff)
+    oracle.assert_gemm_close(out.cpu().numpy(), ref, "pow2 wgrad")
