@@ -453,7 +453,7 @@ mxg_status bw_quantize_128x128(const void* w, int64_t rows, int64_t cols, int64_
   DeviceGuard g(dev);
   if (!g.ok) return MXG_ERR_CUDA;
   return cuda_status(launch_bw_weight(w, rows, cols, ld_w, q, ld_q, s, 0, qT, ld_qT, sT, 0, false,
-                                      static_cast<cudaStream_t>(stream)));
+                                      static_cast<cudaStream_t>(stream), sms));
 }
 
 mxg_status bw_quantize_colwise_padded(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -477,7 +477,7 @@ mxg_status bw_quantize_colwise_padded(const void* x, int64_t rows, int64_t cols,
   if (!g.ok) return MXG_ERR_CUDA;
   return cuda_status(launch_bw_colwise(x, rows, cols, ld_x, d_m_splits, G, qT, ld_q, sT, ld_s,
                                        capacity, d_pad_offsets, d_status, false,
-                                       static_cast<cudaStream_t>(stream)));
+                                       static_cast<cudaStream_t>(stream), sms));
 }
 
 // ---- power-of-two blockwise scales, written as MX (UE8M0 per 32) operands
@@ -519,7 +519,7 @@ mxg_status bw_quantize_128x128_pow2(const void* w, int64_t rows, int64_t cols, i
   DeviceGuard g(dev);
   if (!g.ok) return MXG_ERR_CUDA;
   return cuda_status(launch_bw_weight(w, rows, cols, ld_w, q, ld_q, s, ld_s, qT, ld_qT, sT, ld_sT,
-                                      true, static_cast<cudaStream_t>(stream)));
+                                      true, static_cast<cudaStream_t>(stream), sms));
 }
 
 mxg_status bw_quantize_colwise_padded_pow2(const void* x, int64_t rows, int64_t cols,
@@ -544,7 +544,7 @@ mxg_status bw_quantize_colwise_padded_pow2(const void* x, int64_t rows, int64_t 
   if (!g.ok) return MXG_ERR_CUDA;
   return cuda_status(launch_bw_colwise(x, rows, cols, ld_x, d_m_splits, G, qT, ld_q, sT, ld_s,
                                        capacity, d_pad_offsets, d_status, true,
-                                       static_cast<cudaStream_t>(stream)));
+                                       static_cast<cudaStream_t>(stream), sms));
 }
 
 size_t bw_gemm_workspace_size(int32_t G) {

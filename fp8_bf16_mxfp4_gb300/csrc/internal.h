@@ -27,11 +27,11 @@ cudaError_t launch_bw_rowwise(const void* x, int64_t rows, int64_t cols, int64_t
                               int num_sms);
 cudaError_t launch_bw_weight(const void* w, int64_t rows, int64_t K, int64_t ld_w, void* q,
                              int64_t ld_q, void* s, int64_t ld_s, void* qT, int64_t ld_qT, void* sT,
-                             int64_t ld_sT, bool pow2, cudaStream_t stream);
+                             int64_t ld_sT, bool pow2, cudaStream_t stream, int num_sms);
 cudaError_t launch_bw_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                               const int32_t* splits, int G, void* qT, int64_t ld_q, void* sT,
                               int64_t ld_s, int64_t capacity, int64_t* pad_offsets,
-                              int32_t* status, bool pow2, cudaStream_t stream);
+                              int32_t* status, bool pow2, cudaStream_t stream, int num_sms);
 
 // Grouped MX GEMM (tcgen05 block-scaled).  See gemm_mx.cu.
 struct GemmArgs {

@@ -166,6 +166,49 @@ __device__ int find_segment(const SegTable& t, int G, int64_t j) {
   return lo;  // the last such g is non-empty since poff[g+1] > j
 }
 
+// Blockwise FP8 arithmetic (see the blockwise section below).
+constexpr float kBwAmaxFloor = 1e-4f;
+
+MXG_DEVINL float bw_scale(uint32_t amax_bits) {
+  const float a = fmaxf(__uint_as_float(amax_bits << 16), kBwAmaxFloor);
+  return __fdiv_rn(a, 448.0f);
+}
+
+// Power-of-two form: s = 2^k, the smallest power of two with 448 * s >= a,
+// a = max(amax, 1e-4f) = m * 2^e with m in [1, 2).  Since 448 = 1.75 * 2^8,
+// k = e - 8, plus one when m > 1.75.  k is in [-22, 120] for finite BF16
+// input, so the UE8M0 byte k + 127 is an MX scale and x / s = x * 2^-k exactly.
+MXG_DEVINL int bw_pow2_exponent(uint32_t amax_bits) {
+  const float a = fmaxf(__uint_as_float(amax_bits << 16), kBwAmaxFloor);
+  const uint32_t b = __float_as_uint(a);
+  return (int)((b >> 23) & 0xFFu) - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+}
+MXG_DEVINL uint32_t ue8m0x4(int k) { return (uint32_t)(k + 127) * 0x01010101u; }
+
+// 8 bf16 (four words) * m (a power of two) -> 8 E4M3 codes (two words).
+MXG_DEVINL void bw_quantize8_mul(const uint32_t* w, float m, uint32_t* o) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16lo_to_f32(w[i]) * m;
+    v[2 * i + 1] = bf16hi_to_f32(w[i]) * m;
+  }
+  o[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]);
+  o[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]);
+}
+
+// 8 bf16 (four words) / s -> 8 E4M3 codes (two words).
+MXG_DEVINL void bw_quantize8(const uint32_t* w, float s, uint32_t* o) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __fdiv_rn(bf16lo_to_f32(w[i]), s);
+    v[2 * i + 1] = __fdiv_rn(bf16hi_to_f32(w[i]), s);
+  }
+  o[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]);
+  o[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]);
+}
+
 // Quantizes one 32-element block (16 words of bf16 pairs, element 2i in the
 // low half) and writes its codes and scale.
 template <int kElem>
@@ -194,6 +237,30 @@ MXG_DEVINL void emit_col_block(const uint32_t* w, uint8_t* qrow, uint8_t* srow) 
   *srow = (uint8_t)(e + 127);
 }
 
+// One column's quarter (32 tokens, 16 words) of a 128-token blockwise block
+// whose amax over the four quarters is `am`: E4M3 codes (32 bytes) and, from
+// the first quarter, the block's scale -- fp32 at sT[(j0/128)*ld_s + col]
+// (kBw 1) or the UE8M0 byte repeated four times at sT + col*ld_s + j0/32 (kBw 2).
+template <int kBw>
+MXG_DEVINL void emit_bw_col(const uint32_t* w, uint32_t am, uint8_t* q, void* sT, int64_t ld_s,
+                            int64_t col, int64_t j0, bool first_quarter) {
+  uint32_t o[8];
+  if constexpr (kBw == 2) {
+    const int k = bw_pow2_exponent(am);
+    const float m = pow2_neg(k);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bw_quantize8_mul(&w[4 * i], m, &o[2 * i]);
+    if (first_quarter) *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(sT) + col * ld_s + j0 / 32) = ue8m0x4(k);
+  } else {
+    const float sc = bw_scale(am);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bw_quantize8(&w[4 * i], sc, &o[2 * i]);
+    if (first_quarter) static_cast<float*>(sT)[(j0 / 128) * ld_s + col] = sc;
+  }
+  __stcs(reinterpret_cast<uint4*>(q), make_uint4(o[0], o[1], o[2], o[3]));
+  __stcs(reinterpret_cast<uint4*>(q) + 1, make_uint4(o[4], o[5], o[6], o[7]));
+}
+
 // Persistent CTAs over tiles of 128 padded token positions x 128 columns
 // (tile = token tile * column tiles + column tile), kColCtasPerSm per SM.
 // The expert table is built once per CTA.  For each tile the source row of
@@ -211,16 +278,22 @@ MXG_DEVINL void emit_col_block(const uint32_t* w, uint8_t* qrow, uint8_t* srow) 
 // quantizer, one HBM read of x for both): each real token row of the staged
 // tile is quantized along the columns, four 32-blocks per row and tile, and
 // written at its source row; padding positions write nothing.
+//
+// kBw (blockwise FP8 column-wise operand, segments padded to 128, E4M3): a
+// tile is one 128-token block; the four lanes of a column pair reduce the
+// block's amax with two shuffles and each quantizes its 32 tokens (kBw 1:
+// fp32 scales, kBw 2: power-of-two scales as UE8M0, see emit_bw_col).
 constexpr int kColCtasPerSm = 2;
 
-template <int kElem, bool kDual>
+template <int kElem, bool kDual, int kBw = 0>
 __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
     const int32_t* __restrict__ splits, int G, int pad, uint8_t* __restrict__ qT, int64_t ld_q,
-    uint8_t* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
+    void* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
     int32_t* status, uint8_t* __restrict__ q_row, int64_t ld_qr, uint8_t* __restrict__ s_row,
     int64_t ld_sr) {
   static_assert(kColTokens == 128 && kColCols == 128 && kColThreads == 256, "thread mapping");
+  static_assert(!(kDual && kBw), "the dual pass is MX only");
   __shared__ SegTable tab;
   __shared__ __align__(16) uint32_t tile[kColTokens * (kColCols / 2) + 4 * 8];
   __shared__ int64_t src_row[2][kColTokens];  // source row of each position, or -1
@@ -282,19 +355,40 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
 
     const int64_t jb = (tile_id / ntc) * kColTokens + 32 * blk;
     const int64_t col = (tile_id % ntc) * kColCols + 2 * cp;
-    if (jb < ptot && col < cols) {  // beyond the last expert: nothing written
-      const uint32_t* tp = tile + (32 * blk) * 64 + blk * 8 + cp;
-      uint32_t wa[16], wb[16];
+    const uint32_t* tp = tile + (32 * blk) * 64 + blk * 8 + cp;
+    uint32_t wa[16], wb[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t t0 = tp[(2 * i) * 64], t1 = tp[(2 * i + 1) * 64];
+      wa[i] = __byte_perm(t0, t1, 0x5410);  // column col:   tokens 2i, 2i+1
+      wb[i] = __byte_perm(t0, t1, 0x7632);  // column col+1
+    }
+    if constexpr (kBw == 0) {
+      if (jb < ptot && col < cols) {  // beyond the last expert: nothing written
+        const int64_t qoff = (jb >> 5) * kBytesPerBlock;
+        uint8_t* s8 = static_cast<uint8_t*>(sT);
+        emit_col_block<kElem>(wa, qT + col * ld_q + qoff, s8 + col * ld_s + (jb >> 5));
+        if (col + 1 < cols)
+          emit_col_block<kElem>(wb, qT + (col + 1) * ld_q + qoff, s8 + (col + 1) * ld_s + (jb >> 5));
+      }
+    } else {
+      // the 128-token block's amax over the four quarter lanes (all lanes
+      // take part; validity is uniform per warp: cols % 32 == 0, ptot % 128 == 0)
+      uint32_t ama = 0, amb = 0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const uint32_t t0 = tp[(2 * i) * 64], t1 = tp[(2 * i + 1) * 64];
-        wa[i] = __byte_perm(t0, t1, 0x5410);  // column col:   tokens 2i, 2i+1
-        wb[i] = __byte_perm(t0, t1, 0x7632);  // column col+1
+        ama = max(ama, bf16x2_absmax_bits(wa[i]));
+        amb = max(amb, bf16x2_absmax_bits(wb[i]));
       }
-      const int64_t qoff = (jb >> 5) * kBytesPerBlock;
-      emit_col_block<kElem>(wa, qT + col * ld_q + qoff, sT + col * ld_s + (jb >> 5));
-      if (col + 1 < cols)
-        emit_col_block<kElem>(wb, qT + (col + 1) * ld_q + qoff, sT + (col + 1) * ld_s + (jb >> 5));
+      ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 1));
+      ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 2));
+      amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 1));
+      amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 2));
+      if (jb < ptot && col < cols) {
+        const int64_t j0 = jb - 32 * blk;
+        emit_bw_col<kBw>(wa, ama, qT + col * ld_q + jb, sT, ld_s, col, j0, blk == 0);
+        if (col + 1 < cols) emit_bw_col<kBw>(wb, amb, qT + (col + 1) * ld_q + jb, sT, ld_s, col + 1, j0, blk == 0);
+      }
     }
     if constexpr (kDual) {
       // row-wise blocks: thread -> token row tid/2, 32-blocks 2*(tid%2) and +1
@@ -332,238 +426,156 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
 // 128-block kb) at s[kb * ld_s + r], so a GEMM epilogue thread holding row r
 // reads its scales with coalesced loads.
 // ---------------------------------------------------------------------------
-constexpr float kBwAmaxFloor = 1e-4f;
-
-MXG_DEVINL float bw_scale(uint32_t amax_bits) {
-  const float a = fmaxf(__uint_as_float(amax_bits << 16), kBwAmaxFloor);
-  return __fdiv_rn(a, 448.0f);
-}
-
-// Power-of-two form: s = 2^k, the smallest power of two with 448 * s >= a,
-// a = max(amax, 1e-4f) = m * 2^e with m in [1, 2).  Since 448 = 1.75 * 2^8,
-// k = e - 8, plus one when m > 1.75.  k is in [-22, 120] for finite BF16
-// input, so the UE8M0 byte k + 127 is an MX scale and x / s = x * 2^-k exactly.
-MXG_DEVINL int bw_pow2_exponent(uint32_t amax_bits) {
-  const float a = fmaxf(__uint_as_float(amax_bits << 16), kBwAmaxFloor);
-  const uint32_t b = __float_as_uint(a);
-  return (int)((b >> 23) & 0xFFu) - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-}
-MXG_DEVINL uint32_t ue8m0x4(int k) { return (uint32_t)(k + 127) * 0x01010101u; }
-
-// 8 bf16 (four words) * m (a power of two) -> 8 E4M3 codes (two words).
-MXG_DEVINL void bw_quantize8_mul(const uint32_t* w, float m, uint32_t* o) {
-  float v[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = bf16lo_to_f32(w[i]) * m;
-    v[2 * i + 1] = bf16hi_to_f32(w[i]) * m;
-  }
-  o[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]);
-  o[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]);
-}
-
-// 8 bf16 (four words) / s -> 8 E4M3 codes (two words).
-MXG_DEVINL void bw_quantize8(const uint32_t* w, float s, uint32_t* o) {
-  float v[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __fdiv_rn(bf16lo_to_f32(w[i]), s);
-    v[2 * i + 1] = __fdiv_rn(bf16hi_to_f32(w[i]), s);
-  }
-  o[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]);
-  o[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]);
-}
-
-// 1x128 along the row: 16 lanes per block, 8 values (16 bytes) per lane.
+// 1x128 along the row: four lanes per block, 32 values (four 16-byte loads)
+// per lane; the block amax is reduced over the four lanes with two shuffles.
 // kPow2: power-of-two scales written as UE8M0 bytes [rows, cols/32], each
 // block's byte repeated over its four 32-blocks (an MXFP8 operand).
 template <bool kPow2>
 __global__ void __launch_bounds__(kRowThreads) bw_rowwise_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
     uint8_t* __restrict__ q, int64_t ld_q, void* __restrict__ s, int64_t ld_s) {
-  const int64_t chunks_per_row = cols >> 3;
-  const int64_t total = rows * chunks_per_row;
+  const int64_t b32_per_row = cols >> 5;
+  const int64_t total = rows * b32_per_row;
   const int64_t step = (int64_t)gridDim.x * kRowThreads;
   for (int64_t base = (int64_t)blockIdx.x * kRowThreads; base < total; base += step) {
     const int64_t t = base + threadIdx.x;
-    const bool live = t < total;
-    const int64_t r = live ? t / chunks_per_row : 0;
-    const int64_t c8 = live ? t - r * chunks_per_row : 0;
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (live) raw = __ldcs(reinterpret_cast<const uint4*>(x + r * ld_x + c8 * 8));
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t am = max(max(bf16x2_absmax_bits(w[0]), bf16x2_absmax_bits(w[1])),
-                      max(bf16x2_absmax_bits(w[2]), bf16x2_absmax_bits(w[3])));
+    const bool live = t < total;  // total % 4 == 0: a block's four lanes live or die together
+    const int64_t r = live ? t / b32_per_row : 0;
+    const int64_t b = live ? t - r * b32_per_row : 0;
+    uint32_t w[16];
+    if (live) {
+      const uint4* src = reinterpret_cast<const uint4*>(x + r * ld_x + b * 32);
 #pragma unroll
-    for (int d = 1; d < 16; d <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = __ldcs(src + i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = 0;
+    }
+    uint32_t am = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) am = max(am, bf16x2_absmax_bits(w[i]));
+    am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
     if (!live) continue;
-    uint32_t o[2];
+    uint32_t o[8];
+    const bool first = (b & 3) == 0;
     if constexpr (kPow2) {
       const int k = bw_pow2_exponent(am);
-      bw_quantize8_mul(w, pow2_neg(k), o);
-      if ((threadIdx.x & 15) == 0)
-        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s) + r * ld_s + (c8 >> 4) * 4) = ue8m0x4(k);
+      const float m = pow2_neg(k);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) bw_quantize8_mul(&w[4 * i], m, &o[2 * i]);
+      if (first)
+        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s) + r * ld_s + b) = ue8m0x4(k);
     } else {
       const float sc = bw_scale(am);
-      bw_quantize8(w, sc, o);
-      if ((threadIdx.x & 15) == 0) static_cast<float*>(s)[(c8 >> 4) * ld_s + r] = sc;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) bw_quantize8(&w[4 * i], sc, &o[2 * i]);
+      if (first) static_cast<float*>(s)[(b >> 2) * ld_s + r] = sc;
     }
-    *reinterpret_cast<uint2*>(q + r * ld_q + c8 * 8) = make_uint2(o[0], o[1]);
+    uint2* dst = reinterpret_cast<uint2*>(q + r * ld_q + b * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint2(o[2 * i], o[2 * i + 1]);
   }
 }
 
-// 128x128 weight tiles: one CTA of 256 threads per tile; thread t holds row
-// t/2, 64 columns.  Optionally writes the transposed codes (dgrad copy).
+// 128x128 weight tiles, persistent CTAs of 256 threads (kWCtasPerSm per SM)
+// over tiles in row-of-blocks order; thread t holds row t/2, 64 columns, and
+// its eight 16-byte loads of the next tile are in flight while the current
+// tile is quantized.  Optionally writes the transposed codes (dgrad copy).
 // fp32 scales: s [rows/128, K/128], sT [K/128, rows/128] (ld_s, ld_sT unused).
 // kPow2: UE8M0 bytes s [rows, K/32] and sT [K, rows/32], the tile's byte in
 // every 32-block of its rows (an MXFP8 operand and its transposed copy).
 constexpr int kBwTile = 128;
+constexpr int kWCtasPerSm = 2;
 template <bool kPow2>
-__global__ void __launch_bounds__(256) bw_weight_kernel(
+__global__ void __launch_bounds__(256, kWCtasPerSm) bw_weight_kernel(
     const uint16_t* __restrict__ w, int64_t rows, int64_t K, int64_t ld_w, uint8_t* __restrict__ q,
     int64_t ld_q, void* __restrict__ s, int64_t ld_s, uint8_t* __restrict__ qT, int64_t ld_qT,
     void* __restrict__ sT, int64_t ld_sT) {
   __shared__ uint32_t warp_max[8];
-  __shared__ float s_tile;
-  __shared__ int k_tile;
   __shared__ __align__(16) uint8_t codes[kBwTile][kBwTile + 16];
-  const int kb = blockIdx.x, rb = blockIdx.y;
   const int t = threadIdx.x, r = t >> 1, h = t & 1;
-  const uint4* src = reinterpret_cast<const uint4*>(w + ((int64_t)rb * kBwTile + r) * ld_w +
-                                                    (int64_t)kb * kBwTile + h * 64);
+  const int64_t nkb = K / kBwTile;
+  const int64_t ntiles = nkb * (rows / kBwTile);
+  int64_t id = blockIdx.x;
+  if (id >= ntiles) return;
+  auto load = [&](int64_t tile, uint32_t* v) {
+    const int64_t rb = tile / nkb, kb = tile - rb * nkb;
+    const uint4* src = reinterpret_cast<const uint4*>(w + (rb * kBwTile + r) * ld_w + kb * kBwTile + h * 64);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 u = __ldcs(src + i);
+      v[4 * i] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
+    }
+  };
   uint32_t v[32];
+  load(id, v);
+  for (; id < ntiles; id += gridDim.x) {
+    const int64_t rb = id / nkb, kb = id - rb * nkb;
+    uint32_t am = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 u = __ldcs(src + i);
-    v[4 * i] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
-  }
-  uint32_t am = 0;
+    for (int i = 0; i < 32; ++i) am = max(am, bf16x2_absmax_bits(v[i]));
 #pragma unroll
-  for (int i = 0; i < 32; ++i) am = max(am, bf16x2_absmax_bits(v[i]));
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
-  if ((t & 31) == 0) warp_max[t >> 5] = am;
-  __syncthreads();
-  if (t == 0) {
+    for (int d = 16; d > 0; d >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
+    if ((t & 31) == 0) warp_max[t >> 5] = am;
+    const int64_t nxt = id + gridDim.x;
+    uint32_t pv[32];
+    if (nxt < ntiles) load(nxt, pv);
+    __syncthreads();
     uint32_t m = 0;
-    for (int i = 0; i < 8; ++i) m = max(m, warp_max[i]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = max(m, warp_max[i]);  // every thread: the tile amax
+    uint32_t o[16];
+    int k2 = 0;
     if constexpr (kPow2) {
-      k_tile = bw_pow2_exponent(m);
+      k2 = bw_pow2_exponent(m);
+      const float mul = pow2_neg(k2);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) bw_quantize8_mul(&v[4 * i], mul, &o[2 * i]);
+      if (h == 0)
+        *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s) + (rb * kBwTile + r) * ld_s + kb * 4) = ue8m0x4(k2);
     } else {
       const float sc = bw_scale(m);
-      s_tile = sc;
-      static_cast<float*>(s)[(int64_t)rb * (K / kBwTile) + kb] = sc;
-      if (sT != nullptr) static_cast<float*>(sT)[(int64_t)kb * (rows / kBwTile) + rb] = sc;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) bw_quantize8(&v[4 * i], sc, &o[2 * i]);
+      if (t == 0) {
+        static_cast<float*>(s)[rb * nkb + kb] = sc;
+        if (sT != nullptr) static_cast<float*>(sT)[kb * (rows / kBwTile) + rb] = sc;
+      }
     }
+    uint4* dst = reinterpret_cast<uint4*>(q + (rb * kBwTile + r) * ld_q + kb * kBwTile + h * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    if (qT != nullptr) {  // uniform
+      uint4* crow = reinterpret_cast<uint4*>(&codes[r][h * 64]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) crow[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      __syncthreads();
+      // transposed: thread t writes row kk = t/2 of the [K, rows] copy, 64 codes
+      const int kk = t >> 1;
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int j = h * 64 + 4 * i;
+        pk[i] = (uint32_t)codes[j][kk] | ((uint32_t)codes[j + 1][kk] << 8) |
+                ((uint32_t)codes[j + 2][kk] << 16) | ((uint32_t)codes[j + 3][kk] << 24);
+      }
+      uint4* tdst = reinterpret_cast<uint4*>(qT + (kb * kBwTile + kk) * ld_qT + rb * kBwTile + h * 64);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tdst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      if constexpr (kPow2) {
+        if (h == 0)
+          *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(sT) + (kb * kBwTile + kk) * ld_sT + rb * 4) =
+              ue8m0x4(k2);
+      }
+    }
+    __syncthreads();  // warp_max and codes are rewritten next iteration
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = pv[i];
   }
-  __syncthreads();
-  uint32_t o[16];
-  if constexpr (kPow2) {
-    const int k = k_tile;
-    const float m = pow2_neg(k);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) bw_quantize8_mul(&v[4 * i], m, &o[2 * i]);
-    if (h == 0)
-      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(s) + ((int64_t)rb * kBwTile + r) * ld_s + kb * 4) =
-          ue8m0x4(k);
-  } else {
-    const float sc = s_tile;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) bw_quantize8(&v[4 * i], sc, &o[2 * i]);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(q + ((int64_t)rb * kBwTile + r) * ld_q + (int64_t)kb * kBwTile + h * 64);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-  if (qT == nullptr) return;
-  uint4* crow = reinterpret_cast<uint4*>(&codes[r][h * 64]);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) crow[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-  __syncthreads();
-  // transposed: thread t writes row k = t/2 of the [K, rows] copy, 64 codes
-  const int k = t >> 1;
-  uint32_t pk[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int j = h * 64 + 4 * i;
-    pk[i] = (uint32_t)codes[j][k] | ((uint32_t)codes[j + 1][k] << 8) |
-            ((uint32_t)codes[j + 2][k] << 16) | ((uint32_t)codes[j + 3][k] << 24);
-  }
-  uint4* tdst = reinterpret_cast<uint4*>(qT + ((int64_t)kb * kBwTile + k) * ld_qT + (int64_t)rb * kBwTile + h * 64);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) tdst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-  if constexpr (kPow2) {
-    if (h == 0)
-      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(sT) + ((int64_t)kb * kBwTile + k) * ld_sT + rb * 4) =
-          ue8m0x4(k_tile);
-  }
-}
-
-// Column-wise, segment-padded to 128 (the variable-K wgrad operand): one CTA
-// per (128 padded token positions = one block, 128 columns); thread t owns
-// column t%128 and tokens [64*(t/128), +64).
-// fp32 scales: sT [capacity/128, cols] (block-column-major); kPow2: UE8M0
-// bytes sT [cols, capacity/32], each block's byte in its four 32-blocks.
-template <bool kPow2>
-__global__ void __launch_bounds__(kColThreads) bw_colwise_kernel(
-    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
-    const int32_t* __restrict__ splits, int G, uint8_t* __restrict__ qT, int64_t ld_q,
-    void* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
-    int32_t* status) {
-  __shared__ SegTable tab;
-  __shared__ __align__(16) uint16_t tile[kColTokens][kColCols + 8];
-  __shared__ uint32_t half_max[kColThreads];
-  const bool first = blockIdx.x == 0 && blockIdx.y == 0;
-  if (!build_seg_table(tab, splits, G, rows, kBwTile, capacity, status, first)) return;
-  if (first && pad_offsets != nullptr) {
-    for (int g = threadIdx.x; g <= G; g += blockDim.x) pad_offsets[g] = tab.poff[g];
-  }
-  const int64_t j0 = (int64_t)blockIdx.x * kColTokens;
-  if (j0 >= tab.poff[G]) return;
-  const int64_t c0 = (int64_t)blockIdx.y * kColCols;
-  const int g = find_segment(tab, G, j0);  // the whole block belongs to one expert
-  const int64_t tok0 = j0 - tab.poff[g];
-  const int64_t mg = tab.off[g + 1] - tab.off[g];
-  for (int idx = threadIdx.x; idx < kColTokens * (kColCols / 8); idx += kColThreads) {
-    const int jr = idx / (kColCols / 8);
-    const int cc = (idx % (kColCols / 8)) * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (tok0 + jr < mg && c0 + cc < cols)
-      v = __ldcs(reinterpret_cast<const uint4*>(x + (tab.off[g] + tok0 + jr) * ld_x + c0 + cc));
-    *reinterpret_cast<uint4*>(&tile[jr][cc]) = v;
-  }
-  __syncthreads();
-  const int col = threadIdx.x & (kColCols - 1);
-  const int half = threadIdx.x >> 7;
-  uint32_t w[32];
-  uint32_t am = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t lo = tile[64 * half + 2 * i][col];
-    const uint32_t hi = tile[64 * half + 2 * i + 1][col];
-    w[i] = lo | (hi << 16);
-    am = max(am, bf16x2_absmax_bits(w[i]));
-  }
-  half_max[threadIdx.x] = am;
-  __syncthreads();
-  am = max(am, half_max[threadIdx.x ^ 128]);
-  if (c0 + col >= cols) return;
-  uint32_t o[16];
-  if constexpr (kPow2) {
-    const int k = bw_pow2_exponent(am);
-    const float m = pow2_neg(k);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) bw_quantize8_mul(&w[4 * i], m, &o[2 * i]);
-    if (half == 0)
-      *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(sT) + (c0 + col) * ld_s + j0 / 32) = ue8m0x4(k);
-  } else {
-    const float sc = bw_scale(am);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) bw_quantize8(&w[4 * i], sc, &o[2 * i]);
-    if (half == 0) static_cast<float*>(sT)[(j0 / kBwTile) * ld_s + c0 + col] = sc;
-  }
-  uint4* dst = reinterpret_cast<uint4*>(qT + (c0 + col) * ld_q + j0 + 64 * half);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
 }
 
 }  // namespace
@@ -632,7 +644,7 @@ namespace mxg {
 cudaError_t launch_bw_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
                               int64_t ld_q, void* s, int64_t ld_s, bool pow2, cudaStream_t stream,
                               int num_sms) {
-  const int64_t total = rows * (cols / 8);
+  const int64_t total = rows * (cols / 32);
   int64_t blocks = (total + kRowThreads - 1) / kRowThreads;
   const int64_t cap = (int64_t)num_sms * 8 * 4;
   if (blocks > cap) blocks = cap;
@@ -648,33 +660,40 @@ cudaError_t launch_bw_rowwise(const void* x, int64_t rows, int64_t cols, int64_t
 
 cudaError_t launch_bw_weight(const void* w, int64_t rows, int64_t K, int64_t ld_w, void* q,
                              int64_t ld_q, void* s, int64_t ld_s, void* qT, int64_t ld_qT, void* sT,
-                             int64_t ld_sT, bool pow2, cudaStream_t stream) {
-  dim3 grid((unsigned)(K / kBwTile), (unsigned)(rows / kBwTile));
+                             int64_t ld_sT, bool pow2, cudaStream_t stream, int num_sms) {
+  const int64_t tiles = (K / kBwTile) * (rows / kBwTile);
+  int64_t ctas = std::min<int64_t>(tiles, (int64_t)num_sms * kWCtasPerSm);
+  if (ctas < 1) ctas = 1;
   auto* wp = static_cast<const uint16_t*>(w);
   auto* qp = static_cast<uint8_t*>(q);
   auto* qTp = static_cast<uint8_t*>(qT);
   if (pow2)
-    bw_weight_kernel<true><<<grid, 256, 0, stream>>>(wp, rows, K, ld_w, qp, ld_q, s, ld_s, qTp, ld_qT, sT, ld_sT);
+    bw_weight_kernel<true><<<(unsigned)ctas, 256, 0, stream>>>(wp, rows, K, ld_w, qp, ld_q, s, ld_s, qTp, ld_qT,
+                                                               sT, ld_sT);
   else
-    bw_weight_kernel<false><<<grid, 256, 0, stream>>>(wp, rows, K, ld_w, qp, ld_q, s, ld_s, qTp, ld_qT, sT, ld_sT);
+    bw_weight_kernel<false><<<(unsigned)ctas, 256, 0, stream>>>(wp, rows, K, ld_w, qp, ld_q, s, ld_s, qTp, ld_qT,
+                                                                sT, ld_sT);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bw_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                               const int32_t* splits, int G, void* qT, int64_t ld_q, void* sT,
                               int64_t ld_s, int64_t capacity, int64_t* pad_offsets,
-                              int32_t* status, bool pow2, cudaStream_t stream) {
-  const int64_t gx = (capacity + kColTokens - 1) / kColTokens;
-  const int64_t gy = (cols + kColCols - 1) / kColCols;
-  dim3 grid((unsigned)(gx > 0 ? gx : 1), (unsigned)gy);
+                              int32_t* status, bool pow2, cudaStream_t stream, int num_sms) {
+  // the persistent column-wise kernel with one 128-token block per tile
+  const int64_t tiles = (capacity + kColTokens - 1) / kColTokens * ((cols + kColCols - 1) / kColCols);
+  int64_t ctas = std::min<int64_t>(tiles, (int64_t)num_sms * kColCtasPerSm);
+  if (ctas < 1) ctas = 1;
   auto* xp = static_cast<const uint16_t*>(x);
   auto* qp = static_cast<uint8_t*>(qT);
   if (pow2)
-    bw_colwise_kernel<true><<<grid, kColThreads, 0, stream>>>(xp, rows, cols, ld_x, splits, G, qp, ld_q, sT, ld_s,
-                                                             capacity, pad_offsets, status);
+    mx_colwise_kernel<MXG_E4M3, false, 2><<<(unsigned)ctas, kColThreads, 0, stream>>>(
+        xp, rows, cols, ld_x, splits, G, 128, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr, 0,
+        nullptr, 0);
   else
-    bw_colwise_kernel<false><<<grid, kColThreads, 0, stream>>>(xp, rows, cols, ld_x, splits, G, qp, ld_q, sT, ld_s,
-                                                              capacity, pad_offsets, status);
+    mx_colwise_kernel<MXG_E4M3, false, 1><<<(unsigned)ctas, kColThreads, 0, stream>>>(
+        xp, rows, cols, ld_x, splits, G, 128, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr, 0,
+        nullptr, 0);
   return cudaGetLastError();
 }
 
