@@ -149,7 +149,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     const int64_t ex = base + incl[q] - (v[0][q] + v[1][q]);
     if (2 * tid <= G) tabs[q][2 * tid] = (int32_t)ex;
     if (2 * tid + 1 <= G) tabs[q][2 * tid + 1] = (int32_t)(ex + v[0][q]);
-    if (tid == kPlanThreads - 1) totals[q] = base + incl[q];
+    if (tid == kPlanThreads - 1) {
+      // the total, entry G: for G = 2 * kPlanThreads no pair above reaches it
+      totals[q] = base + incl[q];
+      tabs[q][G] = (int32_t)(base + incl[q]);
+    }
   }
   __syncthreads();
   if (tid == 0) {

@@ -146,6 +146,10 @@ __device__ bool build_seg_table(SegTable& t, const int32_t* __restrict__ splits,
   const int64_t em = bm + sm - (m0 + m1), ep = bp + sp - (p0 + p1);
   if (2 * tid <= G) { t.off[2 * tid] = em; t.poff[2 * tid] = ep; }
   if (2 * tid + 1 <= G) { t.off[2 * tid + 1] = em + m0; t.poff[2 * tid + 1] = ep + p0; }
+  if (tid == (int)blockDim.x - 1) {  // the totals, entry G: for G = 512 no pair above reaches it
+    t.off[G] = bm + sm;
+    t.poff[G] = bp + sp;
+  }
   __syncthreads();
   int bad = 0;
   if (any_neg) bad = MXG_ERR_SPLITS;

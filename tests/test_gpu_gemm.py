@@ -199,3 +199,38 @@ def test_wgrad_empty_batch(accumulate):
     mxg.grouped_gemm_wgrad(empty(N), empty(K), i32_to_dev([0, 0, 0]), 0, 32, out=init,
                            accumulate=accumulate, check=True)
     assert (init == (3.0 if accumulate else 0.0)).all()
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "a8w4"])
+def test_fwd_maximum_expert_count(kind):
+    """G = 512 (the most the library accepts): almost every expert empty, a
+    few ragged ones scattered through the table (prefix search and tile
+    enumeration over the full expert table)."""
+    splits = np.zeros(512, dtype=np.int32)
+    splits[[0, 7, 255, 256, 400, 511]] = [1, 129, 64, 3, 200, 31]
+    got, ref = _run_fwd(kind, splits, 64, 256, seed=9)
+    oracle.assert_gemm_close(got, ref, f"fwd G=512 {kind}")
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "mxfp8"])
+def test_fwd_wide_dynamic_range(kind):
+    """Rows and weight rows scaled by powers of two from 2^-40 to 2^40, so the
+    block scales span ~160 binades (products stay inside fp32)."""
+    ea, eb = KINDS[kind]
+    rng = np.random.default_rng(12)
+    splits = np.array([70, 0, 130], dtype=np.int32)
+    G, S, N, K = 3, 200, 96, 256
+    xs = synth.bf16_bits_to_f32(synth.normal_bf16(rng, (S, K)))
+    ws = synth.bf16_bits_to_f32(synth.normal_bf16(rng, (G * N, K)))
+    xs *= np.float32(2.0) ** rng.integers(-40, 41, size=(S, 1)).astype(np.float32)
+    ws *= np.float32(2.0) ** rng.integers(-40, 41, size=(G * N, 1)).astype(np.float32)
+    x, w = synth.f32_to_bf16_bits(xs), synth.f32_to_bf16_bits(ws)
+    A, Ad = oracle_operand_rowwise(x, ea)
+    W, Wd = oracle_operand_rowwise(w, eb)
+    Y = _mxg().grouped_gemm_fwd(A, W, i32_to_dev(splits), N, out_dtype=torch.float32, check=True)
+    ref = oracle.grouped_fwd(Ad, Wd, splits, N)
+    # per output row the magnitude is set by its own scales: check row by row
+    got = Y.cpu().numpy()
+    for r in range(S):
+        if np.abs(ref[r]).max() > 0:
+            oracle.assert_gemm_close(got[r:r + 1], ref[r:r + 1], f"wide range {kind} row {r}")

@@ -191,3 +191,25 @@ def test_dual_rejects_bad_splits_and_writes_nothing():
     assert ei.value.code == 4
     assert (q == 0xAB).all() and (s == 0xCD).all() and (qT == 0xAB).all() and (sT == 0xCD).all()
     assert (poff == -7).all()
+
+
+@pytest.mark.parametrize("elem", ["e2m1", "e4m3"])
+def test_colwise_and_dual_with_512_experts(elem):
+    """G = 512, the most the library accepts (the prefix tables' last entry is
+    the one no scan pair reaches): a few ragged experts among empty ones."""
+    splits = np.zeros(512, dtype=np.int32)
+    splits[[0, 3, 200, 511]] = [33, 64, 1, 90]
+    rng = np.random.default_rng(77)
+    x = synth.normal_bf16(rng, (int(splits.sum()), 64), std=2.0, outlier_frac=0.02)
+    mxg = _mxg()
+    op, poff = mxg.mx_quantize_colwise_segment_padded(bf16_to_dev(x), i32_to_dev(splits), 32, elem, check=True)
+    d, s, p = oracle.quantize_mx_colwise_segment_padded(x, splits, 32, elem)
+    spad = int(p[-1])
+    cb = spad // 2 if elem == "e2m1" else spad
+    assert np.array_equal(poff.cpu().numpy(), p)
+    assert np.array_equal(op.data.cpu().numpy()[:, :cb], d)
+    assert np.array_equal(op.scale.cpu().numpy()[:, : spad // 32], s)
+    row, col, poff2 = mxg.mx_quantize_dual_segment_padded(bf16_to_dev(x), i32_to_dev(splits), 32, elem, check=True)
+    rd, rs = oracle.quantize_mx_rowwise(x, elem)
+    assert np.array_equal(row.data.cpu().numpy(), rd) and np.array_equal(row.scale.cpu().numpy(), rs)
+    assert np.array_equal(col.data.cpu().numpy()[:, :cb], d)
