@@ -263,6 +263,7 @@ class A8W4Forward:
 class MXFP4Train:
     """MXFP4 MoE training step of one expert layer: fwd, dgrad, variable-K wgrad."""
     name = "mxfp4_moe_train"
+    elem = "e2m1"
 
     def __init__(self, dev):
         import torch
@@ -299,18 +300,18 @@ class MXFP4Train:
 
     def step(self, time_gemm=False):
         mxg, G, N, K, pad = self.mxg, self.G, self.N, self.K, self.pad
-        Xq = mxg.mx_quantize_rowwise(self.x, "e2m1")
-        Wq = mxg.mx_quantize_rowwise(self.w, "e2m1")
+        Xq = mxg.mx_quantize_rowwise(self.x, self.elem)
+        Wq = mxg.mx_quantize_rowwise(self.w, self.elem)
         self.timed.run("fwd", lambda: mxg.grouped_gemm_fwd(Xq, Wq, self.d_splits, N, out=self.y,
                                                            workspace=self.ws, status=self.status), time_gemm)
-        dYq = mxg.mx_quantize_rowwise(self.dy, "e2m1")
-        Wt, _ = mxg.mx_quantize_colwise_segment_padded(self.w, self.w_splits, 32, "e2m1",
+        dYq = mxg.mx_quantize_rowwise(self.dy, self.elem)
+        Wt, _ = mxg.mx_quantize_colwise_segment_padded(self.w, self.w_splits, 32, self.elem,
                                                        capacity=G * N, status=self.status)
         self.timed.run("dgrad", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx,
                                                                workspace=self.ws, status=self.status), time_gemm)
-        dYt, _ = mxg.mx_quantize_colwise_segment_padded(self.dy, self.d_splits, pad, "e2m1",
+        dYt, _ = mxg.mx_quantize_colwise_segment_padded(self.dy, self.d_splits, pad, self.elem,
                                                         capacity=self.cap, status=self.status)
-        Xt, _ = mxg.mx_quantize_colwise_segment_padded(self.x, self.d_splits, pad, "e2m1",
+        Xt, _ = mxg.mx_quantize_colwise_segment_padded(self.x, self.d_splits, pad, self.elem,
                                                        capacity=self.cap, status=self.status)
         self.timed.run("wgrad", lambda: mxg.grouped_gemm_wgrad(dYt, Xt, self.d_splits, self.S, pad,
                                                                out=self.main_grad, accumulate=True,
@@ -418,6 +419,27 @@ class DenseMXFP4:
 
     def check(self):
         self.mxg.check_status(self.status)
+
+
+class MXFP8Train(MXFP4Train):
+    """The MXFP4 training step's shapes with MXFP8 (E4M3) operands in all
+    three passes (kind::mxf8f6f4)."""
+    name = "mxfp8_moe_train"
+    elem = "e4m3"
+
+    def __init__(self, dev):
+        super().__init__(dev)
+        f = 2.0 * self.S * self.N * self.K
+        self.gemm_info = {p: (f, FP8_OVER_BF16, "mxf8f6f4 (mxfp8)") for p in ("fwd", "dgrad", "wgrad")}
+
+    def config(self):
+        c = super().config()
+        c["workload"] = ("MXFP8 MoE training step: G=32, 16384 tokens top-8 Zipf(1.1) -> S=131072, "
+                         "hidden K=7168, FFN N=2048; fwd TN, dgrad NN, wgrad NT (pad 32, fp32 accumulate "
+                         "into main_grad), E4M3 with UE8M0 per 32, BF16 in/out")
+        return c
+
+    dtype = "mxf8f6f4 (e4m3 x e4m3, fp32 accumulate)"
 
 
 class BlockwiseFP8:
@@ -536,7 +558,8 @@ def torch_bf16():
     return torch.bfloat16
 
 
-WORKLOAD_CLASSES = {c.name: c for c in (A8W4Forward, MXFP4Train, BlockwiseFP8, DenseMXFP4, BlockwiseFP8Pow2)}
+WORKLOAD_CLASSES = {c.name: c for c in (A8W4Forward, MXFP4Train, MXFP8Train, BlockwiseFP8, DenseMXFP4,
+                                        BlockwiseFP8Pow2)}
 
 
 def build_workload(name, dev):
@@ -639,6 +662,7 @@ ORACLE_SAMPLES = {
     # workload: (rows of A and of W sampled, K, A format, W format)
     "a8w4_fwd": (2048, 4096, "e4m3", "e2m1"),
     "mxfp4_moe_train": (1024, 7168, "e2m1", "e2m1"),
+    "mxfp8_moe_train": (1024, 7168, "e4m3", "e4m3"),
     "blockwise_fp8": (1024, 7168, "bw", "bw"),
     "blockwise_fp8_pow2": (1024, 7168, "bw_pow2", "bw_pow2"),
     "dense_mxfp4_m8192": (1024, 8192, "e2m1", "e2m1"),

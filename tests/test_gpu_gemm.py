@@ -134,6 +134,42 @@ def test_wgrad_parity(kind, pad, accumulate):
         assert np.array_equal(got[1], init[1]) and np.array_equal(got[5], init[5])
 
 
+@pytest.mark.parametrize("kind", ["mxfp4", "mxfp8"])
+def test_fp32_forward_many_tiles_per_cta(kind):
+    """FP32 output over more tiles than SMs (49 m-tiles x 4 n-tiles, the last
+    one ragged), so that every CTA reuses its accumulator and scale slots
+    across tiles of different experts."""
+    splits = [1500, 0, 1, 2047, 129, 2300]
+    got, ref = _run_fwd(kind, splits, 896, 320, out_dtype=torch.float32, seed=41)
+    oracle.assert_gemm_close(got, ref, f"fwd fp32 {kind} N=896")
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "mxfp8"])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_wgrad_many_tiles_per_cta(kind, accumulate):
+    """Variable-K wgrad with more tiles than SMs (8 experts x 4 x 5 tiles, the
+    last n-tile ragged): the accumulator and every scale slot are reused
+    across experts of different contraction lengths."""
+    e = KINDS[kind][0]
+    splits = np.array([300, 0, 77, 513, 200, 31, 1, 640], dtype=np.int32)
+    G, S = len(splits), int(splits.sum())
+    N, K, pad = 512, 1120, 32
+    rng = np.random.default_rng(90 + accumulate)
+    dy = synth.normal_bf16(rng, (S, N), outlier_frac=0.01)
+    x = synth.normal_bf16(rng, (S, K), outlier_frac=0.01)
+    cap = synth.padded_rows_capacity(S, G, pad)
+    dYt, dYtd, poff = oracle_operand_colwise(dy, splits, pad, e, capacity=cap)
+    Xt, Xtd, _ = oracle_operand_colwise(x, splits, pad, e, capacity=cap)
+    init = rng.standard_normal((G, N, K)).astype(np.float32) * np.float32(1e-3)
+    out = torch.from_numpy(init.copy()).to("cuda:0")
+    _mxg().grouped_gemm_wgrad(dYt, Xt, i32_to_dev(splits), S, pad, out=out, accumulate=accumulate, check=True)
+    ref = oracle.grouped_wgrad(dYtd, Xtd, poff, out_init=init if accumulate else None)
+    got = out.cpu().numpy()
+    oracle.assert_gemm_close(got, ref, f"wgrad {kind} many tiles acc={accumulate}")
+    if accumulate:
+        assert np.array_equal(got[1], init[1])
+
+
 def test_wgrad_bf16_output():
     splits = np.array([70, 33], dtype=np.int32)
     S, N, K = 103, 256, 256
