@@ -20,6 +20,9 @@ no blocking or fusion.  Each function cites the passage it follows:
   operand.
 * "Integrate MXFP4 hipblaslt GEMM support" (PR #697): the per-pass shapes
   (forward contracts hidden, dgrad contracts out, wgrad contracts tokens).
+* "Integrate MXFP4 hipblaslt GEMM support" (PR #697), Takeaways, and the
+  "fused scale packing kernel" commit of PR #723: MX scales written in the
+  matrix engine's blocked order (``oracle.packed``).
 * The OCP Microscaling Formats (MX) v1.0 specification for the E2M1 / E4M3
   element encodings and the shared-exponent rule.
 
@@ -50,6 +53,12 @@ from .blockwise import (  # noqa: F401
     dequantize_bw_128x128,
     transpose_bw_128x128,
     pow2_scale,
+)
+from .packed import (  # noqa: F401
+    tile_prefix,
+    packed_scale_bytes,
+    pack_scales_mma,
+    pack_scales_mma_by_tiles,
 )
 from .gemm import (  # noqa: F401
     check_splits,
