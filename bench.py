@@ -5,7 +5,8 @@ tokens routed top-2 with Dirichlet(0.5)-skewed expert probabilities (S = 8192
 rows), hidden K = 4096, expert FFN N = 14336; activations MXFP8 E4M3, weights
 MXFP4 E2M1.  One step = every row of the hot path over one batch:
     quantize X (BF16 -> MXFP8, row-wise), quantize W (BF16 -> MXFP4, row-wise),
-    grouped_gemm_fwd (split validation, scale packing, tcgen05 GEMM, BF16 out).
+    with the scales written straight into the tensor cores' staging order, then
+    grouped_gemm_fwd (split validation, tcgen05 GEMM, BF16 out).
 Metric: TFLOPS = 2 * sum(m_g) * N * K / step time.
 
 `--workload mxfp4_moe_train` times the MXFP4 MoE training step (G = 32,
@@ -194,6 +195,7 @@ class _Timed:
 class A8W4Forward:
     """a8w4 grouped forward (the default)."""
     name = "a8w4_fwd"
+    call_kernels = "plan + tcgen05 GEMM; scales arrive packed"
 
     def __init__(self, dev):
         import torch
@@ -212,23 +214,19 @@ class A8W4Forward:
         self.splits_host = torch.from_numpy(self.splits).pin_memory()
         self.d_splits = self.splits_host.to(dev)
         S, N, K, G = self.S, self.N, self.K, self.G
-        self.qx = torch.empty((S, K), dtype=torch.uint8, device=dev)
-        self.sx = torch.empty((S, K // 32), dtype=torch.uint8, device=dev)
-        self.qw = torch.empty((G * N, K // 2), dtype=torch.uint8, device=dev)
-        self.sw = torch.empty((G * N, K // 32), dtype=torch.uint8, device=dev)
         self.y = torch.empty((S, N), dtype=torch.bfloat16, device=dev)
         self.y_host = torch.empty((S, N), dtype=torch.bfloat16).pin_memory()
         self.ws = torch.empty(mxg.gemm_workspace_size("fwd", G, S, N, K), dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.flops = 2.0 * S * N * K
-        self.launches_per_step = 2 + 3   # two quantizers; plan + scale pack + GEMM
+        self.launches_per_step = 2 + 2   # two quantizers (scales written packed); plan + GEMM
         self.timed = _Timed()
         self.gemm_info = {"fwd": (self.flops, FP8_OVER_BF16, "mxf8f6f4 (a8w4)")}
 
     def step(self, time_gemm=False):
         mxg = self.mxg
-        A = mxg.mx_quantize_rowwise(self.x, "e4m3", q=self.qx, s=self.sx)
-        W = mxg.mx_quantize_rowwise(self.wt, "e2m1", q=self.qw, s=self.sw)
+        A = mxg.mx_quantize_rowwise_packed(self.x, "e4m3", m_splits=self.d_splits, status=self.status)
+        W = mxg.mx_quantize_rowwise_packed(self.wt, "e2m1", groups=self.G)
         self.timed.run("fwd", lambda: mxg.grouped_gemm_fwd(A, W, self.d_splits, self.N, out=self.y,
                                                            workspace=self.ws, status=self.status),
                        time_gemm)
@@ -247,14 +245,14 @@ class A8W4Forward:
         return {"workload": "a8w4 grouped forward: G=8, 4096 tokens top-2 Dirichlet(0.5) -> S=8192, "
                             "K=4096, N=14336; X MXFP8 E4M3, W MXFP4 E2M1 (UE8M0 / 32), BF16 out",
                 "G": self.G, "S": self.S, "N": self.N, "K": self.K, "m_splits": self.splits.tolist(),
-                "step": "quantize X + quantize W + grouped_gemm_fwd",
+                "step": "quantize X + quantize W (scales in the MMA staging order) + grouped_gemm_fwd",
                 "l2": "inputs larger than L2 (X 67 MB + W 940 MB BF16), no flush"}
 
     dtype = "mxf8f6f4 (e4m3 x e2m1, fp32 accumulate)"
-    # DRAM bytes (read + write) of one forward call -- plan, scale pack and GEMM
-    # kernels -- counted by ncu on GB300 (dram__bytes_read.sum +
-    # dram__bytes_write.sum); algorithmic bytes of the call: 519,045,120.
-    traffic_bytes = 506477312
+    # DRAM bytes (read + write) of one forward call -- plan and GEMM kernels --
+    # counted by ncu on GB300 (dram__bytes_read.sum + dram__bytes_write.sum).
+    # Algorithmic bytes of the call: 519,045,120.
+    traffic_bytes = 490997248
 
     def check(self):
         self.mxg.check_status(self.status)
@@ -294,17 +292,18 @@ class MXFP4Train:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         f = 2.0 * S * N * K
         self.flops = 3 * f
-        self.launches_per_step = 6 + 3 * 3   # six quantizers; three GEMM calls of three kernels
+        # six quantizers; fwd: plan + GEMM (both operands packed); dgrad, wgrad: plan + pack + GEMM
+        self.launches_per_step = 6 + 2 + 3 + 3
         self.timed = _Timed()
         self.gemm_info = {p: (f, FP4_OVER_BF16, "mxf4") for p in ("fwd", "dgrad", "wgrad")}
 
     def step(self, time_gemm=False):
         mxg, G, N, K, pad = self.mxg, self.G, self.N, self.K, self.pad
-        Xq = mxg.mx_quantize_rowwise(self.x, self.elem)
-        Wq = mxg.mx_quantize_rowwise(self.w, self.elem)
+        Xq = mxg.mx_quantize_rowwise_packed(self.x, self.elem, m_splits=self.d_splits, status=self.status)
+        Wq = mxg.mx_quantize_rowwise_packed(self.w, self.elem, groups=G)
         self.timed.run("fwd", lambda: mxg.grouped_gemm_fwd(Xq, Wq, self.d_splits, N, out=self.y,
                                                            workspace=self.ws, status=self.status), time_gemm)
-        dYq = mxg.mx_quantize_rowwise(self.dy, self.elem)
+        dYq = mxg.mx_quantize_rowwise_packed(self.dy, self.elem, m_splits=self.d_splits, status=self.status)
         Wt, _ = mxg.mx_quantize_colwise_segment_padded(self.w, self.w_splits, 32, self.elem,
                                                        capacity=G * N, status=self.status)
         self.timed.run("dgrad", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx,
@@ -375,17 +374,18 @@ class DenseMXFP4:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         f = 2.0 * S * N * K
         self.flops = 3 * f
-        self.launches_per_step = 6 + 3 * 3   # six quantizers; three GEMM calls of three kernels
+        # six quantizers; fwd: plan + GEMM (both operands packed); dgrad, wgrad: plan + pack + GEMM
+        self.launches_per_step = 6 + 2 + 3 + 3
         self.timed = _Timed()
         self.gemm_info = {p: (f, FP4_OVER_BF16, "mxf4") for p in ("fwd", "dgrad", "wgrad")}
 
     def step(self, time_gemm=False):
         mxg, N, pad = self.mxg, self.N, self.pad
-        Xq = mxg.mx_quantize_rowwise(self.x, "e2m1")
-        Wq = mxg.mx_quantize_rowwise(self.w, "e2m1")
+        Xq = mxg.mx_quantize_rowwise_packed(self.x, "e2m1", m_splits=self.d_splits, status=self.status)
+        Wq = mxg.mx_quantize_rowwise_packed(self.w, "e2m1", groups=1)
         self.timed.run("fwd", lambda: mxg.grouped_gemm_fwd(Xq, Wq, self.d_splits, N, out=self.y,
                                                            workspace=self.ws, status=self.status), time_gemm)
-        dYq = mxg.mx_quantize_rowwise(self.dy, "e2m1")
+        dYq = mxg.mx_quantize_rowwise_packed(self.dy, "e2m1", m_splits=self.d_splits, status=self.status)
         Wt, _ = mxg.mx_quantize_colwise_segment_padded(self.w, self.w_splits, 32, "e2m1",
                                                        capacity=N, status=self.status)
         self.timed.run("dgrad", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx,

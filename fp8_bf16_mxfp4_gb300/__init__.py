@@ -22,6 +22,7 @@ from . import _lib
 
 __all__ = [
     "MXOperand", "MXGError", "mx_quantize_rowwise", "mx_quantize_colwise_segment_padded",
+    "mx_quantize_rowwise_packed", "mx_packed_scale_bytes",
     "mx_quantize_dual_segment_padded",
     "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "gemm_workspace_size",
     "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns",
@@ -32,6 +33,7 @@ __all__ = [
 ]
 
 ELEM = {"e2m1": 1, "e4m3": 2}
+SCALE_LAYOUT = {"plain": 0, "packed": 1}
 PASS = {"fwd": 0, "dgrad": 1, "wgrad": 2}
 _OUT = {torch.bfloat16: 1, torch.float32: 2}
 
@@ -67,20 +69,25 @@ def _need_cuda(*ts):
 @dataclass
 class MXOperand:
     """A quantized K-major operand: codes, UE8M0 scales, element format and
-    logical column count (the contraction length)."""
+    logical column count (the contraction length).  ``scale_layout`` "plain"
+    means scales [rows, cols/32]; "packed" means the tensor-core staging order
+    of ``mx_quantize_rowwise_packed`` (a flat uint8 tensor)."""
     data: torch.Tensor
     scale: torch.Tensor
     elem: str
     cols: int
+    scale_layout: str = "plain"
 
     @property
     def rows(self) -> int:
         return self.data.shape[0]
 
     def c(self) -> _lib.MxOperandC:
+        packed = self.scale_layout == "packed"
         return _lib.MxOperandC(self.data.data_ptr(), self.scale.data_ptr(), self.rows, self.cols,
                                _ld(self.data, _codes_cols(self.elem, self.cols)),
-                               _ld(self.scale, self.cols // 32), ELEM[self.elem], 0)
+                               0 if packed else _ld(self.scale, self.cols // 32), ELEM[self.elem],
+                               SCALE_LAYOUT[self.scale_layout])
 
 
 def _ld(t: torch.Tensor, row_elems: int) -> int:
@@ -140,6 +147,45 @@ def mx_quantize_rowwise(x: torch.Tensor, elem: str, q: torch.Tensor | None = Non
                                 _ld(q, _codes_cols(elem, cols)), _ptr(s), _ld(s, cols // 32),
                                 _stream(x.device)), "mx_quantize_rowwise")
     return MXOperand(q, s, elem, cols)
+
+
+def mx_packed_scale_bytes(rows: int, cols: int, G: int) -> int:
+    """Bytes of packed scales for `rows` x `cols` cut into G segments (an upper
+    bound over every split)."""
+    return int(_lib.load().mx_packed_scale_bytes(rows, cols, G))
+
+
+def mx_quantize_rowwise_packed(x: torch.Tensor, elem: str, m_splits: torch.Tensor | None = None,
+                               groups: int | None = None, status: torch.Tensor | None = None,
+                               check: bool = False) -> MXOperand:
+    """BF16 [rows, cols] -> MX operand whose scales are already in the grouped
+    GEMM's tensor-core staging order (no repacking pass in the GEMM).  Rows
+    are cut into segments by the device ``m_splits`` (activations and
+    gradients), or into ``groups`` equal segments (forward weights: G experts
+    of N rows).  The GEMM call must use the same segments."""
+    _need_cuda(x, m_splits)
+    if x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError("x must be a 2-D bfloat16 tensor")
+    if (m_splits is None) == (groups is None):
+        raise ValueError("give exactly one of m_splits and groups")
+    rows, cols = x.shape
+    G = m_splits.numel() if m_splits is not None else int(groups)
+    if m_splits is not None and m_splits.dtype != torch.int32:
+        raise ValueError("m_splits must be int32")
+    nbytes = mx_packed_scale_bytes(rows, cols, G)
+    if nbytes < 0:
+        raise ValueError("invalid shape for packed scales")
+    q = torch.empty((rows, _codes_cols(elem, cols)), dtype=torch.uint8, device=x.device)
+    s = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=x.device)
+    st = status if status is not None else status_tensor(x.device)
+    lib = _lib.load()
+    _ok(lib.mx_quantize_rowwise_packed(_ptr(x), rows, cols, _ld(x, cols), ELEM[elem], _ptr(q),
+                                       _ld(q, _codes_cols(elem, cols)), _ptr(s), s.numel(),
+                                       _ptr(m_splits), G, _ptr(st),
+                                       _stream(x.device)), "mx_quantize_rowwise_packed")
+    if check:
+        check_status(st)
+    return MXOperand(q, s, elem, cols, "packed")
 
 
 def mx_quantize_colwise_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, pad_multiple: int,

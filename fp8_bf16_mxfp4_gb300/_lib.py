@@ -30,7 +30,7 @@ class MxOperandC(ctypes.Structure):
         ("ld", c_i64),
         ("scale_ld", c_i64),
         ("elem", c_i32),
-        ("reserved", c_i32),
+        ("scale_layout", c_i32),
     ]
 
 
@@ -58,6 +58,9 @@ SIGNATURES = {
         c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp, c_i64,
                 c_vp, c_i64, c_vp, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "mx_padded_rows_capacity": (c_i64, [c_i64, c_i32, c_i32]),
+    "mx_packed_scale_bytes": (c_i64, [c_i64, c_i64, c_i32]),
+    "mx_quantize_rowwise_packed": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp,
+                                           c_i32, c_vp, c_vp]),
     "grouped_gemm_fwd": (
         c_i32, [ctypes.POINTER(MxOperandC), ctypes.POINTER(MxOperandC), c_vp, c_i32, c_i64, c_vp,
                 c_i64, c_i32, c_vp, c_size, c_vp, c_vp]),

@@ -90,16 +90,19 @@ inline bool valid_elem(int32_t e) { return e == MXG_E2M1 || e == MXG_E4M3; }
 
 // Host checks of one MX GEMM operand.  An operand with no elements (rows == 0,
 // or cols == 0 where `allow_no_cols`) may have NULL data and scale pointers.
-mxg_status check_operand(const mxg_mx_operand* op, bool allow_no_cols = false) {
+// Packed scales are accepted only where `allow_packed`.
+mxg_status check_operand(const mxg_mx_operand* op, bool allow_no_cols = false, bool allow_packed = false) {
   if (op == nullptr) return MXG_ERR_NULL;
-  if (!valid_elem(op->elem) || op->reserved != 0) return MXG_ERR_UNSUPPORTED;
+  if (!valid_elem(op->elem)) return MXG_ERR_UNSUPPORTED;
+  const bool packed = op->scale_layout == MXG_SCALE_PACKED;
+  if (!(op->scale_layout == MXG_SCALE_PLAIN || (packed && allow_packed))) return MXG_ERR_UNSUPPORTED;
   if (op->rows < 0 || op->cols < 0 || op->cols % 32 != 0) return MXG_ERR_SHAPE;
   if (op->cols == 0 && !allow_no_cols) return MXG_ERR_SHAPE;
-  if (op->ld < code_bytes(op->elem, op->cols) || op->scale_ld < op->cols / 32) return MXG_ERR_SHAPE;
+  if (op->ld < code_bytes(op->elem, op->cols) || (!packed && op->scale_ld < op->cols / 32)) return MXG_ERR_SHAPE;
   if (op->ld % 16 != 0) return MXG_ERR_ALIGN;
   if (op->rows == 0 || op->cols == 0) return MXG_OK;
   if (op->data == nullptr || op->scale == nullptr) return MXG_ERR_NULL;
-  if (!aligned16(op->data)) return MXG_ERR_ALIGN;
+  if (!aligned16(op->data) || (packed && !aligned16(op->scale))) return MXG_ERR_ALIGN;
   return MXG_OK;
 }
 
@@ -218,6 +221,42 @@ mxg_status mx_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_
                                        static_cast<cudaStream_t>(stream), sms));
 }
 
+int64_t mx_packed_scale_bytes(int64_t rows, int64_t cols, int32_t G) {
+  if (rows < 0 || cols < 0 || cols % 32 != 0 || G < 1 || G > kMaxExperts) return -1;
+  const int64_t nonempty = rows < G ? rows : (int64_t)G;
+  const int64_t rt_max = (rows + nonempty * 127) / 128;
+  return (cols + 127) / 128 * rt_max * 512;
+}
+
+mxg_status mx_quantize_rowwise_packed(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                      int32_t elem, void* q, int64_t ld_q, uint8_t* s_packed,
+                                      int64_t s_bytes, const int32_t* d_m_splits, int32_t G,
+                                      int32_t* d_status, void* stream) {
+  if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0) return MXG_ERR_SHAPE;
+  if (d_m_splits == nullptr && rows % G != 0) return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < code_bytes(elem, cols)) return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 16 != 0) return MXG_ERR_ALIGN;
+  if (d_m_splits != nullptr && d_status == nullptr) return MXG_ERR_NULL;
+  const int64_t need = mx_packed_scale_bytes(rows, cols, G);
+  if (s_bytes < need) return MXG_ERR_SHAPE;
+  // the split check still runs when there are no rows (a non-zero split is an error)
+  if (rows == 0 && d_m_splits == nullptr) return MXG_OK;
+  if ((rows > 0 && (x == nullptr || q == nullptr)) || (need > 0 && s_packed == nullptr)) return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s_packed)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, q, s_packed, d_m_splits, d_status}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  const int64_t nonempty = rows < G ? rows : (int64_t)G;
+  const int64_t rt_bound = d_m_splits ? (rows + nonempty * 127) / 128 : (int64_t)G * ((rows / G + 127) / 128);
+  return cuda_status(launch_mx_rowwise_packed(x, rows, cols, ld_x, elem, q, ld_q, s_packed, d_m_splits, G,
+                                              d_m_splits ? 0 : rows / G, rt_bound, d_status,
+                                              static_cast<cudaStream_t>(stream), sms));
+}
+
 mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64_t cols,
                                               int64_t ld_x, const int32_t* d_m_splits,
                                               int32_t G, int32_t pad_multiple, int32_t elem,
@@ -295,7 +334,8 @@ mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
                             int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
                             int32_t* d_status, void* stream) {
   mxg_status st;
-  if ((st = check_operand(A)) != MXG_OK || (st = check_operand(W)) != MXG_OK) return st;
+  if ((st = check_operand(A, false, true)) != MXG_OK || (st = check_operand(W, false, true)) != MXG_OK)
+    return st;
   if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
   if ((st = check_out(out, A->rows, ld_out, N, out_dtype)) != MXG_OK) return st;
   if (G < 1 || G > kMaxExperts || N <= 0 || N % 32 != 0) return MXG_ERR_SHAPE;
@@ -325,6 +365,8 @@ mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
   a.b_data = static_cast<const uint8_t*>(W->data); a.b_ld = W->ld;
   a.b_scale = W->scale; a.b_scale_ld = W->scale_ld;
   a.b_rows = W->rows; a.b_cols = W->cols; a.b_elem = W->elem;
+  a.a_packed = A->scale_layout == MXG_SCALE_PACKED;
+  a.b_packed = W->scale_layout == MXG_SCALE_PACKED;
   a.splits = d_m_splits;
   a.total_rows = A->rows;
   a.N = N; a.K = A->cols;
@@ -339,7 +381,7 @@ mxg_status grouped_gemm_dgrad(const mxg_mx_operand* dY, const mxg_mx_operand* Wt
                               int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* d_status,
                               void* stream) {
   mxg_status st;
-  if ((st = check_operand(dY)) != MXG_OK || (st = check_operand(Wt)) != MXG_OK) return st;
+  if ((st = check_operand(dY, false, true)) != MXG_OK || (st = check_operand(Wt)) != MXG_OK) return st;
   if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
   if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
   const int64_t N = dY->cols, K = Wt->rows;
@@ -364,6 +406,7 @@ mxg_status grouped_gemm_dgrad(const mxg_mx_operand* dY, const mxg_mx_operand* Wt
   a.b_data = static_cast<const uint8_t*>(Wt->data); a.b_ld = Wt->ld;
   a.b_scale = Wt->scale; a.b_scale_ld = Wt->scale_ld;
   a.b_rows = Wt->rows; a.b_cols = Wt->cols; a.b_elem = Wt->elem;
+  a.a_packed = dY->scale_layout == MXG_SCALE_PACKED;
   a.splits = d_m_splits;
   a.total_rows = dY->rows;
   a.N = N; a.K = K;

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, 
   if (pv.hdr[0] == 0) return;
   const bool isA = blockIdx.z == 0;
   const PackSrc ps = isA ? sa : sb;
+  if (ps.dst == nullptr) return;  // this operand's scales arrive packed
   const int G = p.G;
   const int nrt = (int)((p.N + 127) / 128);
   int RT, KC;
@@ -586,6 +587,9 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
   uint8_t* packA = ws + plan_bytes(a.G);
   uint8_t* packB = packA + align256((size_t)(ps.rtA * ps.kcA) * kChunkBytes);
+  // operands quantized with packed scales are read in place
+  if (a.a_packed) packA = const_cast<uint8_t*>(a.a_scale);
+  if (a.b_packed) packB = const_cast<uint8_t*>(a.b_scale);
 
   Params p{};
   p.pass = a.pass;
@@ -630,14 +634,17 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   // An empty forward / dgrad batch needs only the split validation.
   if (a.pass != MXG_PASS_WGRAD && a.total_rows == 0) return MXG_OK;
 
-  // 2. scale packing (both operands in one launch)
-  PackSrc sa{a.a_scale, a.a_scale_ld, packA};
-  PackSrc sb{a.b_scale, a.b_scale_ld, packB};
-  const int64_t gx = std::max<int64_t>(1, std::max(ps.rtA, ps.rtB));
-  const int64_t gy = std::max<int64_t>(1, cdiv(std::max(ps.kcA, ps.kcB), kPackKc));
-  if (gy > 65535) return MXG_ERR_SHAPE;
-  pack_scales_kernel<<<dim3((unsigned)gx, (unsigned)gy, 2), 128, 0, stream>>>(p, sa, sb);
-  if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
+  // 2. scale packing (both operands in one launch; none for packed operands)
+  if (!(a.a_packed && a.b_packed)) {
+    PackSrc sa{a.a_scale, a.a_scale_ld, a.a_packed ? nullptr : packA};
+    PackSrc sb{a.b_scale, a.b_scale_ld, a.b_packed ? nullptr : packB};
+    const int64_t gx = std::max<int64_t>(1, std::max(a.a_packed ? 0 : ps.rtA, a.b_packed ? 0 : ps.rtB));
+    const int64_t gy = std::max<int64_t>(
+        1, cdiv(std::max(a.a_packed ? 0 : ps.kcA, a.b_packed ? 0 : ps.kcB), kPackKc));
+    if (gy > 65535) return MXG_ERR_SHAPE;
+    pack_scales_kernel<<<dim3((unsigned)gx, (unsigned)gy, 2), 128, 0, stream>>>(p, sa, sb);
+    if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
+  }
 
   // 3. tensor maps + GEMM
   CUtensorMap tmA, tmB;

@@ -15,6 +15,11 @@ cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t
                               void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
                               cudaStream_t stream, int num_sms);
 
+cudaError_t launch_mx_rowwise_packed(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int elem,
+                                     void* q, int64_t ld_q, uint8_t* sp, const int32_t* splits, int G,
+                                     int64_t seg_rows, int64_t rt_bound, int32_t* status,
+                                     cudaStream_t stream, int num_sms);
+
 cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                               const int32_t* splits, int G, int pad, int elem, void* qT,
                               int64_t ld_q, uint8_t* sT, int64_t ld_s, int64_t capacity,
@@ -50,6 +55,7 @@ struct GemmArgs {
   int64_t b_scale_ld;
   int64_t b_rows, b_cols;
   int b_elem;
+  bool a_packed, b_packed;  // scales already in the GEMM's staging order
   const int32_t* splits;
   int64_t total_rows;  // S
   int64_t N, K;        // fwd: out [S,N] over K; dgrad: out [S,K] over N; wgrad: out [G,N,K]

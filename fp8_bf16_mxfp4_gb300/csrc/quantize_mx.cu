@@ -103,6 +103,146 @@ __global__ void __launch_bounds__(kRowThreads) mx_rowwise_kernel(
   }
 }
 
+// Row-wise with the scales written straight into the tensor-core staging
+// order ("pre-swizzled" scales: "Integrate MXFP4 hipblaslt GEMM support",
+// Takeaways; the "fused scale packing kernel" of the Triton grouped GEMM).
+// The rows are cut into segments (the routing splits, or G equal segments of
+// seg_rows rows), each segment into tiles of 128 rows, tiles numbered across
+// segments (RT in all); the scales of 128 rows x 4 blocks form a 512-byte
+// chunk, chunk (kc, rt) at ((kc * RT + rt) * 512), local row i and block j at
+// byte (i % 32) * 16 + (i / 32) * 4 + j; bytes without a row or block are 0.
+//
+// The loop runs over padded positions (tile row, block rounded up to 4), one
+// block per lane as in the plain kernel; the four lanes that share a chunk
+// word gather its bytes with shuffles and one of them stores the word.  A
+// warp's lanes take consecutive positions, so every group of four is aligned
+// to a word and the warp iterates as a whole (the shuffles need all lanes).
+template <int kElem, bool kSplits>
+__global__ void __launch_bounds__(kRowThreads) mx_rowwise_packed_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
+    uint8_t* __restrict__ q, int64_t ld_q, uint8_t* __restrict__ sp,
+    const int32_t* __restrict__ splits, int G, int64_t seg_rows, int32_t* status) {
+  __shared__ int64_t s_off[kMaxExperts + 1];  // row offsets of the segments
+  __shared__ int32_t s_rtp[kMaxExperts + 1];  // first tile of each segment; [G] = RT
+  __shared__ int64_t warp_m[kRowThreads / 32];
+  __shared__ int32_t warp_t[kRowThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int64_t RT;
+  int tps = 1;  // tiles per segment (equal segments)
+  if constexpr (kSplits) {
+    // block-wide scan of (rows, tiles) over the G <= 512 splits, two per thread
+    static_assert(2 * kRowThreads >= kMaxExperts, "two splits per thread");
+    int64_t m0 = 0, m1 = 0;
+    if (2 * tid < G) m0 = splits[2 * tid];
+    if (2 * tid + 1 < G) m1 = splits[2 * tid + 1];
+    const bool neg = m0 < 0 || m1 < 0;
+    const int32_t t0 = m0 > 0 ? (int32_t)((m0 + 127) >> 7) : 0;
+    const int32_t t1 = m1 > 0 ? (int32_t)((m1 + 127) >> 7) : 0;
+    int64_t sm = m0 + m1;
+    int32_t st = t0 + t1;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int64_t om = __shfl_up_sync(0xffffffffu, sm, d);
+      const int32_t ot = __shfl_up_sync(0xffffffffu, st, d);
+      if (lane >= d) { sm += om; st += ot; }
+    }
+    if (lane == 31) { warp_m[wid] = sm; warp_t[wid] = st; }
+    const int any_neg = __syncthreads_or(neg);
+    int64_t bm = 0;
+    int32_t bt = 0;
+    for (int w = 0; w < wid; ++w) { bm += warp_m[w]; bt += warp_t[w]; }
+    const int64_t em = bm + sm - (m0 + m1);
+    const int32_t et = bt + st - (t0 + t1);
+    if (2 * tid <= G) { s_off[2 * tid] = em; s_rtp[2 * tid] = et; }
+    if (2 * tid + 1 <= G) { s_off[2 * tid + 1] = em + m0; s_rtp[2 * tid + 1] = et + t0; }
+    if (tid == kRowThreads - 1) { s_off[G] = bm + sm; s_rtp[G] = bt + st; }  // totals (G = 512 too)
+    __syncthreads();
+    if (any_neg || s_off[G] != rows) {  // nothing is written
+      if (blockIdx.x == 0 && tid == 0) report(status, MXG_ERR_SPLITS);
+      return;
+    }
+    RT = s_rtp[G];
+  } else {
+    tps = (int)((seg_rows + 127) >> 7);
+    RT = (int64_t)G * tps;
+  }
+  const int64_t KB = cols >> 5;
+  const int64_t KBp = (KB + 3) & ~int64_t(3);
+  const int64_t total = RT * 128 * KBp;
+  const int64_t step = (int64_t)gridDim.x * kRowThreads;
+  for (int64_t base = (int64_t)blockIdx.x * kRowThreads + wid * 32; base < total; base += step) {
+    const int64_t t = base + lane;
+    uint32_t sbyte = 0;
+    int64_t prow = 0, b = 0;
+    if (t < total) {
+      prow = t / KBp;
+      b = t - prow * KBp;
+      const int rt = (int)(prow >> 7);
+      int g;
+      int64_t m, row0;
+      if constexpr (kSplits) {
+        int lo = 0, hi = G - 1;  // last g with s_rtp[g] <= rt: non-empty, since s_rtp[g + 1] > rt
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_rtp[mid] <= rt) lo = mid; else hi = mid - 1;
+        }
+        g = lo;
+        m = s_off[g + 1] - s_off[g];
+        row0 = s_off[g];
+      } else {
+        g = rt / tps;
+        m = seg_rows;
+        row0 = (int64_t)g * seg_rows;
+      }
+      const int64_t i = (int64_t)(rt - (kSplits ? s_rtp[g] : g * tps)) * 128 + (prow & 127);
+      if (i < m && b < KB) {
+        const int64_t r = row0 + i;
+        const uint4* src = reinterpret_cast<const uint4*>(x + r * ld_x + b * 32);
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = __ldcs(src + k);
+          w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+        }
+        uint32_t am = 0;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) am = max(am, bf16x2_absmax_bits(w[k]));
+        const int e = mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax);
+        const float sinv = pow2_neg(e);
+        if constexpr (kElem == MXG_E2M1) {
+          uint4 o;
+          quantize8<kElem>(&w[0], sinv, &o.x);
+          quantize8<kElem>(&w[4], sinv, &o.y);
+          quantize8<kElem>(&w[8], sinv, &o.z);
+          quantize8<kElem>(&w[12], sinv, &o.w);
+          __stcs(reinterpret_cast<uint4*>(q + r * ld_q + b * 16), o);
+        } else {
+          uint4 o0, o1;
+          quantize8<kElem>(&w[0], sinv, &o0.x);
+          quantize8<kElem>(&w[4], sinv, &o0.z);
+          quantize8<kElem>(&w[8], sinv, &o1.x);
+          quantize8<kElem>(&w[12], sinv, &o1.z);
+          uint4* dst = reinterpret_cast<uint4*>(q + r * ld_q + b * 32);
+          __stcs(dst, o0);
+          __stcs(dst + 1, o1);
+        }
+        sbyte = (uint32_t)(e + 127);
+      }
+    }
+    // the word of blocks 4c .. 4c+3: lanes (lane & ~3) + j, j = 0..3
+    const int l0 = lane & ~3;
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) word |= __shfl_sync(0xffffffffu, sbyte, l0 + j) << (8 * j);
+    if (t < total && (lane & 3) == 0) {
+      const int64_t rt = prow >> 7;
+      const int il = (int)(prow & 127);
+      const int64_t kc = b >> 2;
+      *reinterpret_cast<uint32_t*>(sp + (kc * RT + rt) * 512 + (il & 31) * 16 + (il >> 5) * 4) = word;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Column-wise, segment-padded.
 // ---------------------------------------------------------------------------
@@ -601,6 +741,39 @@ cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t
   else
     mx_rowwise_kernel<MXG_E4M3><<<(unsigned)blocks, threads, 0, stream>>>(xp, rows, cols, ld_x, qp,
                                                                           ld_q, s, ld_s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_rowwise_packed(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int elem,
+                                     void* q, int64_t ld_q, uint8_t* sp, const int32_t* splits, int G,
+                                     int64_t seg_rows, int64_t rt_bound, int32_t* status,
+                                     cudaStream_t stream, int num_sms) {
+  const int64_t kbp = ((cols / 32) + 3) / 4 * 4;
+  const int64_t total = rt_bound * 128 * kbp;
+  int64_t blocks = (total + kRowThreads - 1) / kRowThreads;
+  // With splits every CTA scans them first: one resident wave, each CTA then
+  // loops, so the scan is paid once per CTA rather than once per 256 blocks.
+  const int64_t cap = (int64_t)num_sms * 8 * (splits ? 1 : 4);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  auto* xp = static_cast<const uint16_t*>(x);
+  auto* qp = static_cast<uint8_t*>(q);
+  const dim3 grid((unsigned)blocks);
+  if (elem == MXG_E2M1) {
+    if (splits)
+      mx_rowwise_packed_kernel<MXG_E2M1, true><<<grid, kRowThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, qp, ld_q, sp, splits, G, seg_rows, status);
+    else
+      mx_rowwise_packed_kernel<MXG_E2M1, false><<<grid, kRowThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, qp, ld_q, sp, nullptr, G, seg_rows, status);
+  } else {
+    if (splits)
+      mx_rowwise_packed_kernel<MXG_E4M3, true><<<grid, kRowThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, qp, ld_q, sp, splits, G, seg_rows, status);
+    else
+      mx_rowwise_packed_kernel<MXG_E4M3, false><<<grid, kRowThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, qp, ld_q, sp, nullptr, G, seg_rows, status);
+  }
   return cudaGetLastError();
 }
 

@@ -72,12 +72,23 @@ typedef enum mxg_status {
 typedef enum mxg_elem { MXG_E2M1 = 1, MXG_E4M3 = 2 } mxg_elem;
 typedef enum mxg_out_dtype { MXG_OUT_BF16 = 1, MXG_OUT_F32 = 2 } mxg_out_dtype;
 typedef enum mxg_pass { MXG_PASS_FWD = 0, MXG_PASS_DGRAD = 1, MXG_PASS_WGRAD = 2 } mxg_pass;
+/* Where an MX operand's scales are: row-major [rows, cols/32] bytes, or the
+ * packed tensor-core staging order written by mx_quantize_rowwise_packed. */
+typedef enum mxg_scale_layout { MXG_SCALE_PLAIN = 0, MXG_SCALE_PACKED = 1 } mxg_scale_layout;
 
 /* One MX operand of a grouped GEMM, K-major: `rows` rows of `cols` elements,
  * quantized along `cols` (the contraction dimension).
- *   data   : codes, row r at (uint8*)data + r*ld  (ld >= cols or cols/2 bytes)
- *   scale  : UE8M0 bytes, row r at scale + r*scale_ld, entries [0, cols/32)
- *   elem   : MXG_E2M1 or MXG_E4M3
+ *   data         : codes, row r at (uint8*)data + r*ld  (ld >= cols or cols/2 bytes)
+ *   scale        : MXG_SCALE_PLAIN: UE8M0 bytes, row r at scale + r*scale_ld,
+ *                  entries [0, cols/32);
+ *                  MXG_SCALE_PACKED: the packed order of mx_quantize_rowwise_packed
+ *                  (16-byte aligned; scale_ld is ignored), cut into the same
+ *                  segments as the call's experts: the m_splits for the forward
+ *                  activations and the dgrad gradient, G segments of N rows for
+ *                  the forward weights.  The other operands (dgrad weights,
+ *                  both wgrad operands) take plain scales only (MXG_ERR_UNSUPPORTED).
+ *   elem         : MXG_E2M1 or MXG_E4M3
+ *   scale_layout : mxg_scale_layout
  * Requirements: cols % 32 == 0; data 16-byte aligned (32 for E2M1 weights of
  * the a8w4 forward); ld % 16 == 0 (32 for those weights). */
 typedef struct mxg_mx_operand {
@@ -88,7 +99,7 @@ typedef struct mxg_mx_operand {
   int64_t ld;
   int64_t scale_ld;
   int32_t elem;
-  int32_t reserved; /* must be 0 */
+  int32_t scale_layout;
 } mxg_mx_operand;
 
 /* --------------------------------------------------------------------------
@@ -108,6 +119,34 @@ typedef struct mxg_mx_operand {
 mxg_status mx_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                                int32_t elem, void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
                                void* stream);
+
+/* Bytes of the packed scales of a row-wise MX operand of `rows` x `cols`
+ * whose rows are cut into G segments: KC * RTmax * 512, KC = ceil(cols/128),
+ * RTmax = floor((rows + min(rows, G) * 127) / 128) -- at least the row tiles
+ * of every split of `rows` into G segments.  -1 on invalid input. */
+int64_t mx_packed_scale_bytes(int64_t rows, int64_t cols, int32_t G);
+
+/* Row-wise MX quantization (the rule of mx_quantize_rowwise, codes laid out
+ * the same way) with the scales written in the tensor-core staging order, so
+ * that a grouped GEMM reads them without a repacking pass ("Integrate MXFP4
+ * hipblaslt GEMM support", Takeaways: pre-swizzled scales; PR #723 "fused
+ * scale packing kernel").  The rows are cut into segments -- the device
+ * d_m_splits (int32[G]; activations and gradients), or, when d_m_splits is
+ * NULL, G equal segments of rows/G rows (forward weights, rows % G == 0) --
+ * and each segment into tiles of 128 rows, numbered across segments (RT in
+ * all).  The scales of a tile's 128 rows and 4 consecutive blocks form one
+ * 512-byte chunk; chunk (kc, rt) starts at byte (kc * RT + rt) * 512, and the
+ * scale of the tile's row i, block 4*kc + j sits at (i % 32) * 16 + (i / 32) * 4
+ * + j in it.  Bytes with no row or block (segment tails, blocks past cols/32)
+ * are written as 0.
+ *   s_packed : device, 16-byte aligned, s_bytes >= mx_packed_scale_bytes(rows, cols, G)
+ *   d_status : required with d_m_splits; a negative split or a sum != rows
+ *              sets MXG_ERR_SPLITS and nothing is written.
+ * Other arguments and checks as mx_quantize_rowwise. */
+mxg_status mx_quantize_rowwise_packed(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                      int32_t elem, void* q, int64_t ld_q, uint8_t* s_packed,
+                                      int64_t s_bytes, const int32_t* d_m_splits, int32_t G,
+                                      int32_t* d_status, void* stream);
 
 /* Column-wise, segment-padded MX quantization: the wgrad operand of PR #723
  * (`_col_operand_grouped_padded`).  x is BF16 [rows, cols] with the experts'

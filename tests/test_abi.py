@@ -139,8 +139,10 @@ def test_gemm_host_checks(lib):
     assert call(A, W, ws_bytes=16) == 9                        # workspace too small
     assert call(_op(512, 512, 1), _op(1024, 512, 2)) == 5      # E2M1 x E4M3 not provided
     assert call(_op(512, 96, 2), _op(1024, 96, 1)) == 2        # a8w4 needs K % 128
-    bad = _op(512, 512, 1); bad.reserved = 7
-    assert call(bad, W) == 5
+    bad = _op(512, 512, 1); bad.scale_layout = 7
+    assert call(bad, W) == 5                                   # unknown scale layout
+    pk = _op(512, 512, 1); pk.scale_layout = 1; pk.scale = FAKE + 4
+    assert call(pk, W) == 3                                    # packed scales not 16-byte aligned
     d = lib.grouped_gemm_dgrad
     dY, Wt = _op(512, 256, 2), _op(512, 4 * 256, 1)
     assert d(ctypes.byref(dY), ctypes.byref(Wt), vp(FAKE), 4, vp(FAKE), 512, 1, vp(FAKE), ws,
@@ -151,6 +153,38 @@ def test_gemm_host_checks(lib):
              ws, vp(FAKE), None) == 5                          # accumulate needs FP32
     assert w(ctypes.byref(dYt), ctypes.byref(Xt), vp(FAKE), 4, 900, 48, vp(FAKE), 2, 1, vp(FAKE),
              ws, vp(FAKE), None) == 2                          # pad % 32
+    dYp = _op(512, 256, 2); dYp.scale_layout = 1
+    Wtp = _op(512, 4 * 256, 2); Wtp.scale_layout = 1
+    assert d(ctypes.byref(dYp), ctypes.byref(Wtp), vp(FAKE), 4, vp(FAKE), 512, 1, vp(FAKE), ws,
+             vp(FAKE), None) == 5                              # dgrad weights: plain scales only
+    dYtp = _op(256, 1024, 1); dYtp.scale_layout = 1
+    assert w(ctypes.byref(dYtp), ctypes.byref(Xt), vp(FAKE), 4, 900, 32, vp(FAKE), 2, 1, vp(FAKE),
+             ws, vp(FAKE), None) == 5                          # wgrad operands: plain scales only
+
+
+def test_packed_quantize_host_checks(lib):
+    vp = ctypes.c_void_p
+    assert lib.mx_packed_scale_bytes(1000, 160, 4) == 2 * ((1000 + 4 * 127) // 128) * 512
+    assert lib.mx_packed_scale_bytes(3 * 256, 512, 3) == 4 * 8 * 512       # bound, not the 6 exact tiles
+    assert lib.mx_packed_scale_bytes(2, 64, 8) == 1 * ((2 + 2 * 127) // 128) * 512
+    assert lib.mx_packed_scale_bytes(0, 64, 8) == 0
+    assert lib.mx_packed_scale_bytes(10, 48, 8) == -1 and lib.mx_packed_scale_bytes(10, 64, 0) == -1
+    f = lib.mx_quantize_rowwise_packed
+    need = lib.mx_packed_scale_bytes(768, 512, 3)
+    #        x         rows cols ld_x elem q        ld_q s         bytes splits G  status     stream
+    args = [vp(FAKE), 768, 512, 512, 1, vp(FAKE), 256, vp(FAKE), need, None, 3, vp(FAKE), None]
+    bad = list(args); bad[8] = need - 1
+    assert f(*bad) == 2                                                   # packed buffer too small
+    bad = list(args); bad[10] = 5
+    assert f(*bad) == 2                                                   # rows % G with equal segments
+    bad = list(args); bad[9] = vp(FAKE); bad[11] = None
+    assert f(*bad) == 1                                                   # splits without a status word
+    bad = list(args); bad[7] = vp(FAKE + 8)
+    assert f(*bad) == 3                                                   # packed scales misaligned
+    bad = list(args); bad[4] = 3
+    assert f(*bad) == 5                                                   # bad elem
+    bad = list(args); bad[10] = 513
+    assert f(*bad) == 2                                                   # G > 512
 
 
 def test_binding_refuses_cpu_tensors():
