@@ -105,7 +105,8 @@ __global__ void __launch_bounds__(kRowThreads) mx_rowwise_kernel(
 
 // Row-wise with the scales written straight into the tensor-core staging
 // order ("pre-swizzled" scales: "Integrate MXFP4 hipblaslt GEMM support",
-// Takeaways; the "fused scale packing kernel" of the Triton grouped GEMM).
+// Takeaways; the "fused scale packing kernel" of "Grouped MXFP8 GEMMs with
+// HipKittens", ROCm TransformerEngine PR #661).
 // The rows are cut into segments (the routing splits, or G equal segments of
 // seg_rows rows), each segment into tiles of 128 rows, tiles numbered across
 // segments (RT in all); the scales of 128 rows x 4 blocks form a 512-byte
@@ -751,9 +752,20 @@ cudaError_t launch_mx_rowwise_packed(const void* x, int64_t rows, int64_t cols, 
   const int64_t kbp = ((cols / 32) + 3) / 4 * 4;
   const int64_t total = rt_bound * 128 * kbp;
   int64_t blocks = (total + kRowThreads - 1) / kRowThreads;
-  // With splits every CTA scans them first: one resident wave, each CTA then
-  // loops, so the scan is paid once per CTA rather than once per 256 blocks.
-  const int64_t cap = (int64_t)num_sms * 8 * (splits ? 1 : 4);
+  // With splits every CTA scans them first: one resident wave (as many CTAs
+  // as fit on the SMs at once), each CTA then loops, so the scan is paid once
+  // per CTA.  Without splits, a few waves as in the plain kernel.
+  int64_t cap = (int64_t)num_sms * 8 * 4;
+  if (splits) {
+    int per_sm = 0;
+    const void* fn = elem == MXG_E2M1 ? (const void*)mx_rowwise_packed_kernel<MXG_E2M1, true>
+                                      : (const void*)mx_rowwise_packed_kernel<MXG_E4M3, true>;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRowThreads, 0) != cudaSuccess || per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 4;
+    }
+    cap = (int64_t)num_sms * per_sm;
+  }
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   auto* xp = static_cast<const uint16_t*>(x);

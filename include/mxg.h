@@ -129,8 +129,8 @@ int64_t mx_packed_scale_bytes(int64_t rows, int64_t cols, int32_t G);
 /* Row-wise MX quantization (the rule of mx_quantize_rowwise, codes laid out
  * the same way) with the scales written in the tensor-core staging order, so
  * that a grouped GEMM reads them without a repacking pass ("Integrate MXFP4
- * hipblaslt GEMM support", Takeaways: pre-swizzled scales; PR #723 "fused
- * scale packing kernel").  The rows are cut into segments -- the device
+ * hipblaslt GEMM support", Takeaways: pre-swizzled scales; "Grouped MXFP8
+ * GEMMs with HipKittens" PR #661, "fused scale packing kernel").  The rows are cut into segments -- the device
  * d_m_splits (int32[G]; activations and gradients), or, when d_m_splits is
  * NULL, G equal segments of rows/G rows (forward weights, rows % G == 0) --
  * and each segment into tiles of 128 rows, numbered across segments (RT in

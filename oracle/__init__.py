@@ -21,7 +21,8 @@ no blocking or fusion.  Each function cites the passage it follows:
 * "Integrate MXFP4 hipblaslt GEMM support" (PR #697): the per-pass shapes
   (forward contracts hidden, dgrad contracts out, wgrad contracts tokens).
 * "Integrate MXFP4 hipblaslt GEMM support" (PR #697), Takeaways, and the
-  "fused scale packing kernel" commit of PR #723: MX scales written in the
+  "fused scale packing kernel" commit of "Grouped MXFP8 GEMMs with
+  HipKittens" (PR #661): MX scales written in the
   matrix engine's blocked order (``oracle.packed``).
 * The OCP Microscaling Formats (MX) v1.0 specification for the E2M1 / E4M3
   element encodings and the shared-exponent rule.

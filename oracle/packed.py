@@ -5,8 +5,8 @@ TEST INFRASTRUCTURE ONLY (see the package docstring).
 "Integrate MXFP4 hipblaslt GEMM support" (ROCm TransformerEngine PR #697),
 Takeaways: a GEMM fed plain UE8M0 scales ran at about 0.61x of the one fed
 scales already laid out in the matrix engine's blocked order, so that order is
-worth producing in the quantizer itself; "Triton mxfp4 (and a8w4) grouped GEMM
-kernel" (PR #723) does the same with its "fused scale packing kernel" commit.
+worth producing in the quantizer itself; "Grouped MXFP8 GEMMs with HipKittens"
+(PR #661) does the same with its "fused scale packing kernel" commit.
 The blocked order here is the one a Blackwell block-scaled MMA reads: the
 scale factors of 128 rows x 4 blocks (128 contraction elements) form one
 512-byte chunk, which fills four TMEM columns of a 32-lane quarter -- lane l
