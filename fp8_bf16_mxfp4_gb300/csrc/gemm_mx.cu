@@ -62,6 +62,12 @@ constexpr int kATileBytes = BM * 128;  // 128 bytes of K per row per stage
 constexpr int kBTileBytes = BN * 128;
 constexpr int kChunkBytes = 512;       // 128 rows x 4 scale bytes
 constexpr int kTmemCols = 512;
+// Epilogue output staging: per epilogue warp (32 tile rows), two boxes of 16
+// rows x 128 bytes (64 BF16 or 32 FP32 columns) in the TMA 128-byte swizzle.
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBoxRows = 16;
+constexpr int kEpiBoxBytes = kEpiBoxRows * 128;
+constexpr int kEpiWarpBytes = 2 * kEpiBoxBytes;
 constexpr int kSfTmemCol0 = 256;       // scale staging columns start after the accumulator
 
 enum Kind { KIND_MXF4 = 0, KIND_A8W4 = 1, KIND_MXF8 = 2 };
@@ -73,9 +79,6 @@ struct KindCfg {
   static constexpr int kKPS = kStageK / 128;                      // scale k-chunks per stage
   static constexpr int kSfBytes = kKPS * kChunkBytes * 3;         // A: 1 row chunk, B: 2
   static constexpr int kSfCols = kKPS * 12;                       // TMEM columns per stage
-  // instruction descriptor element types (A, B)
-  static constexpr uint32_t kAType = kKind == KIND_MXF4 ? 1u : 0u;  // mxf4: E2M1=1; f8f6f4: E4M3=0
-  static constexpr uint32_t kBType = kKind == KIND_MXF4 ? 1u : (kKind == KIND_A8W4 ? 5u : 0u);
 };
 
 // ---------------------------------------------------------------------------
@@ -215,9 +218,9 @@ struct Smem {
   static constexpr int kBarOff = kSfOff + kStages * KindCfg<kKind>::kSfBytes;
   static constexpr int kNumBars = 3 * kStages + 3;  // full, empty, sready, tmem_full, tmem_empty, drain
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem addr, abort flag
-  static constexpr int kTabOff = kMiscOff + 16;
-  static constexpr int kTabBytes = 5 * (kMaxExperts + 1) * 4;
-  static constexpr int kTotal = kTabOff + kTabBytes + 1024;  // + alignment slack
+  // epilogue staging: one buffer per epilogue warp, 1024-byte aligned (swizzle atoms)
+  static constexpr int kEpiOff = (kMiscOff + 16 + 1023) & ~1023;
+  static constexpr int kTotal = kEpiOff + kEpiWarps * kEpiWarpBytes + 1024;  // + alignment slack
 };
 
 // FP32 output: one 32-column chunk of a row, stored with 32-byte accesses,
@@ -244,7 +247,8 @@ MXG_DEVINL uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
 template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB, const Params p) {
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmOut, const Params p) {
   using Cfg = KindCfg<kKind>;
   using L = Smem<kKind>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -258,19 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_tiles = pv.hdr[1];
   if ((int)blockIdx.x >= total_tiles) return;
 
-  // per-expert tables into shared memory
-  int32_t* t_off = reinterpret_cast<int32_t*>(smem + L::kTabOff);
-  int32_t* t_rt = t_off + (kMaxExperts + 1);
-  int32_t* t_poff = t_rt + (kMaxExperts + 1);
-  int32_t* t_kc = t_poff + (kMaxExperts + 1);
-  int32_t* t_tiles = t_kc + (kMaxExperts + 1);
-  for (int i = threadIdx.x; i <= G; i += kThreads) {
-    t_off[i] = pv.off[i];
-    t_rt[i] = pv.rt[i];
-    t_poff[i] = pv.poff[i];
-    t_kc[i] = pv.kc[i];
-    t_tiles[i] = pv.tiles[i];
-  }
+  // per-expert tables: read in place from the plan (a few loads per tile and role)
+  const int32_t* t_off = pv.off;
+  const int32_t* t_rt = pv.rt;
+  const int32_t* t_poff = pv.poff;
+  const int32_t* t_kc = pv.kc;
+  const int32_t* t_tiles = pv.tiles;
   const uint32_t bar0 = sbase + L::kBarOff;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
@@ -294,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmOut);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -457,13 +455,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // BF16: the whole 128x256 tile is read from TMEM into registers (128
-    // packed words per thread), TMEM is handed back to the MMA warp, and only
-    // then are the rows stored -- the next tile's MMAs overlap the stores.
-    // FP32: 32-column chunks are read and stored in turn, TMEM released after.
+    // Warp q owns TMEM lane quarter q: rows q*32 .. q*32+31 of the tile.  The
+    // output goes out through the warp's staging buffer: two 16-row boxes of
+    // 128 bytes per row (64 BF16 / 32 FP32 columns) in the TMA 128-byte
+    // swizzle, written to global memory by tiled bulk stores -- bulk
+    // reduce-adds when accumulating -- issued by lane 0, so that the tile
+    // leaves the SM as whole lines instead of one 32-byte piece per row and
+    // lane.  A box only partly inside the expert's rows is written by the
+    // lanes of its valid rows directly; columns past the output's last are
+    // clipped by the tensor map.
+    // BF16: the whole tile is read from TMEM into registers (BN/2 packed words
+    // per thread) and TMEM is handed back before any store.  FP32: 32-column
+    // chunks are read and sent in turn; TMEM is handed back after the last read.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t ebuf = sbase + (uint32_t)(L::kEpiOff + quarter * kEpiWarpBytes);
+    const int brow = lane & 15;                                  // row inside this lane's box
+    const uint32_t my_row = ebuf + (uint32_t)((lane >> 4) * kEpiBoxBytes + brow * 128);
     uint32_t acc_phase = 0;
+    bool pending = false;  // lane 0: bulk groups issued from the buffer
+    // stage this lane's 128-byte row piece v[0..31] and send the full boxes
+    auto send = [&](const uint32_t* v, int64_t x, int64_t y0, bool full0, bool full1, bool reduce) {
+      if (lane == 0 && pending) ptx::bulk_wait_group_read0();  // the buffer has been read
+      __syncwarp();
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        ptx::st_shared_v4(my_row + (uint32_t)((k ^ (brow & 7)) << 4), v[4 * k], v[4 * k + 1], v[4 * k + 2],
+                          v[4 * k + 3]);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && (full0 || full1)) {
+        for (int b = 0; b < 2; ++b) {
+          if (!(b == 0 ? full0 : full1)) continue;
+          const uint32_t src = ebuf + (uint32_t)(b * kEpiBoxBytes);
+          const int yy = (int)(y0 + b * kEpiBoxRows);
+          if (reduce) ptx::tma_reduce_add_2d(&tmOut, src, (int)x, yy);
+          else ptx::tma_store_2d(&tmOut, src, (int)x, yy);
+        }
+        ptx::bulk_commit_group();
+        pending = true;
+      }
+    };
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int g, mt, nt;
       Geo e;
@@ -471,11 +503,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ready = ptx::mbar_wait(tmem_full, acc_phase, abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ready)) break;  // the warp leaves together (.aligned TMEM loads)
       ptx::tc_fence_after();
-      const int row = mt * BM + quarter * 32 + lane;
+      const int row0 = mt * BM + quarter * 32;  // the warp's first row inside the expert
+      const int row = row0 + lane;
       const bool row_ok = row < e.M;
       const int64_t orow = e.out_row0 + row;
+      const int64_t oy0 = e.out_row0 + row0;
       const int ncols = min(BN, e.Nn - nt * BN);  // multiple of 32
       const int64_t col0 = (int64_t)nt * BN;
+      const int vrows = e.M - row0;               // the warp's rows inside the expert (may be <= 0)
+      const bool full0 = vrows >= kEpiBoxRows, full1 = vrows >= 2 * kEpiBoxRows;
+      const bool direct = row_ok && !((lane >> 4) == 0 ? full0 : full1);  // partial box: own store
+      const bool skip_out = vrows <= 0 || (e.Kc == 0 && p.accumulate);   // nothing of this warp to write
       if (p.out_dtype == MXG_OUT_BF16) {
         uint32_t h[BN / 2];
 #pragma unroll
@@ -497,37 +535,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(tmem_empty);
-        if (row_ok && !(e.Kc == 0 && p.accumulate)) {
+        if (!skip_out) {
           __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * p.ld_out + col0;
 #pragma unroll
-          for (int c = 0; c < BN / 32; ++c) {
-            if (c * 32 < ncols) {
-              ptx::st_global_v8(dst + c * 32, &h[c * 16]);
-              ptx::st_global_v8(dst + c * 32 + 16, &h[c * 16 + 8]);
+          for (int c4 = 0; c4 < BN / 64; ++c4) {
+            if (c4 * 64 < ncols) {  // warp-uniform
+              send(&h[c4 * 32], col0 + c4 * 64, oy0, full0, full1, false);
+              if (direct) {
+                ptx::st_global_v8(dst + c4 * 64, &h[c4 * 32]);
+                ptx::st_global_v8(dst + c4 * 64 + 16, &h[c4 * 32 + 8]);
+                if (c4 * 64 + 32 < ncols) {
+                  ptx::st_global_v8(dst + c4 * 64 + 32, &h[c4 * 32 + 16]);
+                  ptx::st_global_v8(dst + c4 * 64 + 48, &h[c4 * 32 + 24]);
+                }
+              }
             }
           }
         }
       } else {
-        for (int c = 0; c < BN / 32; ++c) {
-          if (c * 32 >= ncols) break;  // warp-uniform
+        const int nch = ncols / 32;
+        if (e.Kc == 0) {  // nothing in TMEM to read: hand it back at once
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(tmem_empty);
+        }
+        for (int c = 0; c < nch; ++c) {
           uint32_t r[32];
           if (e.Kc > 0) {
             __syncwarp();
             ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(c * 32), r);
             ptx::tmem_ld_wait();
+            if (c == nch - 1) {  // last read: the accumulator is free for the next tile
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(tmem_empty);
+            }
           } else {
-            if (p.accumulate) continue;  // empty expert, accumulating: leave untouched
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = 0;
           }
-          if (row_ok) store_row_chunk_f32(p, orow, col0 + c * 32, r);
+          if (skip_out) continue;  // warp-uniform
+          send(r, col0 + c * 32, oy0, full0, full1, p.accumulate != 0);
+          if (direct) store_row_chunk_f32(p, orow, col0 + c * 32, r);
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(tmem_empty);
       }
       acc_phase ^= 1u;
     }
+    // every bulk store has completed before the CTA ends
+    if (lane == 0 && pending) ptx::bulk_wait_group0();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -665,6 +721,17 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
          make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_cols, a.b_rows, a.b_ld, 128, BN);
   }
   if (!ok) return MXG_ERR_CUDA;
+  // the output as tiled-store destination: columns = N (fwd) or K, rows = S
+  // (fwd, dgrad) or G*N (wgrad); boxes of 16 rows x 128 bytes
+  CUtensorMap tmOut;
+  {
+    const bool f32 = a.out_dtype == MXG_OUT_F32;
+    const int64_t ocols = a.pass == MXG_PASS_FWD ? a.N : a.K;
+    const int64_t orows = a.pass == MXG_PASS_WGRAD ? (int64_t)a.G * a.N : a.total_rows;
+    if (!make_tmap(&tmOut, a.out, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ocols,
+                   orows, a.ld_out * (f32 ? 4 : 2), f32 ? 32 : 64, kEpiBoxRows))
+      return MXG_ERR_CUDA;
+  }
 
   int dev = 0;
   cudaGetDevice(&dev);
@@ -689,9 +756,9 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   }
   const dim3 grid((unsigned)num_sms), block(kThreads);
   switch (kind) {
-    case KIND_MXF4: grouped_mx_gemm_kernel<KIND_MXF4><<<grid, block, smem, stream>>>(tmA, tmB, p); break;
-    case KIND_A8W4: grouped_mx_gemm_kernel<KIND_A8W4><<<grid, block, smem, stream>>>(tmA, tmB, p); break;
-    default: grouped_mx_gemm_kernel<KIND_MXF8><<<grid, block, smem, stream>>>(tmA, tmB, p); break;
+    case KIND_MXF4: grouped_mx_gemm_kernel<KIND_MXF4><<<grid, block, smem, stream>>>(tmA, tmB, tmOut, p); break;
+    case KIND_A8W4: grouped_mx_gemm_kernel<KIND_A8W4><<<grid, block, smem, stream>>>(tmA, tmB, tmOut, p); break;
+    default: grouped_mx_gemm_kernel<KIND_MXF8><<<grid, block, smem, stream>>>(tmA, tmB, tmOut, p); break;
   }
   if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
   return MXG_OK;
