@@ -18,7 +18,8 @@
 //              stage's shared memory for the producer (the partial being
 //              complete means its MMAs have read the stage), and adds
 //              partial * sa[row, kb] * sb[., kb] into fp32 registers; at the
-//              end of the tile the registers are stored (BF16, FP32 or +=).
+//              end of the tile the registers go out through a shared-memory
+//              box per warp by TMA tiled stores (bulk reduce-adds for +=).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -41,6 +42,10 @@ constexpr int kTileBytes = 128 * 128;  // one operand tile per stage: 128 rows x
 constexpr int kSbBytes = 128 * 4;      // wgrad: 128 fp32 column scales per stage
 constexpr int kTmemCols = 512;
 constexpr int kPBufs = 4;  // 128-column partial accumulators in TMEM
+// Output staging: one box of 16 rows x 128 bytes (64 BF16 / 32 FP32 columns,
+// TMA 128-byte swizzle) per promotion warp.
+constexpr int kBoxRows = 16;
+constexpr int kBoxBytes = kBoxRows * 128;
 
 struct BwParams {
   Params p;
@@ -57,14 +62,14 @@ struct BwSmem {
   static constexpr int kBarOff = kSbOff + kStages * kSbBytes;
   static constexpr int kNumBars = 2 * kStages + 2 * kPBufs + 1;  // full, empty, pfull, pempty, drain
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kTabOff = kMiscOff + 16;
-  static constexpr int kTabBytes = 5 * (kMaxExperts + 1) * 4;
-  static constexpr int kTotal = kTabOff + kTabBytes + 1024;
+  static constexpr int kEpiOff = (kMiscOff + 16 + 1023) & ~1023;  // 1024-byte aligned (swizzle atoms)
+  static constexpr int kTotal = kEpiOff + kEpiWarps * kBoxBytes + 1024;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_bw_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                           const __grid_constant__ CUtensorMap tmB, const BwParams bp) {
+                           const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmOut, const BwParams bp) {
   using L = BwSmem;
   const Params& p = bp.p;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -79,18 +84,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_tiles = pv.hdr[1];
   if ((int)blockIdx.x >= total_tiles) return;
 
-  int32_t* t_off = reinterpret_cast<int32_t*>(smem + L::kTabOff);
-  int32_t* t_rt = t_off + (kMaxExperts + 1);
-  int32_t* t_poff = t_rt + (kMaxExperts + 1);
-  int32_t* t_kc = t_poff + (kMaxExperts + 1);
-  int32_t* t_tiles = t_kc + (kMaxExperts + 1);
-  for (int i = threadIdx.x; i <= G; i += kThreads) {
-    t_off[i] = pv.off[i];
-    t_rt[i] = pv.rt[i];
-    t_poff[i] = pv.poff[i];
-    t_kc[i] = pv.kc[i];
-    t_tiles[i] = pv.tiles[i];
-  }
+  // per-expert tables: read in place from the plan
+  const int32_t* t_off = pv.off;
+  const int32_t* t_rt = pv.rt;
+  const int32_t* t_poff = pv.poff;
+  const int32_t* t_kc = pv.kc;
+  const int32_t* t_tiles = pv.tiles;
   const uint32_t bar0 = sbase + L::kBarOff;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
@@ -116,6 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmOut);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -209,6 +209,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int chalf = (warp - 2) >> 2;  // columns [64*chalf, 64*chalf + 64)
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(chalf * 64);
+    // this warp's staging box; lane l's row of it is l % 16 (lanes 0-15 fill it for
+    // rows 0-15 of the warp, then lanes 16-31 for rows 16-31)
+    const uint32_t box = sbase + (uint32_t)(L::kEpiOff + (warp - 2) * kBoxBytes);
+    const int brow = lane & 15;
+    bool pending = false;  // lane 0: bulk groups issued from the box
+    // stage the 128-byte row pieces v of lanes (lane >> 4) == half and, when
+    // the half's 16 rows are all inside the expert, send them as one box
+    auto send_half = [&](int half, const uint32_t* v, int64_t x, int64_t y, bool full, bool reduce) {
+      if (lane == 0 && pending) ptx::bulk_wait_group_read<0>();  // the box has been read
+      __syncwarp();
+      if ((lane >> 4) == half) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          ptx::st_shared_v4(box + (uint32_t)(brow * 128 + ((k ^ (brow & 7)) << 4)), v[4 * k], v[4 * k + 1],
+                            v[4 * k + 2], v[4 * k + 3]);
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && full) {
+        if (reduce) ptx::tma_reduce_add_2d(&tmOut, box, (int)x, (int)y);
+        else ptx::tma_store_2d(&tmOut, box, (int)x, (int)y);
+        ptx::bulk_commit_group();
+        pending = true;
+      }
+    };
     uint32_t kcount = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
@@ -271,8 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (!row_ok || (nk == 0 && p.accumulate)) continue;
+      const int row0 = mt * 128 + quarter * 32;  // the warp's first row inside the expert
+      const int vrows = e.M - row0;
+      if (vrows <= 0 || (nk == 0 && p.accumulate)) continue;  // warp-uniform: nothing to write
+      const bool full[2] = {vrows >= kBoxRows, vrows >= 2 * kBoxRows};
+      const bool direct = row_ok && !full[lane >> 4];  // partial box: the lane stores its own row
       const int64_t col = (int64_t)nt * BN + chalf * 64;
+      const int64_t oy0 = e.out_row0 + row0;
       if (p.out_dtype == MXG_OUT_BF16) {
         uint32_t h[32];
 #pragma unroll
@@ -280,26 +310,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
           h[i] = *reinterpret_cast<const uint32_t*>(&b);
         }
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (e.out_row0 + row) * p.ld_out + col;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) ptx::st_global_v8(dst + 16 * i, h + 8 * i);
+        for (int half = 0; half < 2; ++half) send_half(half, h, col, oy0 + half * kBoxRows, full[half], false);
+        if (direct) {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (e.out_row0 + row) * p.ld_out + col;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) ptx::st_global_v8(dst + 16 * i, h + 8 * i);
+        }
       } else {
-        float* dst = static_cast<float*>(p.out) + (e.out_row0 + row) * p.ld_out + col;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t v[8];
-          if (p.accumulate) {
-            ptx::ld_global_v8(dst + 8 * i, v);
+        for (int piece = 0; piece < 2; ++piece) {  // 32 fp32 columns each
+          const uint32_t* v = reinterpret_cast<const uint32_t*>(acc + 32 * piece);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + acc[8 * i + j]);
-          } else {
+          for (int half = 0; half < 2; ++half)
+            send_half(half, v, col + 32 * piece, oy0 + half * kBoxRows, full[half], p.accumulate != 0);
+        }
+        if (direct) {
+          float* dst = static_cast<float*>(p.out) + (e.out_row0 + row) * p.ld_out + col;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(acc[8 * i + j]);
+          for (int i = 0; i < 8; ++i) {
+            uint32_t v[8];
+            if (p.accumulate) {
+              ptx::ld_global_v8(dst + 8 * i, v);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + acc[8 * i + j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) v[j] = __float_as_uint(acc[8 * i + j]);
+            }
+            ptx::st_global_v8(dst + 8 * i, v);
           }
-          ptx::st_global_v8(dst + 8 * i, v);
         }
       }
     }
+    // every bulk store has completed before the CTA ends
+    if (lane == 0 && pending) ptx::bulk_wait_group0();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();
@@ -359,6 +405,16 @@ mxg_status launch_grouped_bw_gemm(const BwGemmArgs& a, cudaStream_t stream, int 
          make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_cols, a.b_rows, a.b_ld, 128, BN);
   }
   if (!ok) return MXG_ERR_CUDA;
+  // the output as tiled-store destination (see gemm_mx.cu): boxes of 16 rows x 128 bytes
+  CUtensorMap tmOut;
+  {
+    const bool f32 = a.out_dtype == MXG_OUT_F32;
+    const int64_t ocols = a.pass == MXG_PASS_FWD ? a.N : a.K;
+    const int64_t orows = a.pass == MXG_PASS_WGRAD ? (int64_t)a.G * a.N : a.total_rows;
+    if (!make_tmap(&tmOut, a.out, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ocols,
+                   orows, a.ld_out * (f32 ? 4 : 2), f32 ? 32 : 64, kBoxRows))
+      return MXG_ERR_CUDA;
+  }
 
   int dev = 0;
   cudaGetDevice(&dev);
@@ -375,7 +431,7 @@ mxg_status launch_grouped_bw_gemm(const BwGemmArgs& a, cudaStream_t stream, int 
       attr_set[dev] = true;
     }
   }
-  grouped_bw_gemm_kernel<<<num_sms, kThreads, BwSmem::kTotal, stream>>>(tmA, tmB, bp);
+  grouped_bw_gemm_kernel<<<num_sms, kThreads, BwSmem::kTotal, stream>>>(tmA, tmB, tmOut, bp);
   if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
   return MXG_OK;
 }

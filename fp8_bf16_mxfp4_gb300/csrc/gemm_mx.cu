@@ -56,7 +56,7 @@ namespace {
 
 constexpr int BM = 128;           // tile rows (TMEM lanes)
 constexpr int BN = 256;           // tile columns (TMEM fp32 columns)
-constexpr int kStages = 4;
+constexpr int kStages = 4;  // operand pipeline depth
 constexpr int kThreads = 320;
 constexpr int kATileBytes = BM * 128;  // 128 bytes of K per row per stage
 constexpr int kBTileBytes = BN * 128;
@@ -463,31 +463,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // leaves the SM as whole lines instead of one 32-byte piece per row and
     // lane.  A box only partly inside the expert's rows is written by the
     // lanes of its valid rows directly; columns past the output's last are
-    // clipped by the tensor map.
-    // BF16: the whole tile is read from TMEM into registers (BN/2 packed words
-    // per thread) and TMEM is handed back before any store.  FP32: 32-column
-    // chunks are read and sent in turn; TMEM is handed back after the last read.
+    // clipped by the tensor map.  TMEM is handed back right after its last
+    // read: BF16 first reads the whole tile into registers (BN/2 packed words
+    // per thread), so that the buffer waits come after the hand-back; FP32
+    // sends each 32-column chunk as it is read.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t ebuf = sbase + (uint32_t)(L::kEpiOff + quarter * kEpiWarpBytes);
+    const uint32_t buf = sbase + (uint32_t)(L::kEpiOff + quarter * kEpiWarpBytes);
     const int brow = lane & 15;                                  // row inside this lane's box
-    const uint32_t my_row = ebuf + (uint32_t)((lane >> 4) * kEpiBoxBytes + brow * 128);
+    const uint32_t my_off = (uint32_t)((lane >> 4) * kEpiBoxBytes + brow * 128);
     uint32_t acc_phase = 0;
-    bool pending = false;  // lane 0: bulk groups issued from the buffer
+    bool pending = false;  // lane 0: bulk groups issued
     // stage this lane's 128-byte row piece v[0..31] and send the full boxes
     auto send = [&](const uint32_t* v, int64_t x, int64_t y0, bool full0, bool full1, bool reduce) {
-      if (lane == 0 && pending) ptx::bulk_wait_group_read0();  // the buffer has been read
+      // the buffer's previous contents have been read
+      if (lane == 0 && pending) ptx::bulk_wait_group_read<0>();
       __syncwarp();
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        ptx::st_shared_v4(my_row + (uint32_t)((k ^ (brow & 7)) << 4), v[4 * k], v[4 * k + 1], v[4 * k + 2],
-                          v[4 * k + 3]);
+        ptx::st_shared_v4(buf + my_off + (uint32_t)((k ^ (brow & 7)) << 4), v[4 * k], v[4 * k + 1],
+                          v[4 * k + 2], v[4 * k + 3]);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && (full0 || full1)) {
         for (int b = 0; b < 2; ++b) {
           if (!(b == 0 ? full0 : full1)) continue;
-          const uint32_t src = ebuf + (uint32_t)(b * kEpiBoxBytes);
+          const uint32_t src = buf + (uint32_t)(b * kEpiBoxBytes);
           const int yy = (int)(y0 + b * kEpiBoxRows);
           if (reduce) ptx::tma_reduce_add_2d(&tmOut, src, (int)x, yy);
           else ptx::tma_store_2d(&tmOut, src, (int)x, yy);
@@ -495,6 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::bulk_commit_group();
         pending = true;
       }
+    };
+    auto release = [&]() {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(tmem_empty);
     };
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       int g, mt, nt;
@@ -514,67 +520,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full0 = vrows >= kEpiBoxRows, full1 = vrows >= 2 * kEpiBoxRows;
       const bool direct = row_ok && !((lane >> 4) == 0 ? full0 : full1);  // partial box: own store
       const bool skip_out = vrows <= 0 || (e.Kc == 0 && p.accumulate);   // nothing of this warp to write
+      const int nch = ncols / 32;
+      // 32 fp32 columns c of the accumulator (zeros for an empty contraction)
+      auto read_chunk = [&](int c, uint32_t* r) {
+        if (e.Kc > 0) {
+          __syncwarp();
+          ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(c * 32), r);
+          ptx::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0;
+        }
+      };
       if (p.out_dtype == MXG_OUT_BF16) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * p.ld_out + col0;
+        auto store_direct = [&](int c4, const uint32_t* v) {  // 64 columns of this lane's row
+          ptx::st_global_v8(dst + c4 * 64, v);
+          ptx::st_global_v8(dst + c4 * 64 + 16, v + 8);
+          if (c4 * 64 + 32 < ncols) {
+            ptx::st_global_v8(dst + c4 * 64 + 32, v + 16);
+            ptx::st_global_v8(dst + c4 * 64 + 48, v + 24);
+          }
+        };
         uint32_t h[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
-          if (c * 32 < ncols) {
+          if (c < nch) {
             uint32_t r[32];
-            if (e.Kc > 0) {
-              __syncwarp();
-              ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(c * 32), r);
-              ptx::tmem_ld_wait();
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = 0;
-            }
+            read_chunk(c, r);
 #pragma unroll
             for (int i = 0; i < 16; ++i) h[c * 16 + i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) h[c * 16 + i] = 0;
           }
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(tmem_empty);
+        release();
         if (!skip_out) {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * p.ld_out + col0;
 #pragma unroll
           for (int c4 = 0; c4 < BN / 64; ++c4) {
             if (c4 * 64 < ncols) {  // warp-uniform
               send(&h[c4 * 32], col0 + c4 * 64, oy0, full0, full1, false);
-              if (direct) {
-                ptx::st_global_v8(dst + c4 * 64, &h[c4 * 32]);
-                ptx::st_global_v8(dst + c4 * 64 + 16, &h[c4 * 32 + 8]);
-                if (c4 * 64 + 32 < ncols) {
-                  ptx::st_global_v8(dst + c4 * 64 + 32, &h[c4 * 32 + 16]);
-                  ptx::st_global_v8(dst + c4 * 64 + 48, &h[c4 * 32 + 24]);
-                }
-              }
+              if (direct) store_direct(c4, &h[c4 * 32]);
             }
           }
         }
       } else {
-        const int nch = ncols / 32;
-        if (e.Kc == 0) {  // nothing in TMEM to read: hand it back at once
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(tmem_empty);
-        }
         for (int c = 0; c < nch; ++c) {
           uint32_t r[32];
-          if (e.Kc > 0) {
-            __syncwarp();
-            ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(c * 32), r);
-            ptx::tmem_ld_wait();
-            if (c == nch - 1) {  // last read: the accumulator is free for the next tile
-              ptx::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(tmem_empty);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0;
-          }
-          if (skip_out) continue;  // warp-uniform
+          read_chunk(c, r);
+          if (c == nch - 1) release();  // last read: the accumulator is free for the next tile
+          if (skip_out) continue;       // warp-uniform
           send(r, col0 + c * 32, oy0, full0, full1, p.accumulate != 0);
           if (direct) store_row_chunk_f32(p, orow, col0 + c * 32, r);
         }
@@ -621,6 +617,7 @@ PackSizes pack_sizes(int pass, int G, int64_t S, int64_t N, int64_t K, int pad) 
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
 
 }  // namespace
 
@@ -755,10 +752,10 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
     }
   }
   const dim3 grid((unsigned)num_sms), block(kThreads);
-  switch (kind) {
-    case KIND_MXF4: grouped_mx_gemm_kernel<KIND_MXF4><<<grid, block, smem, stream>>>(tmA, tmB, tmOut, p); break;
-    case KIND_A8W4: grouped_mx_gemm_kernel<KIND_A8W4><<<grid, block, smem, stream>>>(tmA, tmB, tmOut, p); break;
-    default: grouped_mx_gemm_kernel<KIND_MXF8><<<grid, block, smem, stream>>>(tmA, tmB, tmOut, p); break;
+  void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmOut, (void*)&p};
+  if (cudaLaunchKernel(fn, grid, block, args, (size_t)smem, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MXG_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
   return MXG_OK;

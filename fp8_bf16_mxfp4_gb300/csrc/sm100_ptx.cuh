@@ -92,8 +92,9 @@ MXG_DEVINL void tma_reduce_add_2d(const void* tmap, uint32_t src, int32_t x, int
                : "memory");
 }
 MXG_DEVINL void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// the shared-memory sources of every committed group have been read
-MXG_DEVINL void bulk_wait_group_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// the shared-memory sources of all but the newest N committed groups have been read
+template <int N>
+MXG_DEVINL void bulk_wait_group_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 // every committed group has completed (its global writes performed)
 MXG_DEVINL void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 MXG_DEVINL void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
