@@ -24,6 +24,14 @@ the MXFP8 E4M3 reference quantizer of PR #745):
 Readings where the pages are silent (all written out in the design notes):
 all-zero blocks get scale byte 0x00 and zero codes; negative values that round
 to zero keep their sign bit; NaN/Inf inputs are outside the contract.
+
+Selectable scale rule ``rule="round_up"``: the TransformerEngine recipe that the
+same PR #745 review describes (the scale is amax / 448 taken to E8M0, i.e. a
+power of two that never lets an element saturate, with the same -127 floor):
+e is the smallest integer with maxval * 2^e >= amax (maxval 448 for E4M3, 6 for
+E2M1), clamped to [-127, 127]; -127 for an all-zero block.  It differs from
+the OCP rule only when amax's mantissa exceeds maxval's (1.75 / 1.5), where the
+OCP rule saturates the largest elements and this one takes the next exponent.
 """
 
 from __future__ import annotations
@@ -33,6 +41,8 @@ import numpy as np
 E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
 BLOCK = 32
 EMAX = {"e2m1": 2, "e4m3": 8}
+MAXVAL = {"e2m1": 6.0, "e4m3": 448.0}
+RULES = ("ocp", "round_up")
 SIGN_SHIFT = {"e2m1": 3, "e4m3": 7}
 
 
@@ -94,17 +104,25 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def shared_exponent(amax: np.ndarray, elem: str) -> np.ndarray:
-    """floor(log2(amax)) - emax, clamped to [-127, 127]; -127 for amax == 0."""
+def shared_exponent(amax: np.ndarray, elem: str, rule: str = "ocp") -> np.ndarray:
+    """OCP: floor(log2(amax)) - emax.  round_up: the smallest e with
+    maxval * 2^e >= amax.  Both clamped to [-127, 127]; -127 for amax == 0."""
+    if rule not in RULES:
+        raise ValueError(rule)
     amax = np.asarray(amax, dtype=np.float64)
     _, ex = np.frexp(amax)                     # amax = f * 2^ex, f in [0.5, 1)
     e = (ex.astype(np.int64) - 1) - EMAX[elem]
+    if rule == "round_up":
+        # maxval * 2^(e - 1) < 2^floor(log2 amax) <= amax, so the smallest
+        # exponent that covers amax is e or e + 1 (exact float64 comparison)
+        e = np.where(np.ldexp(MAXVAL[elem], e) >= amax, e, e + 1)
     e = np.where(amax == 0.0, -127, e)
     return np.clip(e, -127, 127)
 
 
-def quantize_mx(x_bits: np.ndarray, elem: str):
-    """Quantize BF16 bits along the last axis in blocks of 32.
+def quantize_mx(x_bits: np.ndarray, elem: str, rule: str = "ocp"):
+    """Quantize BF16 bits along the last axis in blocks of 32 (scale rule
+    ``rule``, see ``shared_exponent``).
 
     Returns (codes uint8 [..., C], scale bytes uint8 [..., C/32]).  Codes are
     one per element (unpacked); see ``pack_e2m1``."""
@@ -114,7 +132,7 @@ def quantize_mx(x_bits: np.ndarray, elem: str):
         raise ValueError("quantization axis must be a multiple of 32")
     xb = x.reshape(x.shape[:-1] + (C // BLOCK, BLOCK))
     amax = np.abs(xb).max(axis=-1)
-    e = shared_exponent(amax, elem)
+    e = shared_exponent(amax, elem, rule)
     y = np.ldexp(xb, -e[..., None])            # exact: power-of-two rescale
     codes = round_to_grid(y, elem).reshape(x.shape)
     return codes, (e + 127).astype(np.uint8)
@@ -143,13 +161,13 @@ def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
     return out
 
 
-def quantize_mx_rowwise(x_bits: np.ndarray, elem: str):
+def quantize_mx_rowwise(x_bits: np.ndarray, elem: str, rule: str = "ocp"):
     """Row-wise operand of a K-major GEMM: BF16 [R, C] quantized along C.
 
     Returns (data, scale) in the plain interchange layout: data [R, C/2]
     packed E2M1 or [R, C] E4M3 bytes, scale [R, C/32] UE8M0 bytes.  This is the
     ``_row_operand`` bridge of PR #723 ((N, K/2) data, (N, K/32) scales)."""
-    codes, scale = quantize_mx(x_bits, elem)
+    codes, scale = quantize_mx(x_bits, elem, rule)
     data = pack_e2m1(codes) if elem == "e2m1" else codes
     return data, scale
 
@@ -161,7 +179,8 @@ def padded_offsets(m_splits, pad: int) -> np.ndarray:
     return np.concatenate([[0], np.cumsum(p)]).astype(np.int64)
 
 
-def quantize_mx_colwise_segment_padded(x_bits: np.ndarray, m_splits, pad: int, elem: str):
+def quantize_mx_colwise_segment_padded(x_bits: np.ndarray, m_splits, pad: int, elem: str,
+                                       rule: str = "ocp"):
     """Columnwise, segment-padded operand of the variable-K wgrad (PR #723,
     ``_col_operand_grouped_padded``: (C, Mpad/2) data + scales).
 
@@ -187,7 +206,7 @@ def quantize_mx_colwise_segment_padded(x_bits: np.ndarray, m_splits, pad: int, e
             continue
         seg = np.zeros((C, p_g), dtype=np.uint16)        # +0.0 padding
         seg[:, : m[g]] = x_bits[off[g]: off[g + 1]].T
-        cg, sg = quantize_mx(seg, elem)
+        cg, sg = quantize_mx(seg, elem, rule)
         codes[:, poff[g]: poff[g + 1]] = cg
         scale[:, poff[g] // BLOCK: poff[g + 1] // BLOCK] = sg
     data = pack_e2m1(codes) if elem == "e2m1" else codes

@@ -53,12 +53,21 @@ def floor_log2_bf16_magnitude(bits: int):
     return -133 + (m.bit_length() - 1)           # subnormal: m * 2^-133
 
 
-def mx_scale_exponent(block_bits, elem: str) -> int:
+def mx_scale_exponent(block_bits, elem: str, rule: str = "ocp") -> int:
     mags = [b & 0x7FFF for b in block_bits]
     amax_bits = max(mags)                          # magnitude order == integer order
     fl = floor_log2_bf16_magnitude(amax_bits)
     if fl is None:
         return -127
+    if rule == "round_up":
+        # walk powers of two: the smallest 2^e with maxval * 2^e >= amax
+        amax = bf16_value(amax_bits)
+        e = 0
+        while _FMT[elem]["max_val"] * Fraction(2) ** e < amax:
+            e += 1
+        while _FMT[elem]["max_val"] * Fraction(2) ** (e - 1) >= amax:
+            e -= 1
+        return max(-127, min(127, e))
     emax = 2 if elem == "e2m1" else 8
     return max(-127, min(127, fl - emax))
 
@@ -107,9 +116,9 @@ def encode(v: Fraction, elem: str, negative: bool) -> int:
     return code_mag | ((1 << p["sign_bit"]) if negative else 0)
 
 
-def quantize_block_mx(block_bits, elem: str):
+def quantize_block_mx(block_bits, elem: str, rule: str = "ocp"):
     """One 32-element BF16 block -> (scale byte, list of codes)."""
-    e = mx_scale_exponent(block_bits, elem)
+    e = mx_scale_exponent(block_bits, elem, rule)
     codes = []
     for b in block_bits:
         v = bf16_value(b) / (Fraction(2) ** e)

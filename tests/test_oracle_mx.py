@@ -210,3 +210,66 @@ def test_colwise_rejects_bad_splits():
         oracle.quantize_mx_colwise_segment_padded(x, [12, -2], 32, "e2m1")
     with pytest.raises(ValueError):
         oracle.quantize_mx_colwise_segment_padded(x, [10], 48, "e2m1")
+
+
+# ---------------------------------------------------------------- round-up scale rule
+
+def test_golden_blocks_round_up(golden_dir):
+    recs = read_records(os.path.join(golden_dir, "mx_roundup_blocks.txt"))
+    assert len(recs) >= 8
+    for name, elem, scale_hex, data_hex, vals in recs:
+        toks = vals.split()
+        v = [parse_value(t) for t in toks] + [0.0] * (32 - len(toks))
+        bits = bits_of(v)
+        data, scale = oracle.quantize_mx_rowwise(bits[None, :], elem, rule="round_up")
+        assert scale[0].tobytes().hex() == scale_hex, name
+        assert data[0].tobytes().hex() == data_hex, name
+        sb, codes = scalar.quantize_block_mx([int(b) for b in bits], elem, rule="round_up")
+        assert sb == int(scale_hex, 16), name
+
+
+@pytest.mark.parametrize("elem", ["e2m1", "e4m3"])
+def test_round_up_exponent_is_the_smallest_covering_power(elem):
+    """Over every finite positive BF16 amax: maxval * 2^e >= amax, and 2^(e-1)
+    would not cover it (unless e sits at the -127 floor)."""
+    bits = np.arange(1, 0x7F80, dtype=np.uint16)
+    amax = oracle.mx.bf16_to_f64(bits)
+    e = oracle.shared_exponent(amax, elem, rule="round_up")
+    mv = 6.0 if elem == "e2m1" else 448.0
+    assert (np.ldexp(mv, e) >= amax).all()
+    assert ((e == -127) | (np.ldexp(mv, e - 1) < amax)).all()
+    # against the OCP exponent: equal, or one more exactly where OCP saturates the amax
+    eo = oracle.shared_exponent(amax, elem)
+    over = np.ldexp(mv, eo) < amax
+    assert np.array_equal(e, np.clip(eo + over, -127, 127))
+
+
+@pytest.mark.parametrize("elem", ["e2m1", "e4m3"])
+def test_round_up_never_saturates_and_matches_scalar(elem):
+    rng = np.random.default_rng(17)
+    x = synth.normal_bf16(rng, (64, 32), std=3.0, outlier_frac=0.05)
+    x[:4] = synth.f32_to_bf16_bits(np.float32(2.0) ** rng.integers(-140, 120, size=(4, 32)).astype(np.float32))
+    codes, scale = oracle.quantize_mx(x, elem, rule="round_up")
+    e = scale.astype(np.int64) - 127
+    xs = oracle.mx.bf16_to_f64(x).reshape(64, 1, 32)
+    mv = 6.0 if elem == "e2m1" else 448.0
+    assert (np.abs(np.ldexp(xs, -e[..., None])) <= mv).all()
+    for r in range(0, 64, 7):
+        sb, cs = scalar.quantize_block_mx([int(b) for b in x[r]], elem, rule="round_up")
+        assert sb == int(scale[r, 0]) and cs == [int(c) for c in codes[r]]
+
+
+def test_round_up_colwise_matches_rowwise_of_the_transposed_segments():
+    rng = np.random.default_rng(23)
+    splits = [5, 0, 40, 33]
+    x = synth.normal_bf16(rng, (sum(splits), 64), std=2.0, outlier_frac=0.05)
+    d, s, poff = oracle.quantize_mx_colwise_segment_padded(x, splits, 32, "e4m3", rule="round_up")
+    off = np.concatenate([[0], np.cumsum(splits)])
+    for g, m in enumerate(splits):
+        if m == 0:
+            continue
+        seg = np.zeros((64, int(poff[g + 1] - poff[g])), dtype=np.uint16)
+        seg[:, :m] = x[off[g]: off[g + 1]].T
+        dg, sg = oracle.quantize_mx_rowwise(seg, "e4m3", rule="round_up")
+        assert np.array_equal(d[:, poff[g]: poff[g + 1]], dg)
+        assert np.array_equal(s[:, poff[g] // 32: poff[g + 1] // 32], sg)
