@@ -131,8 +131,18 @@ def _codes_cols(elem: str, cols: int) -> int:
     return cols // 2 if elem == "e2m1" else cols
 
 
+SCALE_RULES = {"ocp": 0, "round_up": 0x100}  # MXG_SCALE_ROUND_UP
+
+
+def _quant_elem(elem: str, rule: str) -> int:
+    """The quantizers' elem argument: format code with the scale-rule flag."""
+    if rule not in SCALE_RULES:
+        raise ValueError(f"unknown scale rule {rule!r} (ocp or round_up)")
+    return ELEM[elem] | SCALE_RULES[rule]
+
+
 def mx_quantize_rowwise(x: torch.Tensor, elem: str, q: torch.Tensor | None = None,
-                        s: torch.Tensor | None = None) -> MXOperand:
+                        s: torch.Tensor | None = None, rule: str = "ocp") -> MXOperand:
     """BF16 [rows, cols] -> MX operand quantized along cols."""
     _need_cuda(x)
     if x.dtype != torch.bfloat16 or x.dim() != 2:
@@ -143,7 +153,7 @@ def mx_quantize_rowwise(x: torch.Tensor, elem: str, q: torch.Tensor | None = Non
     if s is None:
         s = torch.empty((rows, cols // 32), dtype=torch.uint8, device=x.device)
     lib = _lib.load()
-    _ok(lib.mx_quantize_rowwise(_ptr(x), rows, cols, _ld(x, cols), ELEM[elem], _ptr(q),
+    _ok(lib.mx_quantize_rowwise(_ptr(x), rows, cols, _ld(x, cols), _quant_elem(elem, rule), _ptr(q),
                                 _ld(q, _codes_cols(elem, cols)), _ptr(s), _ld(s, cols // 32),
                                 _stream(x.device)), "mx_quantize_rowwise")
     return MXOperand(q, s, elem, cols)
@@ -157,7 +167,7 @@ def mx_packed_scale_bytes(rows: int, cols: int, G: int) -> int:
 
 def mx_quantize_rowwise_packed(x: torch.Tensor, elem: str, m_splits: torch.Tensor | None = None,
                                groups: int | None = None, status: torch.Tensor | None = None,
-                               check: bool = False) -> MXOperand:
+                               check: bool = False, rule: str = "ocp") -> MXOperand:
     """BF16 [rows, cols] -> MX operand whose scales are already in the grouped
     GEMM's tensor-core staging order (no repacking pass in the GEMM).  Rows
     are cut into segments by the device ``m_splits`` (activations and
@@ -179,7 +189,7 @@ def mx_quantize_rowwise_packed(x: torch.Tensor, elem: str, m_splits: torch.Tenso
     s = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=x.device)
     st = status if status is not None else status_tensor(x.device)
     lib = _lib.load()
-    _ok(lib.mx_quantize_rowwise_packed(_ptr(x), rows, cols, _ld(x, cols), ELEM[elem], _ptr(q),
+    _ok(lib.mx_quantize_rowwise_packed(_ptr(x), rows, cols, _ld(x, cols), _quant_elem(elem, rule), _ptr(q),
                                        _ld(q, _codes_cols(elem, cols)), _ptr(s), s.numel(),
                                        _ptr(m_splits), G, _ptr(st),
                                        _stream(x.device)), "mx_quantize_rowwise_packed")
@@ -190,7 +200,8 @@ def mx_quantize_rowwise_packed(x: torch.Tensor, elem: str, m_splits: torch.Tenso
 
 def mx_quantize_colwise_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, pad_multiple: int,
                                        elem: str, capacity: int | None = None,
-                                       status: torch.Tensor | None = None, check: bool = False):
+                                       status: torch.Tensor | None = None, check: bool = False,
+                                       rule: str = "ocp"):
     """BF16 [S, C] with experts' rows concatenated -> (operand [C, capacity],
     int64 padded offsets [G+1]).  Columns beyond the last expert's padded end
     are left uninitialised."""
@@ -205,7 +216,7 @@ def mx_quantize_colwise_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, 
     st = status if status is not None else status_tensor(x.device)
     lib = _lib.load()
     _ok(lib.mx_quantize_colwise_segment_padded(
-        _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, pad_multiple, ELEM[elem], _ptr(qT),
+        _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, pad_multiple, _quant_elem(elem, rule), _ptr(qT),
         _ld(qT, _codes_cols(elem, capacity)), _ptr(sT), _ld(sT, capacity // 32), capacity,
         _ptr(poff), _ptr(st), _stream(x.device)),
         "mx_quantize_colwise_segment_padded")
@@ -217,7 +228,8 @@ def mx_quantize_colwise_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, 
 def mx_quantize_dual_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, pad_multiple: int,
                                     elem: str, capacity: int | None = None,
                                     q: torch.Tensor | None = None, s: torch.Tensor | None = None,
-                                    status: torch.Tensor | None = None, check: bool = False):
+                                    status: torch.Tensor | None = None, check: bool = False,
+                                    rule: str = "ocp"):
     """BF16 [S, C] -> (row-wise operand [S, C], column-wise operand
     [C, capacity], int64 padded offsets [G+1]) from one read of x; the same
     bytes as mx_quantize_rowwise plus mx_quantize_colwise_segment_padded."""
@@ -238,7 +250,7 @@ def mx_quantize_dual_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, pad
     st = status if status is not None else status_tensor(x.device)
     lib = _lib.load()
     _ok(lib.mx_quantize_dual_segment_padded(
-        _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, pad_multiple, ELEM[elem], _ptr(q),
+        _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, pad_multiple, _quant_elem(elem, rule), _ptr(q),
         _ld(q, _codes_cols(elem, C)), _ptr(s), _ld(s, C // 32), _ptr(qT),
         _ld(qT, _codes_cols(elem, capacity)), _ptr(sT), _ld(sT, capacity // 32), capacity,
         _ptr(poff), _ptr(st), _stream(x.device)),

@@ -87,6 +87,9 @@ inline mxg_status cuda_status(cudaError_t e) {
 
 inline int64_t code_bytes(int elem, int64_t cols) { return elem == MXG_E2M1 ? cols / 2 : cols; }
 inline bool valid_elem(int32_t e) { return e == MXG_E2M1 || e == MXG_E4M3; }
+// A quantizer's elem argument: the element format, optionally with the
+// MXG_SCALE_ROUND_UP rule flag (carried on to the launchers).
+inline bool valid_quant_elem(int32_t e) { return valid_elem(e & ~MXG_SCALE_ROUND_UP); }
 
 // Host checks of one MX GEMM operand.  An operand with no elements (rows == 0,
 // or cols == 0 where `allow_no_cols`) may have NULL data and scale pointers.
@@ -204,9 +207,9 @@ mxg_status mxg_check_status(int32_t* d_status, void* stream) {
 mxg_status mx_quantize_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                                int32_t elem, void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
                                void* stream) {
-  if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (!valid_quant_elem(elem)) return MXG_ERR_UNSUPPORTED;
   if (rows < 0 || cols <= 0 || cols % 32 != 0) return MXG_ERR_SHAPE;
-  if (ld_x < cols || ld_q < code_bytes(elem, cols) || ld_s < cols / 32) return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < code_bytes(elem & ~MXG_SCALE_ROUND_UP, cols) || ld_s < cols / 32) return MXG_ERR_SHAPE;
   // codes are written 16 bytes per block (E2M1) or two 16-byte halves (E4M3)
   if (ld_x % 8 != 0 || ld_q % 16 != 0) return MXG_ERR_ALIGN;
   if (rows == 0) return MXG_OK;  // nothing to read or write; pointers may be NULL
@@ -232,11 +235,11 @@ mxg_status mx_quantize_rowwise_packed(const void* x, int64_t rows, int64_t cols,
                                       int32_t elem, void* q, int64_t ld_q, uint8_t* s_packed,
                                       int64_t s_bytes, const int32_t* d_m_splits, int32_t G,
                                       int32_t* d_status, void* stream) {
-  if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (!valid_quant_elem(elem)) return MXG_ERR_UNSUPPORTED;
   if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
   if (rows < 0 || cols <= 0 || cols % 32 != 0) return MXG_ERR_SHAPE;
   if (d_m_splits == nullptr && rows % G != 0) return MXG_ERR_SHAPE;
-  if (ld_x < cols || ld_q < code_bytes(elem, cols)) return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < code_bytes(elem & ~MXG_SCALE_ROUND_UP, cols)) return MXG_ERR_SHAPE;
   if (ld_x % 8 != 0 || ld_q % 16 != 0) return MXG_ERR_ALIGN;
   if (d_m_splits != nullptr && d_status == nullptr) return MXG_ERR_NULL;
   const int64_t need = mx_packed_scale_bytes(rows, cols, G);
@@ -264,12 +267,12 @@ mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64
                                               int64_t capacity, int64_t* d_pad_offsets,
                                               int32_t* d_status, void* stream) {
   if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
-  if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (!valid_quant_elem(elem)) return MXG_ERR_UNSUPPORTED;
   if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
   if (pad_multiple <= 0 || pad_multiple % 32 != 0) return MXG_ERR_SHAPE;
   if (rows < 0 || cols <= 0 || cols % 32 != 0 || capacity < 0 || capacity % 32 != 0)
     return MXG_ERR_SHAPE;
-  if (ld_x < cols || ld_q < code_bytes(elem, capacity) || ld_s < capacity / 32) return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < code_bytes(elem & ~MXG_SCALE_ROUND_UP, capacity) || ld_s < capacity / 32) return MXG_ERR_SHAPE;
   if (ld_x % 8 != 0 || ld_q % 16 != 0) return MXG_ERR_ALIGN;
   // x may be NULL when there are no rows; qT / sT when there is no capacity
   if ((rows > 0 && x == nullptr) || (capacity > 0 && (qT == nullptr || sT == nullptr)))
@@ -293,13 +296,13 @@ mxg_status mx_quantize_dual_segment_padded(const void* x, int64_t rows, int64_t 
                                            int64_t capacity, int64_t* d_pad_offsets,
                                            int32_t* d_status, void* stream) {
   if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
-  if (!valid_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (!valid_quant_elem(elem)) return MXG_ERR_UNSUPPORTED;
   if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
   if (pad_multiple <= 0 || pad_multiple % 32 != 0) return MXG_ERR_SHAPE;
   if (rows < 0 || cols <= 0 || cols % 32 != 0 || capacity < 0 || capacity % 32 != 0)
     return MXG_ERR_SHAPE;
-  if (ld_x < cols || ld_q < code_bytes(elem, cols) || ld_s < cols / 32 ||
-      ld_qT < code_bytes(elem, capacity) || ld_sT < capacity / 32)
+  if (ld_x < cols || ld_q < code_bytes(elem & ~MXG_SCALE_ROUND_UP, cols) || ld_s < cols / 32 ||
+      ld_qT < code_bytes(elem & ~MXG_SCALE_ROUND_UP, capacity) || ld_sT < capacity / 32)
     return MXG_ERR_SHAPE;
   if (ld_x % 8 != 0 || ld_q % 16 != 0 || ld_qT % 16 != 0) return MXG_ERR_ALIGN;
   // x, q, s may be NULL when there are no rows; qT / sT when there is no capacity

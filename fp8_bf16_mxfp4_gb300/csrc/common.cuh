@@ -42,7 +42,13 @@ MXG_DEVINL uint32_t bf16x2_absmax_bits(uint32_t w) {
 
 // MX shared exponent from a BF16 magnitude pattern (OCP MX v1.0 rule with the
 // -127 floor): floor(log2(amax)) - emax clamped to [-127, 127]; -127 for 0.
-MXG_DEVINL int mx_exponent_from_amax_bits(uint32_t amax, int emax) {
+// With `round_up` (the TransformerEngine recipe of the PR #745 review: amax /
+// maxval taken up to a power of two) it is the smallest e with maxval * 2^e >=
+// amax: one more than the OCP exponent exactly when amax's mantissa exceeds
+// maxval's, i.e. its 7 BF16 mantissa bits exceed `up_mant` (1.75 = 1 + 96/128
+// for E4M3's 448, 1.5 = 1 + 64/128 for E2M1's 6).  A subnormal amax lands on
+// the -127 floor under either rule.
+MXG_DEVINL int mx_exponent_from_amax_bits(uint32_t amax, int emax, bool round_up = false, int up_mant = 0) {
   const int E = (int)(amax >> 7);
   const int m = (int)(amax & 0x7F);
   int fl;
@@ -53,7 +59,7 @@ MXG_DEVINL int mx_exponent_from_amax_bits(uint32_t amax, int emax) {
   } else {
     return -127;
   }
-  int e = fl - emax;
+  int e = fl - emax + ((round_up && E != 0 && m > up_mant) ? 1 : 0);
   return e < -127 ? -127 : (e > 127 ? 127 : e);
 }
 

@@ -28,11 +28,18 @@ struct MxFmt;
 template <>
 struct MxFmt<MXG_E2M1> {
   static constexpr int kEmax = 2;
+  static constexpr int kUpMant = 64;  // 6 = (1 + 64/128) * 2^2
 };
 template <>
 struct MxFmt<MXG_E4M3> {
   static constexpr int kEmax = 8;
+  static constexpr int kUpMant = 96;  // 448 = (1 + 96/128) * 2^8
 };
+
+template <int kElem>
+MXG_DEVINL int mx_exponent(uint32_t am, bool round_up) {
+  return mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax, round_up, MxFmt<kElem>::kUpMant);
+}
 
 // Quantize 8 BF16 values (four 32-bit words) with inverse scale `sinv`.
 // E2M1 -> one 32-bit word (8 nibbles); E4M3 -> two 32-bit words.
@@ -63,7 +70,7 @@ constexpr int kRowThreads = 256;
 template <int kElem>
 __global__ void __launch_bounds__(kRowThreads) mx_rowwise_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
-    uint8_t* __restrict__ q, int64_t ld_q, uint8_t* __restrict__ s, int64_t ld_s) {
+    uint8_t* __restrict__ q, int64_t ld_q, uint8_t* __restrict__ s, int64_t ld_s, bool round_up) {
   const int64_t blocks_per_row = cols >> 5;
   const int64_t total = rows * blocks_per_row;
   const int64_t step = (int64_t)gridDim.x * kRowThreads;
@@ -80,7 +87,7 @@ __global__ void __launch_bounds__(kRowThreads) mx_rowwise_kernel(
     uint32_t am = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) am = max(am, bf16x2_absmax_bits(w[i]));
-    const int e = mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax);
+    const int e = mx_exponent<kElem>(am, round_up);
     const float sinv = pow2_neg(e);
     if constexpr (kElem == MXG_E2M1) {
       uint4 o;
@@ -122,7 +129,7 @@ template <int kElem, bool kSplits>
 __global__ void __launch_bounds__(kRowThreads) mx_rowwise_packed_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
     uint8_t* __restrict__ q, int64_t ld_q, uint8_t* __restrict__ sp,
-    const int32_t* __restrict__ splits, int G, int64_t seg_rows, int32_t* status) {
+    const int32_t* __restrict__ splits, int G, int64_t seg_rows, int32_t* status, bool round_up) {
   __shared__ int64_t s_off[kMaxExperts + 1];  // row offsets of the segments
   __shared__ int32_t s_rtp[kMaxExperts + 1];  // first tile of each segment; [G] = RT
   __shared__ int64_t warp_m[kRowThreads / 32];
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(kRowThreads) mx_rowwise_packed_kernel(
         uint32_t am = 0;
 #pragma unroll
         for (int k = 0; k < 16; ++k) am = max(am, bf16x2_absmax_bits(w[k]));
-        const int e = mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax);
+        const int e = mx_exponent<kElem>(am, round_up);
         const float sinv = pow2_neg(e);
         if constexpr (kElem == MXG_E2M1) {
           uint4 o;
@@ -357,11 +364,11 @@ MXG_DEVINL void bw_quantize8(const uint32_t* w, float s, uint32_t* o) {
 // Quantizes one 32-element block (16 words of bf16 pairs, element 2i in the
 // low half) and writes its codes and scale.
 template <int kElem>
-MXG_DEVINL void emit_col_block(const uint32_t* w, uint8_t* qrow, uint8_t* srow) {
+MXG_DEVINL void emit_col_block(const uint32_t* w, uint8_t* qrow, uint8_t* srow, bool round_up) {
   uint32_t am = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) am = max(am, bf16x2_absmax_bits(w[i]));
-  const int e = mx_exponent_from_amax_bits(am, MxFmt<kElem>::kEmax);
+  const int e = mx_exponent<kElem>(am, round_up);
   const float sinv = pow2_neg(e);
   if constexpr (kElem == MXG_E2M1) {
     uint4 o;
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
     const int32_t* __restrict__ splits, int G, int pad, uint8_t* __restrict__ qT, int64_t ld_q,
     void* __restrict__ sT, int64_t ld_s, int64_t capacity, int64_t* __restrict__ pad_offsets,
     int32_t* status, uint8_t* __restrict__ q_row, int64_t ld_qr, uint8_t* __restrict__ s_row,
-    int64_t ld_sr) {
+    int64_t ld_sr, bool round_up) {
   static_assert(kColTokens == 128 && kColCols == 128 && kColThreads == 256, "thread mapping");
   static_assert(!(kDual && kBw), "the dual pass is MX only");
   __shared__ SegTable tab;
@@ -512,9 +519,9 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
       if (jb < ptot && col < cols) {  // beyond the last expert: nothing written
         const int64_t qoff = (jb >> 5) * kBytesPerBlock;
         uint8_t* s8 = static_cast<uint8_t*>(sT);
-        emit_col_block<kElem>(wa, qT + col * ld_q + qoff, s8 + col * ld_s + (jb >> 5));
+        emit_col_block<kElem>(wa, qT + col * ld_q + qoff, s8 + col * ld_s + (jb >> 5), round_up);
         if (col + 1 < cols)
-          emit_col_block<kElem>(wb, qT + (col + 1) * ld_q + qoff, s8 + (col + 1) * ld_s + (jb >> 5));
+          emit_col_block<kElem>(wb, qT + (col + 1) * ld_q + qoff, s8 + (col + 1) * ld_s + (jb >> 5), round_up);
       }
     } else {
       // the 128-token block's amax over the four quarter lanes (all lanes
@@ -553,7 +560,7 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
               w[4 * i] = v4.x; w[4 * i + 1] = v4.y; w[4 * i + 2] = v4.z; w[4 * i + 3] = v4.w;
             }
             emit_col_block<kElem>(w, q_row + sr * ld_qr + (colb >> 5) * kBytesPerBlock,
-                                  s_row + sr * ld_sr + (colb >> 5));
+                                  s_row + sr * ld_sr + (colb >> 5), round_up);
           }
         }
       }
@@ -728,6 +735,8 @@ __global__ void __launch_bounds__(256, kWCtasPerSm) bw_weight_kernel(
 cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int elem,
                               void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,
                               cudaStream_t stream, int num_sms) {
+  const bool round_up = (elem & MXG_SCALE_ROUND_UP) != 0;  // rule flag carried in elem
+  elem &= 0xFF;
   const int64_t total = rows * (cols / 32);
   const int threads = kRowThreads;
   int64_t blocks = (total + threads - 1) / threads;
@@ -738,10 +747,10 @@ cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t
   auto* qp = static_cast<uint8_t*>(q);
   if (elem == MXG_E2M1)
     mx_rowwise_kernel<MXG_E2M1><<<(unsigned)blocks, threads, 0, stream>>>(xp, rows, cols, ld_x, qp,
-                                                                          ld_q, s, ld_s);
+                                                                          ld_q, s, ld_s, round_up);
   else
     mx_rowwise_kernel<MXG_E4M3><<<(unsigned)blocks, threads, 0, stream>>>(xp, rows, cols, ld_x, qp,
-                                                                          ld_q, s, ld_s);
+                                                                          ld_q, s, ld_s, round_up);
   return cudaGetLastError();
 }
 
@@ -749,6 +758,8 @@ cudaError_t launch_mx_rowwise_packed(const void* x, int64_t rows, int64_t cols, 
                                      void* q, int64_t ld_q, uint8_t* sp, const int32_t* splits, int G,
                                      int64_t seg_rows, int64_t rt_bound, int32_t* status,
                                      cudaStream_t stream, int num_sms) {
+  const bool round_up = (elem & MXG_SCALE_ROUND_UP) != 0;  // rule flag carried in elem
+  elem &= 0xFF;
   const int64_t kbp = ((cols / 32) + 3) / 4 * 4;
   const int64_t total = rt_bound * 128 * kbp;
   int64_t blocks = (total + kRowThreads - 1) / kRowThreads;
@@ -774,17 +785,17 @@ cudaError_t launch_mx_rowwise_packed(const void* x, int64_t rows, int64_t cols, 
   if (elem == MXG_E2M1) {
     if (splits)
       mx_rowwise_packed_kernel<MXG_E2M1, true><<<grid, kRowThreads, 0, stream>>>(
-          xp, rows, cols, ld_x, qp, ld_q, sp, splits, G, seg_rows, status);
+          xp, rows, cols, ld_x, qp, ld_q, sp, splits, G, seg_rows, status, round_up);
     else
       mx_rowwise_packed_kernel<MXG_E2M1, false><<<grid, kRowThreads, 0, stream>>>(
-          xp, rows, cols, ld_x, qp, ld_q, sp, nullptr, G, seg_rows, status);
+          xp, rows, cols, ld_x, qp, ld_q, sp, nullptr, G, seg_rows, status, round_up);
   } else {
     if (splits)
       mx_rowwise_packed_kernel<MXG_E4M3, true><<<grid, kRowThreads, 0, stream>>>(
-          xp, rows, cols, ld_x, qp, ld_q, sp, splits, G, seg_rows, status);
+          xp, rows, cols, ld_x, qp, ld_q, sp, splits, G, seg_rows, status, round_up);
     else
       mx_rowwise_packed_kernel<MXG_E4M3, false><<<grid, kRowThreads, 0, stream>>>(
-          xp, rows, cols, ld_x, qp, ld_q, sp, nullptr, G, seg_rows, status);
+          xp, rows, cols, ld_x, qp, ld_q, sp, nullptr, G, seg_rows, status, round_up);
   }
   return cudaGetLastError();
 }
@@ -795,6 +806,8 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
                               int64_t* pad_offsets, int32_t* status, cudaStream_t stream,
                               int num_sms, void* q_row, int64_t ld_qr, uint8_t* s_row,
                               int64_t ld_sr) {
+  const bool round_up = (elem & MXG_SCALE_ROUND_UP) != 0;  // rule flag carried in elem
+  elem &= 0xFF;
   // persistent: at most kColCtasPerSm CTAs per SM, never more than the tiles
   const int64_t tiles = (capacity + kColTokens - 1) / kColTokens * ((cols + kColCols - 1) / kColCols);
   int64_t ctas = std::min<int64_t>(tiles, (int64_t)num_sms * kColCtasPerSm);
@@ -808,20 +821,20 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
     if (dual)
       mx_colwise_kernel<MXG_E2M1, true><<<grid, kColThreads, 0, stream>>>(
           xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, qr, ld_qr,
-          s_row, ld_sr);
+          s_row, ld_sr, round_up);
     else
       mx_colwise_kernel<MXG_E2M1, false><<<grid, kColThreads, 0, stream>>>(
           xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr,
-          0, nullptr, 0);
+          0, nullptr, 0, round_up);
   } else {
     if (dual)
       mx_colwise_kernel<MXG_E4M3, true><<<grid, kColThreads, 0, stream>>>(
           xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, qr, ld_qr,
-          s_row, ld_sr);
+          s_row, ld_sr, round_up);
     else
       mx_colwise_kernel<MXG_E4M3, false><<<grid, kColThreads, 0, stream>>>(
           xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr,
-          0, nullptr, 0);
+          0, nullptr, 0, round_up);
   }
   return cudaGetLastError();
 }
@@ -878,11 +891,11 @@ cudaError_t launch_bw_colwise(const void* x, int64_t rows, int64_t cols, int64_t
   if (pow2)
     mx_colwise_kernel<MXG_E4M3, false, 2><<<(unsigned)ctas, kColThreads, 0, stream>>>(
         xp, rows, cols, ld_x, splits, G, 128, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr, 0,
-        nullptr, 0);
+        nullptr, 0, false);
   else
     mx_colwise_kernel<MXG_E4M3, false, 1><<<(unsigned)ctas, kColThreads, 0, stream>>>(
         xp, rows, cols, ld_x, splits, G, 128, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr, 0,
-        nullptr, 0);
+        nullptr, 0, false);
   return cudaGetLastError();
 }
 

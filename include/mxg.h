@@ -70,6 +70,17 @@ typedef enum mxg_status {
 } mxg_status;
 
 typedef enum mxg_elem { MXG_E2M1 = 1, MXG_E4M3 = 2 } mxg_elem;
+/* Scale-rule flag, OR'ed into the elem argument of the MX quantizers
+ * (mx_quantize_rowwise, _rowwise_packed, _colwise_segment_padded,
+ * _dual_segment_padded).  Without it the shared exponent follows the OCP MX
+ * rule, e = floor(log2 amax) - emax.  With it, the TransformerEngine recipe
+ * described in the review "Clamp tiny block scales to preserve nonzero values"
+ * (ROCm TransformerEngine PR #745): e is the smallest integer with
+ * maxval * 2^e >= amax (maxval 448 for E4M3, 6 for E2M1), so no element
+ * saturates.  Both clamp e to [-127, 127] and give an all-zero block e = -127.
+ * Quantized operands carry no trace of the rule: GEMM operands take the plain
+ * MXG_E2M1 / MXG_E4M3. */
+#define MXG_SCALE_ROUND_UP 0x100
 typedef enum mxg_out_dtype { MXG_OUT_BF16 = 1, MXG_OUT_F32 = 2 } mxg_out_dtype;
 typedef enum mxg_pass { MXG_PASS_FWD = 0, MXG_PASS_DGRAD = 1, MXG_PASS_WGRAD = 2 } mxg_pass;
 /* Where an MX operand's scales are: row-major [rows, cols/32] bytes, or the

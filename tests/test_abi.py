@@ -77,6 +77,9 @@ def test_quantize_host_checks(lib):
     assert q(vp(FAKE), 4, 48, 64, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 2       # cols % 32
     assert q(vp(FAKE), 4, 64, 32, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 2       # ld_x < cols
     assert q(vp(FAKE), 4, 64, 64, 3, vp(FAKE), 32, vp(FAKE), 2, None) == 5       # bad elem
+    assert q(vp(FAKE), 4, 64, 64, 3 | 0x100, vp(FAKE), 32, vp(FAKE), 2, None) == 5  # bad elem with the rule flag
+    assert q(vp(FAKE), 4, 64, 64, 1 | 0x200, vp(FAKE), 32, vp(FAKE), 2, None) == 5  # unknown flag
+    assert q(vp(FAKE + 2), 4, 64, 64, 1 | 0x100, vp(FAKE), 32, vp(FAKE), 2, None) == 3  # flag accepted, x misaligned
     assert q(vp(FAKE + 2), 4, 64, 64, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 3   # x misaligned
     assert q(vp(FAKE), 4, 64, 68, 1, vp(FAKE), 32, vp(FAKE), 2, None) == 3       # ld_x % 8
     assert q(vp(FAKE), 4, 64, 64, 1, vp(FAKE + 4), 32, vp(FAKE), 2, None) == 3   # q not 16-B aligned
@@ -139,6 +142,7 @@ def test_gemm_host_checks(lib):
     assert call(A, W, ws_bytes=16) == 9                        # workspace too small
     assert call(_op(512, 512, 1), _op(1024, 512, 2)) == 5      # E2M1 x E4M3 not provided
     assert call(_op(512, 96, 2), _op(1024, 96, 1)) == 2        # a8w4 needs K % 128
+    assert call(_op(512, 512, 1 | 0x100), W) == 5                # the rule flag is not an operand format
     bad = _op(512, 512, 1); bad.scale_layout = 7
     assert call(bad, W) == 5                                   # unknown scale layout
     pk = _op(512, 512, 1); pk.scale_layout = 1; pk.scale = FAKE + 4
