@@ -24,7 +24,7 @@ __all__ = [
     "MXOperand", "MXGError", "mx_quantize_rowwise", "mx_quantize_colwise_segment_padded",
     "mx_quantize_rowwise_packed", "mx_packed_scale_bytes",
     "mx_quantize_dual_segment_padded",
-    "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "gemm_workspace_size",
+    "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "gemm_workspace_size", "mx_gemm_dense",
     "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns",
     "library_path", "BWOperand", "bw_quantize_1x128", "bw_quantize_128x128",
     "bw_quantize_colwise_padded", "bw_grouped_gemm_fwd", "bw_grouped_gemm_dgrad",
@@ -287,6 +287,27 @@ def grouped_gemm_fwd(A: MXOperand, W: MXOperand, m_splits: torch.Tensor, N: int,
     _ok(_lib.load().grouped_gemm_fwd(ctypes.byref(a), ctypes.byref(w), _ptr(m_splits), G, N,
                                      _ptr(out), _ld(out, N), _OUT[out.dtype], _ptr(ws),
                                      ws.numel(), _ptr(st), _stream(dev)), "grouped_gemm_fwd")
+    if check:
+        check_status(st)
+    return out
+
+
+def mx_gemm_dense(A: MXOperand, B: MXOperand, out_dtype=torch.bfloat16, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                  check: bool = False) -> torch.Tensor:
+    """C[M, N] = A[M, K] @ B[N, K]^T, both MX operands quantized along K (no
+    experts, no m_splits)."""
+    _need_cuda(A.data, B.data)
+    dev = A.data.device
+    N = B.rows
+    if out is None:
+        out = torch.empty((A.rows, N), dtype=out_dtype, device=dev)
+    need = gemm_workspace_size("fwd", 1, A.rows, N, A.cols)
+    ws = _workspace(need, dev, workspace)
+    st = status if status is not None else status_tensor(dev)
+    a, b = A.c(), B.c()
+    _ok(_lib.load().mx_gemm_dense(ctypes.byref(a), ctypes.byref(b), _ptr(out), _ld(out, N), _OUT[out.dtype],
+                                  _ptr(ws), ws.numel(), _ptr(st), _stream(dev)), "mx_gemm_dense")
     if check:
         check_status(st)
     return out

@@ -64,6 +64,9 @@ SIGNATURES = {
     "grouped_gemm_fwd": (
         c_i32, [ctypes.POINTER(MxOperandC), ctypes.POINTER(MxOperandC), c_vp, c_i32, c_i64, c_vp,
                 c_i64, c_i32, c_vp, c_size, c_vp, c_vp]),
+    "mx_gemm_dense": (
+        c_i32, [ctypes.POINTER(MxOperandC), ctypes.POINTER(MxOperandC), c_vp, c_i64, c_i32, c_vp, c_size, c_vp,
+                c_vp]),
     "grouped_gemm_dgrad": (
         c_i32, [ctypes.POINTER(MxOperandC), ctypes.POINTER(MxOperandC), c_vp, c_i32, c_vp, c_i64,
                 c_i32, c_vp, c_size, c_vp, c_vp]),

@@ -332,14 +332,18 @@ size_t mxg_gemm_workspace_size(int32_t pass, int32_t G, int64_t S, int64_t N, in
   return gemm_workspace_bytes(pass, G, S, N, K, pad_multiple);
 }
 
-mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
-                            const int32_t* d_m_splits, int32_t G, int64_t N, void* out,
-                            int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
-                            int32_t* d_status, void* stream) {
+}  // extern "C"
+
+namespace {
+// The forward pass; d_m_splits == NULL means one expert of all A->rows rows
+// (the dense entry point, G == 1).
+mxg_status fwd_impl(const mxg_mx_operand* A, const mxg_mx_operand* W, const int32_t* d_m_splits,
+                    int32_t G, int64_t N, void* out, int64_t ld_out, int32_t out_dtype, void* ws,
+                    size_t ws_bytes, int32_t* d_status, void* stream) {
   mxg_status st;
   if ((st = check_operand(A, false, true)) != MXG_OK || (st = check_operand(W, false, true)) != MXG_OK)
     return st;
-  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (d_status == nullptr) return MXG_ERR_NULL;
   if ((st = check_out(out, A->rows, ld_out, N, out_dtype)) != MXG_OK) return st;
   if (G < 1 || G > kMaxExperts || N <= 0 || N % 32 != 0) return MXG_ERR_SHAPE;
   if (W->rows == 0) return MXG_ERR_SHAPE;
@@ -377,6 +381,23 @@ mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
   a.out = out; a.ld_out = ld_out; a.out_dtype = out_dtype; a.accumulate = 0;
   a.ws = ws; a.ws_bytes = ws_bytes; a.status = d_status;
   return launch_grouped_gemm(a, static_cast<cudaStream_t>(stream), sms);
+}
+}  // namespace
+
+extern "C" {
+
+mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
+                            const int32_t* d_m_splits, int32_t G, int64_t N, void* out,
+                            int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
+                            int32_t* d_status, void* stream) {
+  if (d_m_splits == nullptr) return MXG_ERR_NULL;
+  return fwd_impl(A, W, d_m_splits, G, N, out, ld_out, out_dtype, ws, ws_bytes, d_status, stream);
+}
+
+mxg_status mx_gemm_dense(const mxg_mx_operand* A, const mxg_mx_operand* B, void* out, int64_t ld_out,
+                         int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* d_status, void* stream) {
+  if (B == nullptr) return MXG_ERR_NULL;
+  return fwd_impl(A, B, nullptr, 1, B->rows, out, ld_out, out_dtype, ws, ws_bytes, d_status, stream);
 }
 
 mxg_status grouped_gemm_dgrad(const mxg_mx_operand* dY, const mxg_mx_operand* Wt,

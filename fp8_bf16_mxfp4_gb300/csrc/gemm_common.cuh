@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int g = 2 * tid + i;
-    const int64_t m = g < G ? (int64_t)splits[g] : 0;
+    // no splits: one expert of all S rows (the dense entry point)
+    const int64_t m = g < G ? (splits ? (int64_t)splits[g] : p.S) : 0;
     neg |= m < 0;
     const int64_t mm = m > 0 ? m : 0;
     const int64_t pg = p.pass == MXG_PASS_WGRAD ? ((mm + p.pad - 1) / p.pad) * p.pad : 0;

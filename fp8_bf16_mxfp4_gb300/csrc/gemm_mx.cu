@@ -20,15 +20,17 @@
 //      32x128b.warpx4 expects: byte (r%32)*16 + (r/32)*4 + block), one chunk
 //      per (row tile, 128-element k chunk) with every expert's rows (or k
 //      range) starting on a fresh chunk -- the "scale packing" step that the
-//      HipKittens grouped MXFP8 kernel (PR #661) also performs.
+//      HipKittens grouped MXFP8 kernel (PR #661) also performs.  Skipped for
+//      an operand whose quantizer already wrote that order (packed scales).
 //   3. the persistent GEMM kernel, one CTA per SM, 320 threads:
 //        warp 0    TMA producer: A/B data tiles (128-byte swizzle) and scale
 //                  chunks into a 4-stage shared-memory ring (mbarriers);
 //        warp 1    TMEM owner and MMA issuer (one thread): 4 tcgen05.mma per
 //                  stage (kind::mxf4 for MXFP4, kind::mxf8f6f4 for MXFP8 /
 //                  a8w4) accumulating a 128x256 fp32 tile in TMEM;
-//        warps 2-5 epilogue: tcgen05.ld, fp32 -> BF16/FP32 (optionally +=),
-//                  row/column-masked stores of the expert's valid region;
+//        warps 2-5 epilogue: tcgen05.ld, fp32 -> BF16/FP32, staged through
+//                  shared memory and written by TMA tiled stores (bulk
+//                  reduce-adds for +=), only the expert's valid rows;
 //        warps 6-9 scale feeders, one per 32-lane quarter of TMEM: each
 //                  stage's scale chunks go from shared memory to registers
 //                  and on into that stage's TMEM scale slot (tcgen05.st),
@@ -37,8 +39,9 @@
 //      measured on GB300, a scale copy issued between MMAs (3 per FP8 stage,
 //      6 per FP4 stage) slowed the MMA stream by a third to two thirds, and
 //      more again when the issuer also waited on an mbarrier.
-//      Tiles (expert, m-tile, n-tile) are enumerated expert-major, n fastest,
-//      and strided over the CTAs.
+//      Tiles (expert, m-tile, n-tile) are enumerated expert-major and strided
+//      over the CTAs; inside an expert, m-tiles run in groups (tile_mn) so
+//      that a group's A rows stay in L2 while the n-tiles sweep over them.
 #include <cuda.h>
 #include <cuda_bf16.h>
 

@@ -231,6 +231,17 @@ mxg_status grouped_gemm_fwd(const mxg_mx_operand* A, const mxg_mx_operand* W,
                             int64_t ld_out, int32_t out_dtype, void* ws, size_t ws_bytes,
                             int32_t* d_status, void* stream);
 
+/* Dense (non-grouped) MX GEMM, C[M, N] = A[M, K] * B[N, K]^T with both
+ * operands K-major: the dense hipBLASLt MXFP4 GEMM of "Integrate MXFP4
+ * hipblaslt GEMM support" (PR #697; its forward TN, dgrad NN and wgrad NT are
+ * this call on operands quantized along the respective contraction).  It is
+ * grouped_gemm_fwd with one expert of all A->rows rows, and needs no device
+ * m_splits.  Operand pairs, output, workspace (mxg_gemm_workspace_size(
+ * MXG_PASS_FWD, 1, M, N, K, 32)) and packed scales (one segment) as for
+ * grouped_gemm_fwd; d_status receives device-side errors (a wait timeout). */
+mxg_status mx_gemm_dense(const mxg_mx_operand* A, const mxg_mx_operand* B, void* out, int64_t ld_out,
+                         int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* d_status, void* stream);
+
 /* dgrad (NN).  dY: rows = S, cols = N.  Wt: rows = K, cols = G*N -- W
  * transposed and quantized along N within each expert (mx_quantize_colwise_
  * segment_padded of W [G*N, K] with m_splits = {N, ..., N}, pad 32).

@@ -147,6 +147,16 @@ def test_gemm_host_checks(lib):
     assert call(bad, W) == 5                                   # unknown scale layout
     pk = _op(512, 512, 1); pk.scale_layout = 1; pk.scale = FAKE + 4
     assert call(pk, W) == 3                                    # packed scales not 16-byte aligned
+    dense = lib.mx_gemm_dense
+    assert dense(ctypes.byref(A), None, vp(FAKE), 256, 1, vp(FAKE), ws, vp(FAKE), None) == 1   # NULL B
+    assert dense(ctypes.byref(A), ctypes.byref(_op(256, 512, 1)), vp(FAKE), 256, 1, vp(FAKE), ws, None,
+                 None) == 1                                    # NULL status
+    assert dense(ctypes.byref(A), ctypes.byref(_op(256, 480, 1)), vp(FAKE), 256, 1, vp(FAKE), ws, vp(FAKE),
+                 None) == 2                                    # K mismatch
+    assert dense(ctypes.byref(A), ctypes.byref(_op(250, 512, 1)), vp(FAKE), 256, 1, vp(FAKE), ws, vp(FAKE),
+                 None) == 2                                    # N % 32
+    assert dense(ctypes.byref(A), ctypes.byref(_op(256, 512, 1)), vp(FAKE), 256, 1, vp(FAKE), 16, vp(FAKE),
+                 None) == 9                                    # workspace too small
     d = lib.grouped_gemm_dgrad
     dY, Wt = _op(512, 256, 2), _op(512, 4 * 256, 1)
     assert d(ctypes.byref(dY), ctypes.byref(Wt), vp(FAKE), 4, vp(FAKE), 512, 1, vp(FAKE), ws,

@@ -170,6 +170,37 @@ def test_wgrad_many_tiles_per_cta(kind, accumulate):
         assert np.array_equal(got[1], init[1])
 
 
+@pytest.mark.parametrize("kind", ["mxfp4", "mxfp8", "a8w4"])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_dense_gemm(kind, out_dtype):
+    """mx_gemm_dense (no experts, no m_splits) against the oracle, and equal bit
+    for bit to the one-expert grouped forward; also with packed scales."""
+    mxg = _mxg()
+    ea, eb = KINDS[kind]
+    M, N, K = 333, 320, 256
+    rng = np.random.default_rng(7)
+    x = synth.normal_bf16(rng, (M, K), outlier_frac=0.01)
+    w = synth.normal_bf16(rng, (N, K), outlier_frac=0.01)
+    A, Ad = oracle_operand_rowwise(x, ea)
+    B, Bd = oracle_operand_rowwise(w, eb)
+    C = mxg.mx_gemm_dense(A, B, out_dtype=out_dtype, check=True)
+    oracle.assert_gemm_close(C.float().cpu().numpy(), Ad @ Bd.T, f"dense {kind}")
+    Cg = mxg.grouped_gemm_fwd(A, B, i32_to_dev([M]), N, out_dtype=out_dtype, check=True)
+    assert torch.equal(C, Cg)
+    Ap = mxg.mx_quantize_rowwise_packed(bf16_to_dev(x), ea, groups=1)
+    Bp = mxg.mx_quantize_rowwise_packed(bf16_to_dev(w), eb, groups=1)
+    assert torch.equal(mxg.mx_gemm_dense(Ap, Bp, out_dtype=out_dtype, check=True), C)
+
+
+def test_dense_gemm_empty_rows():
+    mxg = _mxg()
+    B, _ = oracle_operand_rowwise(synth.normal_bf16(np.random.default_rng(1), (64, 128)), "e2m1")
+    A = mxg.MXOperand(torch.empty((0, 64), dtype=torch.uint8, device="cuda:0"),
+                      torch.empty((0, 4), dtype=torch.uint8, device="cuda:0"), "e2m1", 128)
+    C = mxg.mx_gemm_dense(A, B, check=True)
+    assert C.shape == (0, 64)
+
+
 def test_wgrad_bf16_output():
     splits = np.array([70, 33], dtype=np.int32)
     S, N, K = 103, 256, 256
