@@ -29,7 +29,7 @@ __all__ = [
     "library_path", "BWOperand", "bw_quantize_1x128", "bw_quantize_128x128",
     "bw_quantize_colwise_padded", "bw_grouped_gemm_fwd", "bw_grouped_gemm_dgrad",
     "bw_grouped_gemm_wgrad", "bw_quantize_1x128_pow2", "bw_quantize_128x128_pow2",
-    "bw_quantize_colwise_padded_pow2",
+    "bw_quantize_colwise_padded_pow2", "bw_quantize_dual_padded",
 ]
 
 ELEM = {"e2m1": 1, "e4m3": 2}
@@ -485,6 +485,42 @@ def bw_quantize_colwise_padded_pow2(x: torch.Tensor, m_splits: torch.Tensor, cap
     if check:
         check_status(st)
     return MXOperand(qT, sT, "e4m3", capacity), poff
+
+
+def bw_quantize_dual_padded(x: torch.Tensor, m_splits: torch.Tensor, capacity: int | None = None,
+                            pow2: bool = False, status: torch.Tensor | None = None, check: bool = False):
+    """One read of BF16 x [S, C] -> (row-wise 1x128 operand, column-wise
+    operand [C, capacity] with segments padded to 128, int64 padded offsets):
+    the same bytes as the separate row-wise and column-wise quantizers.  With
+    pow2 both are MXFP8 operands (UE8M0 power-of-two scales); otherwise
+    BWOperands with fp32 activation-type scales."""
+    _need_cuda(x, m_splits)
+    S, C = x.shape
+    G = m_splits.numel()
+    dev = x.device
+    if capacity is None:
+        capacity = mx_padded_rows_capacity(S, G, 128)
+    q = torch.empty((S, C), dtype=torch.uint8, device=dev)
+    qT = torch.empty((C, capacity), dtype=torch.uint8, device=dev)
+    if pow2:
+        s = torch.empty((S, C // 32), dtype=torch.uint8, device=dev)
+        sT = torch.empty((C, capacity // 32), dtype=torch.uint8, device=dev)
+        ld_s, ld_sT = _ld(s, C // 32), _ld(sT, capacity // 32)
+    else:
+        s = torch.empty((C // 128, S), dtype=torch.float32, device=dev)
+        sT = torch.empty((capacity // 128, C), dtype=torch.float32, device=dev)
+        ld_s, ld_sT = _ld(s, S), _ld(sT, C)
+    poff = torch.empty(G + 1, dtype=torch.int64, device=dev)
+    st = status if status is not None else status_tensor(dev)
+    fn = _lib.load().bw_quantize_dual_padded_pow2 if pow2 else _lib.load().bw_quantize_dual_padded
+    _ok(fn(_ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, _ptr(q), _ld(q, C), _ptr(s), ld_s, _ptr(qT),
+           _ld(qT, capacity), _ptr(sT), ld_sT, capacity, _ptr(poff), _ptr(st), _stream(dev)),
+        "bw_quantize_dual_padded")
+    if check:
+        check_status(st)
+    if pow2:
+        return MXOperand(q, s, "e4m3", C), MXOperand(qT, sT, "e4m3", capacity), poff
+    return BWOperand(q, s), BWOperand(qT, sT), poff
 
 
 def _bw_ws(G, device, ws):

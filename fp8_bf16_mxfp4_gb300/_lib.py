@@ -89,6 +89,12 @@ SIGNATURES = {
     "bw_quantize_colwise_padded_pow2": (
         c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_vp, c_i64, c_vp, c_i64, c_i64, c_vp, c_vp,
                 c_vp]),
+    "bw_quantize_dual_padded": (
+        c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp, c_i64, c_vp, c_i64,
+                c_i64, c_vp, c_vp, c_vp]),
+    "bw_quantize_dual_padded_pow2": (
+        c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp, c_i64, c_vp, c_i64,
+                c_i64, c_vp, c_vp, c_vp]),
     "bw_grouped_gemm_fwd": (
         c_i32, [ctypes.POINTER(BwOperandC), ctypes.POINTER(BwOperandC), c_vp, c_i32, c_i64, c_vp,
                 c_i64, c_i32, c_vp, c_size, c_vp, c_vp]),

@@ -614,6 +614,60 @@ mxg_status bw_quantize_colwise_padded_pow2(const void* x, int64_t rows, int64_t 
                                        static_cast<cudaStream_t>(stream), sms));
 }
 
+}  // extern "C"
+
+namespace {
+// Shared checks and launch of the dual blockwise quantizers (row-wise 1x128
+// and column-wise padded-to-128 from one read of x).
+mxg_status bw_dual(const void* x, int64_t rows, int64_t cols, int64_t ld_x, const int32_t* d_m_splits,
+                   int32_t G, void* q, int64_t ld_q, void* s, int64_t ld_s, void* qT, int64_t ld_qT, void* sT,
+                   int64_t ld_sT, int64_t capacity, int64_t* d_pad_offsets, int32_t* d_status, bool pow2,
+                   void* stream) {
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  if (rows < 0 || cols <= 0 || cols % 128 != 0 || capacity < 0 || capacity % 128 != 0) return MXG_ERR_SHAPE;
+  // row-wise scales: fp32 block-column-major (ld_s >= rows) or UE8M0 [rows, cols/32]
+  if (ld_x < cols || ld_q < cols || ld_qT < capacity || ld_s < (pow2 ? cols / 32 : rows) ||
+      ld_sT < (pow2 ? capacity / 32 : cols))
+    return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 8 != 0 || ld_qT % 16 != 0 || (pow2 && (ld_s % 4 != 0 || ld_sT % 4 != 0)))
+    return MXG_ERR_ALIGN;
+  if ((rows > 0 && (x == nullptr || q == nullptr || s == nullptr)) ||
+      (capacity > 0 && (qT == nullptr || sT == nullptr)))
+    return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned(q, 8) || !aligned(s, 4) || !aligned16(qT) || !aligned(sT, 4) ||
+      !aligned(d_pad_offsets, 8))
+    return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, d_m_splits, q, s, qT, sT, d_pad_offsets, d_status}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_bw_colwise(x, rows, cols, ld_x, d_m_splits, G, qT, ld_qT, sT, ld_sT, capacity,
+                                       d_pad_offsets, d_status, pow2, static_cast<cudaStream_t>(stream), sms,
+                                       rows > 0 ? q : nullptr, ld_q, s, ld_s));
+}
+}  // namespace
+
+extern "C" {
+
+mxg_status bw_quantize_dual_padded(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                   const int32_t* d_m_splits, int32_t G, void* q, int64_t ld_q, float* s,
+                                   int64_t ld_s, void* qT, int64_t ld_qT, float* sT, int64_t ld_sT,
+                                   int64_t capacity, int64_t* d_pad_offsets, int32_t* d_status, void* stream) {
+  return bw_dual(x, rows, cols, ld_x, d_m_splits, G, q, ld_q, s, ld_s, qT, ld_qT, sT, ld_sT, capacity,
+                 d_pad_offsets, d_status, false, stream);
+}
+
+mxg_status bw_quantize_dual_padded_pow2(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                        const int32_t* d_m_splits, int32_t G, void* q, int64_t ld_q,
+                                        uint8_t* s, int64_t ld_s, void* qT, int64_t ld_qT, uint8_t* sT,
+                                        int64_t ld_sT, int64_t capacity, int64_t* d_pad_offsets,
+                                        int32_t* d_status, void* stream) {
+  return bw_dual(x, rows, cols, ld_x, d_m_splits, G, q, ld_q, s, ld_s, qT, ld_qT, sT, ld_sT, capacity,
+                 d_pad_offsets, d_status, true, stream);
+}
+
 size_t bw_gemm_workspace_size(int32_t G) {
   if (G < 1 || G > kMaxExperts) return 0;
   return bw_gemm_workspace_bytes(G);

@@ -36,7 +36,9 @@ cudaError_t launch_bw_weight(const void* w, int64_t rows, int64_t K, int64_t ld_
 cudaError_t launch_bw_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                               const int32_t* splits, int G, void* qT, int64_t ld_q, void* sT,
                               int64_t ld_s, int64_t capacity, int64_t* pad_offsets,
-                              int32_t* status, bool pow2, cudaStream_t stream, int num_sms);
+                              int32_t* status, bool pow2, cudaStream_t stream, int num_sms,
+                              void* q_row = nullptr, int64_t ld_qr = 0, void* s_row = nullptr,
+                              int64_t ld_sr = 0);
 
 // Grouped MX GEMM (tcgen05 block-scaled).  See gemm_mx.cu.
 struct GemmArgs {

@@ -434,7 +434,12 @@ MXG_DEVINL void emit_bw_col(const uint32_t* w, uint32_t am, uint8_t* q, void* sT
 // kBw (blockwise FP8 column-wise operand, segments padded to 128, E4M3): a
 // tile is one 128-token block; the four lanes of a column pair reduce the
 // block's amax with two shuffles and each quantizes its 32 tokens (kBw 1:
-// fp32 scales, kBw 2: power-of-two scales as UE8M0, see emit_bw_col).
+// fp32 scales, kBw 2: power-of-two scales as UE8M0, see emit_bw_col).  With
+// kDual the same pass writes the 1x128 row-wise operand (the dual blockwise
+// quantizer of "Add ROCm Triton blockwise FP8 grouped GEMM"): each token row
+// of the tile is one 128-column block, taken by 16 lanes of a warp (one
+// 16-byte chunk each, amax over the 16 with four shuffles) so that the row's
+// 128 code bytes leave as one contiguous piece.
 constexpr int kColCtasPerSm = 2;
 
 template <int kElem, bool kDual, int kBw = 0>
@@ -445,7 +450,6 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
     int32_t* status, uint8_t* __restrict__ q_row, int64_t ld_qr, uint8_t* __restrict__ s_row,
     int64_t ld_sr, bool round_up) {
   static_assert(kColTokens == 128 && kColCols == 128 && kColThreads == 256, "thread mapping");
-  static_assert(!(kDual && kBw), "the dual pass is MX only");
   __shared__ SegTable tab;
   __shared__ __align__(16) uint32_t tile[kColTokens * (kColCols / 2) + 4 * 8];
   __shared__ int64_t src_row[2][kColTokens];  // source row of each position, or -1
@@ -542,7 +546,37 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
         if (col + 1 < cols) emit_bw_col<kBw>(wb, amb, qT + (col + 1) * ld_q + jb, sT, ld_s, col + 1, j0, blk == 0);
       }
     }
-    if constexpr (kDual) {
+    if constexpr (kDual && kBw != 0) {
+      // row-wise 1x128 blocks: warp w takes tile rows 16*it + 2w + (lane >> 4);
+      // lane & 15 is the row's 16-byte chunk (8 columns)
+      const int64_t c0 = (tile_id % ntc) * kColCols;  // cols % 128 == 0: the block is the whole tile row
+      const int sub = lane >> 4, ch = lane & 15, wid = threadIdx.x >> 5;
+#pragma unroll 2
+      for (int it = 0; it < kColTokens / 16; ++it) {
+        const int rr = 16 * it + 2 * wid + sub;
+        const int64_t sr = src_row[buf][rr];
+        const uint4 v4 = *reinterpret_cast<const uint4*>(tile + rr * 64 + (rr >> 5) * 8 + 4 * ch);
+        const uint32_t w[4] = {v4.x, v4.y, v4.z, v4.w};
+        uint32_t am = max(max(bf16x2_absmax_bits(w[0]), bf16x2_absmax_bits(w[1])),
+                          max(bf16x2_absmax_bits(w[2]), bf16x2_absmax_bits(w[3])));
+#pragma unroll
+        for (int d = 1; d < 16; d <<= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
+        if (sr >= 0) {
+          uint32_t o[2];
+          if constexpr (kBw == 2) {
+            const int k = bw_pow2_exponent(am);
+            bw_quantize8_mul(w, pow2_neg(k), o);
+            if (ch == 0) *reinterpret_cast<uint32_t*>(s_row + sr * ld_sr + c0 / 32) = ue8m0x4(k);
+          } else {
+            const float sc = bw_scale(am);
+            bw_quantize8(w, sc, o);
+            if (ch == 0) reinterpret_cast<float*>(s_row)[(c0 / 128) * ld_sr + sr] = sc;
+          }
+          *reinterpret_cast<uint2*>(q_row + sr * ld_qr + c0 + 8 * ch) = make_uint2(o[0], o[1]);
+        }
+      }
+    }
+    if constexpr (kDual && kBw == 0) {
       // row-wise blocks: thread -> token row tid/2, 32-blocks 2*(tid%2) and +1
       const int rr = threadIdx.x >> 1;
       const int64_t sr = src_row[buf][rr];
@@ -881,17 +915,29 @@ cudaError_t launch_bw_weight(const void* w, int64_t rows, int64_t K, int64_t ld_
 cudaError_t launch_bw_colwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                               const int32_t* splits, int G, void* qT, int64_t ld_q, void* sT,
                               int64_t ld_s, int64_t capacity, int64_t* pad_offsets,
-                              int32_t* status, bool pow2, cudaStream_t stream, int num_sms) {
+                              int32_t* status, bool pow2, cudaStream_t stream, int num_sms,
+                              void* q_row, int64_t ld_qr, void* s_row, int64_t ld_sr) {
   // the persistent column-wise kernel with one 128-token block per tile
   const int64_t tiles = (capacity + kColTokens - 1) / kColTokens * ((cols + kColCols - 1) / kColCols);
   int64_t ctas = std::min<int64_t>(tiles, (int64_t)num_sms * kColCtasPerSm);
   if (ctas < 1) ctas = 1;
   auto* xp = static_cast<const uint16_t*>(x);
   auto* qp = static_cast<uint8_t*>(qT);
-  if (pow2)
+  auto* qr = static_cast<uint8_t*>(q_row);
+  auto* sr = static_cast<uint8_t*>(s_row);
+  const bool dual = q_row != nullptr;
+  if (pow2 && dual)
+    mx_colwise_kernel<MXG_E4M3, true, 2><<<(unsigned)ctas, kColThreads, 0, stream>>>(
+        xp, rows, cols, ld_x, splits, G, 128, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, qr, ld_qr,
+        sr, ld_sr, false);
+  else if (pow2)
     mx_colwise_kernel<MXG_E4M3, false, 2><<<(unsigned)ctas, kColThreads, 0, stream>>>(
         xp, rows, cols, ld_x, splits, G, 128, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr, 0,
         nullptr, 0, false);
+  else if (dual)
+    mx_colwise_kernel<MXG_E4M3, true, 1><<<(unsigned)ctas, kColThreads, 0, stream>>>(
+        xp, rows, cols, ld_x, splits, G, 128, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, qr, ld_qr,
+        sr, ld_sr, false);
   else
     mx_colwise_kernel<MXG_E4M3, false, 1><<<(unsigned)ctas, kColThreads, 0, stream>>>(
         xp, rows, cols, ld_x, splits, G, 128, qp, ld_q, sT, ld_s, capacity, pad_offsets, status, nullptr, 0,

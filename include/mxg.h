@@ -384,6 +384,30 @@ mxg_status bw_quantize_colwise_padded_pow2(const void* x, int64_t rows, int64_t 
                                            int64_t capacity, int64_t* d_pad_offsets,
                                            int32_t* d_status, void* stream);
 
+/* Dual blockwise quantization: one read of x [rows, cols] (experts' rows
+ * concatenated) writes both activation operands of a training step -- the
+ * 1x128 row-wise one (as bw_quantize_1x128 / _pow2) and the column-wise one
+ * with every expert's segment padded to 128 (as bw_quantize_colwise_padded /
+ * _pow2) -- the fused dual quantizer of "Add ROCm Triton blockwise FP8 grouped
+ * GEMM" (PR #716).  Bytes and scales equal those of the two separate calls.
+ *   q, ld_q (% 8), s, ld_s : row-wise codes [rows, cols] and scales (fp32
+ *                            block-column-major with ld_s >= rows, or UE8M0
+ *                            [rows, cols/32] with ld_s % 4 == 0)
+ *   qT, ld_qT (% 16), sT, ld_sT : column-wise codes [cols, capacity] and scales
+ *                            (fp32 (c, jb) at sT[jb * ld_sT + c], ld_sT >= cols;
+ *                            or UE8M0 [cols, capacity/32], ld_sT % 4 == 0)
+ * cols % 128 == 0, capacity % 128 == 0.  Device errors as for
+ * mx_quantize_colwise_segment_padded; on an error nothing is written. */
+mxg_status bw_quantize_dual_padded(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                   const int32_t* d_m_splits, int32_t G, void* q, int64_t ld_q, float* s,
+                                   int64_t ld_s, void* qT, int64_t ld_qT, float* sT, int64_t ld_sT,
+                                   int64_t capacity, int64_t* d_pad_offsets, int32_t* d_status, void* stream);
+mxg_status bw_quantize_dual_padded_pow2(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                        const int32_t* d_m_splits, int32_t G, void* q, int64_t ld_q,
+                                        uint8_t* s, int64_t ld_s, void* qT, int64_t ld_qT, uint8_t* sT,
+                                        int64_t ld_sT, int64_t capacity, int64_t* d_pad_offsets,
+                                        int32_t* d_status, void* stream);
+
 /* Grouped blockwise-FP8 GEMMs (tcgen05 kind::f8f6f4 + per-128-K promotion in
  * fp32).  Same passes, split validation and output conventions as the MX
  * GEMMs; N and K multiples of 128; the wgrad padding is 128.

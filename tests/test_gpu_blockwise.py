@@ -273,3 +273,51 @@ def test_pow2_blockwise_step_on_the_mx_gemms():
     mxg.grouped_gemm_wgrad(full(dytc, dyts, N), full(xtc, xts, K), d_splits, S, 128, out=out, check=True)
     ref = oracle.grouped_wgrad(oracle.dequantize_bw_1x128(dytc, dyts), oracle.dequantize_bw_1x128(xtc, xts), poff)
     oracle.assert_gemm_close(out.cpu().numpy(), ref, "pow2 wgrad")
+
+
+# ------------------------------------------------------------------ dual blockwise quantizer
+
+@pytest.mark.parametrize("pow2", [False, True])
+@pytest.mark.parametrize("splits,cols", [([200, 0, 1, 128, 55], 128), ([0, 0, 300], 256),
+                                         ([1000, 7, 0, 450], 512)])
+def test_bw_dual_matches_both_oracles(pow2, splits, cols):
+    """One read of x: the 1x128 row-wise and the padded column-wise operands,
+    each bit-exact against its own oracle (codes and scales), with a block
+    below the amax floor, an all-zero block and an exact-fit block."""
+    rng = np.random.default_rng(len(splits) + cols + pow2)
+    splits = np.array(splits, dtype=np.int32)
+    S = int(splits.sum())
+    x = synth.normal_bf16(rng, (S, cols), std=3.0, outlier_frac=0.02)
+    if S > 4:
+        v = synth.bf16_bits_to_f32(x)
+        x[1] = synth.f32_to_bf16_bits(v[1] * np.float32(1e-7))
+        x[2, :128] = 0
+        x[3, :128] = synth.f32_to_bf16_bits(np.full(128, -448.0, np.float32))
+    row, col, poff = _mxg().bw_quantize_dual_padded(bf16_to_dev(x), i32_to_dev(splits), pow2=pow2, check=True)
+    rc, rs = oracle.quantize_bw_1x128(x, pow2=pow2)
+    assert np.array_equal(row.data.cpu().numpy(), rc)
+    assert np.array_equal(row.scale.cpu().numpy(), _ue8m0(rs) if pow2 else rs.T)
+    cc, cs, p = oracle.quantize_bw_colwise_padded(x, splits, pow2=pow2)
+    spad = int(p[-1])
+    assert np.array_equal(poff.cpu().numpy(), p)
+    assert np.array_equal(col.data.cpu().numpy()[:, :spad], cc)
+    if pow2:
+        assert np.array_equal(col.scale.cpu().numpy()[:, : spad // 32], _ue8m0(cs))
+    else:
+        assert np.array_equal(col.scale.cpu().numpy()[: spad // 128], cs.T)
+
+
+def test_bw_dual_rejects_bad_splits_and_writes_nothing():
+    mxg = _mxg()
+    x = bf16_to_dev(synth.normal_bf16(np.random.default_rng(2), (14, 128)))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    q = torch.full((14, 128), 0xAB, dtype=torch.uint8, device="cuda:0")
+    s = torch.full((14, 4), 0xCD, dtype=torch.uint8, device="cuda:0")
+    qT = torch.full((128, 384), 0xAB, dtype=torch.uint8, device="cuda:0")
+    sT = torch.full((128, 12), 0xCD, dtype=torch.uint8, device="cuda:0")
+    rc = mxg._lib.load().bw_quantize_dual_padded_pow2(
+        mxg._ptr(x), 14, 128, 128, mxg._ptr(i32_to_dev([10, -1, 5])), 3, mxg._ptr(q), 128, mxg._ptr(s), 4,
+        mxg._ptr(qT), 384, mxg._ptr(sT), 12, 384, None, mxg._ptr(st), mxg._stream(x.device))
+    assert rc == 0
+    assert int(st.item()) == 4
+    assert (q == 0xAB).all() and (s == 0xCD).all() and (qT == 0xAB).all() and (sT == 0xCD).all()
