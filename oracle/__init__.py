@@ -60,6 +60,9 @@ from .packed import (  # noqa: F401
     packed_scale_bytes,
     pack_scales_mma,
     pack_scales_mma_by_tiles,
+    kseg_chunk_prefix,
+    pack_scales_mma_kseg,
+    pack_scales_mma_kseg_by_experts,
 )
 from .gemm import (  # noqa: F401
     check_splits,

@@ -24,6 +24,11 @@ for forward weights):
   (i % 32)*16 + (i // 32)*4 + j;
 * every byte not covered by a row or block of the operand is zero.
 
+Column-wise (k-segmented) operands -- the dgrad weights and both wgrad
+operands, whose contraction is cut into the experts' padded segments -- use
+the same chunks with the chunk grid restarting at every segment
+(``pack_scales_mma_kseg``).
+
 Parity: ``pack_scales_mma`` (a scatter, one index formula per scale) is pinned
 on the CPU against ``pack_scales_mma_by_tiles`` (each chunk built as a
 reshaped and transposed 128 x 4 tile) and by invariants; its reading by the
@@ -105,3 +110,57 @@ def pack_scales_mma_by_tiles(scale: np.ndarray, seg_rows) -> np.ndarray:
             sl = tile[:, kc * CHUNK_BLOCKS:(kc + 1) * CHUNK_BLOCKS]     # [128 rows, 4 blocks]
             out[kc, rt] = sl.reshape(4, 32, CHUNK_BLOCKS).transpose(1, 0, 2).ravel()
     return out.ravel()
+
+
+def kseg_chunk_prefix(pad_offsets) -> np.ndarray:
+    """[G+1] exclusive prefix of ceil(p_g / 128) for padded segment lengths
+    p_g = poff[g+1] - poff[g]: the first k-chunk of each expert; entry G is
+    the operand's k-chunk count."""
+    poff = np.asarray(pad_offsets, dtype=np.int64)
+    chunks = (np.diff(poff) + TILE_ROWS - 1) // TILE_ROWS
+    return np.concatenate([[0], np.cumsum(chunks)]).astype(np.int64)
+
+
+def pack_scales_mma_kseg(scale: np.ndarray, pad_offsets) -> np.ndarray:
+    """Scales of a column-wise (k-segmented) operand -> packed bytes.
+
+    The operand has C rows (channels) and a contraction cut into the experts'
+    padded segments [poff_g, poff_{g+1}) (multiples of 32); ``scale`` is its
+    plain [C, poff_G / 32] byte array.  The chunk grid restarts at every
+    segment: expert g's k-chunks are kseg_chunk_prefix[g] + c, c over
+    ceil(p_g / 128) chunks of 4 blocks counted from poff_g; rows are cut into
+    128-row tiles (RT = ceil(C / 128)).  Chunk (kc, rt) at (kc*RT + rt)*512,
+    channel i of the tile and block j of the chunk at (i%32)*16 + (i//32)*4 + j,
+    zero where no channel or block exists (the layout the grouped GEMM reads
+    for the dgrad weights and both wgrad operands)."""
+    scale = np.asarray(scale, dtype=np.uint8)
+    C = scale.shape[0]
+    poff = np.asarray(pad_offsets, dtype=np.int64)
+    kcp = kseg_chunk_prefix(poff)
+    RT = (C + TILE_ROWS - 1) // TILE_ROWS
+    out = np.zeros(int(kcp[-1] * RT * CHUNK_BYTES), dtype=np.uint8)
+    ch = np.arange(C, dtype=np.int64)
+    rt, i = ch // TILE_ROWS, ch % TILE_ROWS
+    row_off = (i % 32) * 16 + (i // 32) * 4
+    for g in range(poff.shape[0] - 1):
+        nb = int((poff[g + 1] - poff[g]) // 32)
+        for lb in range(nb):                      # local 32-block of the expert
+            kc = kcp[g] + lb // CHUNK_BLOCKS
+            pos = (kc * RT + rt) * CHUNK_BYTES + row_off + lb % CHUNK_BLOCKS
+            out[pos] = scale[:, poff[g] // 32 + lb]
+    return out
+
+
+def pack_scales_mma_kseg_by_experts(scale: np.ndarray, pad_offsets) -> np.ndarray:
+    """Second formulation of ``pack_scales_mma_kseg``: each expert's slice
+    [C, p_g / 32] is a row-wise operand of one segment of C rows; its packed
+    chunk planes (``pack_scales_mma``) are concatenated in expert order."""
+    scale = np.asarray(scale, dtype=np.uint8)
+    C = scale.shape[0]
+    poff = np.asarray(pad_offsets, dtype=np.int64)
+    parts = []
+    for g in range(poff.shape[0] - 1):
+        sl = scale[:, poff[g] // 32: poff[g + 1] // 32]
+        if sl.shape[1]:
+            parts.append(pack_scales_mma(sl, [C]))
+    return np.concatenate(parts) if parts else np.zeros(0, dtype=np.uint8)

@@ -68,3 +68,50 @@ def test_uniform_segments_equal_plain_row_tiles():
             for lane in (0, 17, 31):
                 for qtr in range(4):
                     assert np.array_equal(p[kc, rt, lane, qtr], rows[qtr * 32 + lane])
+
+
+# ------------------------------------------------------------------ column-wise (k-segmented) operands
+
+KSEG = [[0, 32], [0, 128], [0, 160], [0, 0, 64, 64, 320], [0, 32, 32, 288], [0, 512, 544]]
+
+
+@pytest.mark.parametrize("poff", KSEG)
+@pytest.mark.parametrize("C", [1, 128, 130, 300])
+def test_kseg_two_formulations_agree(poff, C):
+    rng = np.random.default_rng(C + poff[-1])
+    s = rng.integers(0, 256, size=(C, poff[-1] // 32), dtype=np.uint8)
+    a = oracle.pack_scales_mma_kseg(s, poff)
+    b = oracle.pack_scales_mma_kseg_by_experts(s, poff)
+    assert np.array_equal(a, b)
+    assert a.size == oracle.kseg_chunk_prefix(poff)[-1] * ((C + 127) // 128) * 512
+
+
+def test_kseg_hand_worked_positions():
+    # two experts of 160 and 32 padded positions, 130 channels: expert 0 has chunks 0 (blocks 0-3)
+    # and 1 (block 4), expert 1 chunk 2 (block 0); RT = 2 (channels 0-127, 128-129)
+    poff, C = [0, 160, 192], 130
+    s = np.zeros((C, 6), dtype=np.uint8)
+    s[0, 0] = 11       # kc 0, rt 0, lane 0, quarter 0, j 0          -> byte 0
+    s[33, 3] = 22      # kc 0, rt 0, channel 33 -> lane 1, quarter 1, j 3 -> 16 + 4 + 3 = 23
+    s[0, 4] = 33       # expert 0 block 4 -> kc 1, j 0: (1*2 + 0)*512 = 1024
+    s[129, 5] = 44     # expert 1 block 0 -> kc 2, rt 1, channel 1: (2*2 + 1)*512 + 16 = 2576
+    p = oracle.pack_scales_mma_kseg(s, poff)
+    assert p.size == 3 * 2 * 512
+    for pos, v in {0: 11, 23: 22, 1024: 33, 2576: 44}.items():
+        assert p[pos] == v, pos
+    assert np.count_nonzero(p) == 4
+
+
+def test_kseg_uniform_segments_match_the_dgrad_weight_chunks():
+    # dgrad weights: G segments of N (N % 128 == 0) -> k-chunk g*N/128 + c, exactly the plain 128-column chunks
+    G, N, C = 3, 256, 256
+    rng = np.random.default_rng(4)
+    s = rng.integers(1, 256, size=(C, G * N // 32), dtype=np.uint8)
+    poff = np.arange(G + 1) * N
+    p = oracle.pack_scales_mma_kseg(s, poff).reshape(G * N // 128, 2, 32, 4, 4)   # kc, rt, lane, quarter, j
+    for kc in (0, 3, 5):
+        for rt in (0, 1):
+            blk = s[rt * 128:(rt + 1) * 128, kc * 4:(kc + 1) * 4]
+            for lane in (0, 9, 31):
+                for q in range(4):
+                    assert np.array_equal(p[kc, rt, lane, q], blk[q * 32 + lane])
