@@ -261,6 +261,7 @@ class A8W4Forward:
 class MXFP4Train:
     """MXFP4 MoE training step of one expert layer: fwd, dgrad, variable-K wgrad."""
     name = "mxfp4_moe_train"
+    call_kernels = "plan + tcgen05 GEMM; scales arrive packed"
     elem = "e2m1"
 
     def __init__(self, dev):
@@ -292,8 +293,8 @@ class MXFP4Train:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         f = 2.0 * S * N * K
         self.flops = 3 * f
-        # six quantizers; fwd: plan + GEMM (both operands packed); dgrad, wgrad: plan + pack + GEMM
-        self.launches_per_step = 6 + 2 + 3 + 3
+        # six quantizers, all writing staging-order scales; three GEMM calls of plan + GEMM
+        self.launches_per_step = 6 + 3 * 2
         self.timed = _Timed()
         self.gemm_info = {p: (f, FP4_OVER_BF16, "mxf4") for p in ("fwd", "dgrad", "wgrad")}
 
@@ -305,13 +306,13 @@ class MXFP4Train:
                                                            workspace=self.ws, status=self.status), time_gemm)
         dYq = mxg.mx_quantize_rowwise_packed(self.dy, self.elem, m_splits=self.d_splits, status=self.status)
         Wt, _ = mxg.mx_quantize_colwise_segment_padded(self.w, self.w_splits, 32, self.elem,
-                                                       capacity=G * N, status=self.status)
+                                                       capacity=G * N, status=self.status, packed=True)
         self.timed.run("dgrad", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx,
                                                                workspace=self.ws, status=self.status), time_gemm)
         dYt, _ = mxg.mx_quantize_colwise_segment_padded(self.dy, self.d_splits, pad, self.elem,
-                                                        capacity=self.cap, status=self.status)
+                                                        capacity=self.cap, status=self.status, packed=True)
         Xt, _ = mxg.mx_quantize_colwise_segment_padded(self.x, self.d_splits, pad, self.elem,
-                                                       capacity=self.cap, status=self.status)
+                                                       capacity=self.cap, status=self.status, packed=True)
         self.timed.run("wgrad", lambda: mxg.grouped_gemm_wgrad(dYt, Xt, self.d_splits, self.S, pad,
                                                                out=self.main_grad, accumulate=True,
                                                                workspace=self.ws, status=self.status), time_gemm)
@@ -344,6 +345,7 @@ class DenseMXFP4:
     seqlen 2048 x mbs 4 = 8192 tokens, hidden 8192, FFN 28672; fwd and dgrad
     BF16 out, wgrad FP32 out (no accumulate)."""
     name = "dense_mxfp4_m8192"
+    call_kernels = "plan + tcgen05 GEMM; scales arrive packed"
 
     def __init__(self, dev):
         import torch
@@ -374,8 +376,8 @@ class DenseMXFP4:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         f = 2.0 * S * N * K
         self.flops = 3 * f
-        # six quantizers; fwd: plan + GEMM (both operands packed); dgrad, wgrad: plan + pack + GEMM
-        self.launches_per_step = 6 + 2 + 3 + 3
+        # six quantizers, all writing staging-order scales; three GEMM calls of plan + GEMM
+        self.launches_per_step = 6 + 3 * 2
         self.timed = _Timed()
         self.gemm_info = {p: (f, FP4_OVER_BF16, "mxf4") for p in ("fwd", "dgrad", "wgrad")}
 
@@ -387,13 +389,13 @@ class DenseMXFP4:
                                                            workspace=self.ws, status=self.status), time_gemm)
         dYq = mxg.mx_quantize_rowwise_packed(self.dy, "e2m1", m_splits=self.d_splits, status=self.status)
         Wt, _ = mxg.mx_quantize_colwise_segment_padded(self.w, self.w_splits, 32, "e2m1",
-                                                       capacity=N, status=self.status)
+                                                       capacity=N, status=self.status, packed=True)
         self.timed.run("dgrad", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx,
                                                                workspace=self.ws, status=self.status), time_gemm)
         dYt, _ = mxg.mx_quantize_colwise_segment_padded(self.dy, self.d_splits, pad, "e2m1",
-                                                        capacity=self.cap, status=self.status)
+                                                        capacity=self.cap, status=self.status, packed=True)
         Xt, _ = mxg.mx_quantize_colwise_segment_padded(self.x, self.d_splits, pad, "e2m1",
-                                                       capacity=self.cap, status=self.status)
+                                                       capacity=self.cap, status=self.status, packed=True)
         self.timed.run("wgrad", lambda: mxg.grouped_gemm_wgrad(dYt, Xt, self.d_splits, self.S, pad,
                                                                out=self.dw, accumulate=False,
                                                                workspace=self.ws, status=self.status), time_gemm)

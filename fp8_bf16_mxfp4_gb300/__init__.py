@@ -22,7 +22,7 @@ from . import _lib
 
 __all__ = [
     "MXOperand", "MXGError", "mx_quantize_rowwise", "mx_quantize_colwise_segment_padded",
-    "mx_quantize_rowwise_packed", "mx_packed_scale_bytes",
+    "mx_quantize_rowwise_packed", "mx_packed_scale_bytes", "mx_packed_colwise_scale_bytes",
     "mx_quantize_dual_segment_padded",
     "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "gemm_workspace_size", "mx_gemm_dense",
     "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns",
@@ -165,6 +165,12 @@ def mx_packed_scale_bytes(rows: int, cols: int, G: int) -> int:
     return int(_lib.load().mx_packed_scale_bytes(rows, cols, G))
 
 
+def mx_packed_colwise_scale_bytes(cols: int, capacity: int, G: int) -> int:
+    """Bytes of packed scales of a column-wise operand with `cols` channels and
+    `capacity` padded positions over G experts (an upper bound over splits)."""
+    return int(_lib.load().mx_packed_colwise_scale_bytes(cols, capacity, G))
+
+
 def mx_quantize_rowwise_packed(x: torch.Tensor, elem: str, m_splits: torch.Tensor | None = None,
                                groups: int | None = None, status: torch.Tensor | None = None,
                                check: bool = False, rule: str = "ocp") -> MXOperand:
@@ -201,20 +207,34 @@ def mx_quantize_rowwise_packed(x: torch.Tensor, elem: str, m_splits: torch.Tenso
 def mx_quantize_colwise_segment_padded(x: torch.Tensor, m_splits: torch.Tensor, pad_multiple: int,
                                        elem: str, capacity: int | None = None,
                                        status: torch.Tensor | None = None, check: bool = False,
-                                       rule: str = "ocp"):
+                                       rule: str = "ocp", packed: bool = False):
     """BF16 [S, C] with experts' rows concatenated -> (operand [C, capacity],
     int64 padded offsets [G+1]).  Columns beyond the last expert's padded end
-    are left uninitialised."""
+    are left uninitialised.  With ``packed`` the scales are written in the
+    grouped GEMM's staging order (a flat uint8 tensor; the GEMM call must use
+    the same splits and pad)."""
     _need_cuda(x, m_splits)
     S, C = x.shape
     G = m_splits.numel()
     if capacity is None:
         capacity = mx_padded_rows_capacity(S, G, pad_multiple)
     qT = torch.empty((C, _codes_cols(elem, capacity)), dtype=torch.uint8, device=x.device)
-    sT = torch.empty((C, capacity // 32), dtype=torch.uint8, device=x.device)
     poff = torch.empty(G + 1, dtype=torch.int64, device=x.device)
     st = status if status is not None else status_tensor(x.device)
     lib = _lib.load()
+    if packed:
+        nbytes = mx_packed_colwise_scale_bytes(C, capacity, G)
+        if nbytes < 0:
+            raise ValueError("invalid shape for packed scales")
+        sp = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=x.device)
+        _ok(lib.mx_quantize_colwise_segment_padded_packed(
+            _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, pad_multiple, _quant_elem(elem, rule), _ptr(qT),
+            _ld(qT, _codes_cols(elem, capacity)), _ptr(sp), sp.numel(), capacity, _ptr(poff), _ptr(st),
+            _stream(x.device)), "mx_quantize_colwise_segment_padded_packed")
+        if check:
+            check_status(st)
+        return MXOperand(qT, sp, elem, capacity, "packed"), poff
+    sT = torch.empty((C, capacity // 32), dtype=torch.uint8, device=x.device)
     _ok(lib.mx_quantize_colwise_segment_padded(
         _ptr(x), S, C, _ld(x, C), _ptr(m_splits), G, pad_multiple, _quant_elem(elem, rule), _ptr(qT),
         _ld(qT, _codes_cols(elem, capacity)), _ptr(sT), _ld(sT, capacity // 32), capacity,

@@ -59,6 +59,10 @@ SIGNATURES = {
                 c_vp, c_i64, c_vp, c_i64, c_i64, c_vp, c_vp, c_vp]),
     "mx_padded_rows_capacity": (c_i64, [c_i64, c_i32, c_i32]),
     "mx_packed_scale_bytes": (c_i64, [c_i64, c_i64, c_i32]),
+    "mx_packed_colwise_scale_bytes": (c_i64, [c_i64, c_i64, c_i32]),
+    "mx_quantize_colwise_segment_padded_packed": (
+        c_i32, [c_vp, c_i64, c_i64, c_i64, c_vp, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp, c_i64, c_i64, c_vp, c_vp,
+                c_vp]),
     "mx_quantize_rowwise_packed": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp,
                                            c_i32, c_vp, c_vp]),
     "grouped_gemm_fwd": (

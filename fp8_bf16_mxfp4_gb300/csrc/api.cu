@@ -260,6 +260,39 @@ mxg_status mx_quantize_rowwise_packed(const void* x, int64_t rows, int64_t cols,
                                               static_cast<cudaStream_t>(stream), sms));
 }
 
+int64_t mx_packed_colwise_scale_bytes(int64_t cols, int64_t capacity, int32_t G) {
+  if (cols < 0 || capacity < 0 || cols % 32 != 0 || capacity % 32 != 0 || G < 1 || G > kMaxExperts) return -1;
+  return (capacity / 128 + G) * ((cols + 127) / 128) * 512;
+}
+
+mxg_status mx_quantize_colwise_segment_padded_packed(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                                     const int32_t* d_m_splits, int32_t G, int32_t pad_multiple,
+                                                     int32_t elem, void* qT, int64_t ld_q, uint8_t* s_packed,
+                                                     int64_t s_bytes, int64_t capacity, int64_t* d_pad_offsets,
+                                                     int32_t* d_status, void* stream) {
+  if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
+  if (!valid_quant_elem(elem)) return MXG_ERR_UNSUPPORTED;
+  if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
+  if (pad_multiple <= 0 || pad_multiple % 32 != 0) return MXG_ERR_SHAPE;
+  if (rows < 0 || cols <= 0 || cols % 32 != 0 || capacity < 0 || capacity % 32 != 0) return MXG_ERR_SHAPE;
+  if (ld_x < cols || ld_q < code_bytes(elem & ~MXG_SCALE_ROUND_UP, capacity)) return MXG_ERR_SHAPE;
+  if (ld_x % 8 != 0 || ld_q % 16 != 0) return MXG_ERR_ALIGN;
+  const int64_t need = mx_packed_colwise_scale_bytes(cols, capacity, G);
+  if (s_bytes < need) return MXG_ERR_SHAPE;
+  if ((rows > 0 && x == nullptr) || (capacity > 0 && qT == nullptr) || (need > 0 && s_packed == nullptr))
+    return MXG_ERR_NULL;
+  if (!aligned16(x) || !aligned16(qT) || !aligned16(s_packed) || !aligned(d_pad_offsets, 8)) return MXG_ERR_ALIGN;
+  int dev = 0, sms = 0;
+  mxg_status st = check_device({x, d_m_splits, qT, s_packed, d_pad_offsets, d_status}, &dev, &sms);
+  if (st != MXG_OK) return st;
+  DeviceGuard g(dev);
+  if (!g.ok) return MXG_ERR_CUDA;
+  return cuda_status(launch_mx_colwise(x, rows, cols, ld_x, d_m_splits, G, pad_multiple, elem, qT, ld_q,
+                                       s_packed, 0, capacity, d_pad_offsets, d_status,
+                                       static_cast<cudaStream_t>(stream), sms, nullptr, 0, nullptr, 0,
+                                       need > 0 ? need : 0));
+}
+
 mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64_t cols,
                                               int64_t ld_x, const int32_t* d_m_splits,
                                               int32_t G, int32_t pad_multiple, int32_t elem,
@@ -405,7 +438,8 @@ mxg_status grouped_gemm_dgrad(const mxg_mx_operand* dY, const mxg_mx_operand* Wt
                               int32_t out_dtype, void* ws, size_t ws_bytes, int32_t* d_status,
                               void* stream) {
   mxg_status st;
-  if ((st = check_operand(dY, false, true)) != MXG_OK || (st = check_operand(Wt)) != MXG_OK) return st;
+  if ((st = check_operand(dY, false, true)) != MXG_OK || (st = check_operand(Wt, false, true)) != MXG_OK)
+    return st;
   if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
   if (G < 1 || G > kMaxExperts) return MXG_ERR_SHAPE;
   const int64_t N = dY->cols, K = Wt->rows;
@@ -431,6 +465,7 @@ mxg_status grouped_gemm_dgrad(const mxg_mx_operand* dY, const mxg_mx_operand* Wt
   a.b_scale = Wt->scale; a.b_scale_ld = Wt->scale_ld;
   a.b_rows = Wt->rows; a.b_cols = Wt->cols; a.b_elem = Wt->elem;
   a.a_packed = dY->scale_layout == MXG_SCALE_PACKED;
+  a.b_packed = Wt->scale_layout == MXG_SCALE_PACKED;
   a.splits = d_m_splits;
   a.total_rows = dY->rows;
   a.N = N; a.K = K;
@@ -446,7 +481,8 @@ mxg_status grouped_gemm_wgrad(const mxg_mx_operand* dYt, const mxg_mx_operand* X
                               int32_t accumulate, void* ws, size_t ws_bytes, int32_t* d_status,
                               void* stream) {
   mxg_status st;
-  if ((st = check_operand(dYt, true)) != MXG_OK || (st = check_operand(Xt, true)) != MXG_OK) return st;
+  if ((st = check_operand(dYt, true, true)) != MXG_OK || (st = check_operand(Xt, true, true)) != MXG_OK)
+    return st;
   if (d_m_splits == nullptr || d_status == nullptr) return MXG_ERR_NULL;
   if (G < 1 || G > kMaxExperts || total_rows < 0) return MXG_ERR_SHAPE;
   if (pad_multiple <= 0 || pad_multiple % 32 != 0) return MXG_ERR_SHAPE;
@@ -473,6 +509,8 @@ mxg_status grouped_gemm_wgrad(const mxg_mx_operand* dYt, const mxg_mx_operand* X
   a.b_data = static_cast<const uint8_t*>(Xt->data); a.b_ld = Xt->ld;
   a.b_scale = Xt->scale; a.b_scale_ld = Xt->scale_ld;
   a.b_rows = Xt->rows; a.b_cols = Xt->cols; a.b_elem = Xt->elem;
+  a.a_packed = dYt->scale_layout == MXG_SCALE_PACKED;
+  a.b_packed = Xt->scale_layout == MXG_SCALE_PACKED;
   a.splits = d_m_splits;
   a.total_rows = total_rows;
   a.N = N; a.K = K;

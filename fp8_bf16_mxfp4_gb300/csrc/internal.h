@@ -25,7 +25,7 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
                               int64_t ld_q, uint8_t* sT, int64_t ld_s, int64_t capacity,
                               int64_t* pad_offsets, int32_t* status, cudaStream_t stream,
                               int num_sms, void* q_row = nullptr, int64_t ld_qr = 0,
-                              uint8_t* s_row = nullptr, int64_t ld_sr = 0);
+                              uint8_t* s_row = nullptr, int64_t ld_sr = 0, int64_t packed_bytes = 0);
 
 cudaError_t launch_bw_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, void* q,
                               int64_t ld_q, void* s, int64_t ld_s, bool pow2, cudaStream_t stream,

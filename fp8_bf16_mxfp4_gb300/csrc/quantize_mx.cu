@@ -442,7 +442,12 @@ MXG_DEVINL void emit_bw_col(const uint32_t* w, uint32_t am, uint8_t* q, void* sT
 // 128 code bytes leave as one contiguous piece.
 constexpr int kColCtasPerSm = 2;
 
-template <int kElem, bool kDual, int kBw = 0>
+// kPacked (MX, not dual): the scales go straight into the tensor-core staging
+// order of a k-segmented operand -- chunk (kc, rt) at (kc * RT + rt) * 512 with
+// kc = the expert's first k-chunk + local 32-block / 4, RT = ceil(cols / 128),
+// channel i of the row tile and block j of the chunk at (i % 32) * 16 +
+// (i / 32) * 4 + j -- into a buffer the launcher has zeroed (ld_s unused).
+template <int kElem, bool kDual, int kBw = 0, bool kPacked = false>
 __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x,
     const int32_t* __restrict__ splits, int G, int pad, uint8_t* __restrict__ qT, int64_t ld_q,
@@ -453,8 +458,31 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
   __shared__ SegTable tab;
   __shared__ __align__(16) uint32_t tile[kColTokens * (kColCols / 2) + 4 * 8];
   __shared__ int64_t src_row[2][kColTokens];  // source row of each position, or -1
+  __shared__ int32_t kcp[kMaxExperts + 1];     // kPacked: first k-chunk of each expert
   const bool first = blockIdx.x == 0;
   if (!build_seg_table(tab, splits, G, rows, pad, capacity, status, first)) return;
+  if constexpr (kPacked) {
+    // exclusive prefix of ceil(p_g / 128), two experts per thread
+    __shared__ int32_t wsum[kColThreads / 32];
+    const int tid = threadIdx.x, ln = tid & 31, wd = tid >> 5;
+    const int32_t k0 = 2 * tid < G ? (int32_t)((tab.poff[2 * tid + 1] - tab.poff[2 * tid] + 127) >> 7) : 0;
+    const int32_t k1 = 2 * tid + 1 < G ? (int32_t)((tab.poff[2 * tid + 2] - tab.poff[2 * tid + 1] + 127) >> 7) : 0;
+    int32_t sc = k0 + k1;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, sc, d);
+      if (ln >= d) sc += o;
+    }
+    if (ln == 31) wsum[wd] = sc;
+    __syncthreads();
+    int32_t base = 0;
+    for (int w = 0; w < wd; ++w) base += wsum[w];
+    const int32_t ex = base + sc - (k0 + k1);
+    if (2 * tid <= G) kcp[2 * tid] = ex;
+    if (2 * tid + 1 <= G) kcp[2 * tid + 1] = ex + k0;
+    if (tid == kColThreads - 1) kcp[G] = base + sc;  // the total (G = 512 too)
+    __syncthreads();
+  }
   if (first && pad_offsets != nullptr) {
     for (int g = threadIdx.x; g <= G; g += blockDim.x) pad_offsets[g] = tab.poff[g];
   }
@@ -523,9 +551,22 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
       if (jb < ptot && col < cols) {  // beyond the last expert: nothing written
         const int64_t qoff = (jb >> 5) * kBytesPerBlock;
         uint8_t* s8 = static_cast<uint8_t*>(sT);
-        emit_col_block<kElem>(wa, qT + col * ld_q + qoff, s8 + col * ld_s + (jb >> 5), round_up);
-        if (col + 1 < cols)
-          emit_col_block<kElem>(wb, qT + (col + 1) * ld_q + qoff, s8 + (col + 1) * ld_s + (jb >> 5), round_up);
+        uint8_t *sa, *sb;
+        if constexpr (kPacked) {
+          const int g = find_segment(tab, G, jb);      // jb < ptot: a valid expert
+          const int64_t lb = (jb - tab.poff[g]) >> 5;   // the expert's local 32-block
+          const int64_t kc = kcp[g] + (lb >> 2);
+          const int64_t rtn = (cols + 127) >> 7;
+          const int i0 = (int)(col & 127);              // col even: col + 1 is in the same row tile
+          uint8_t* cb = s8 + (kc * rtn + (col >> 7)) * 512 + (lb & 3);
+          sa = cb + (i0 & 31) * 16 + (i0 >> 5) * 4;
+          sb = cb + ((i0 + 1) & 31) * 16 + ((i0 + 1) >> 5) * 4;
+        } else {
+          sa = s8 + col * ld_s + (jb >> 5);
+          sb = s8 + (col + 1) * ld_s + (jb >> 5);
+        }
+        emit_col_block<kElem>(wa, qT + col * ld_q + qoff, sa, round_up);
+        if (col + 1 < cols) emit_col_block<kElem>(wb, qT + (col + 1) * ld_q + qoff, sb, round_up);
       }
     } else {
       // the 128-token block's amax over the four quarter lanes (all lanes
@@ -839,7 +880,7 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
                               int64_t ld_q, uint8_t* sT, int64_t ld_s, int64_t capacity,
                               int64_t* pad_offsets, int32_t* status, cudaStream_t stream,
                               int num_sms, void* q_row, int64_t ld_qr, uint8_t* s_row,
-                              int64_t ld_sr) {
+                              int64_t ld_sr, int64_t packed_bytes) {
   const bool round_up = (elem & MXG_SCALE_ROUND_UP) != 0;  // rule flag carried in elem
   elem &= 0xFF;
   // persistent: at most kColCtasPerSm CTAs per SM, never more than the tiles
@@ -851,6 +892,19 @@ cudaError_t launch_mx_colwise(const void* x, int64_t rows, int64_t cols, int64_t
   auto* qp = static_cast<uint8_t*>(qT);
   auto* qr = static_cast<uint8_t*>(q_row);
   const bool dual = q_row != nullptr;
+  if (packed_bytes > 0) {  // staging-order scales: slack bytes must read as scale 2^-127
+    cudaError_t e = cudaMemsetAsync(sT, 0, (size_t)packed_bytes, stream);
+    if (e != cudaSuccess) return e;
+    if (elem == MXG_E2M1)
+      mx_colwise_kernel<MXG_E2M1, false, 0, true><<<grid, kColThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, 0, capacity, pad_offsets, status, nullptr, 0,
+          nullptr, 0, round_up);
+    else
+      mx_colwise_kernel<MXG_E4M3, false, 0, true><<<grid, kColThreads, 0, stream>>>(
+          xp, rows, cols, ld_x, splits, G, pad, qp, ld_q, sT, 0, capacity, pad_offsets, status, nullptr, 0,
+          nullptr, 0, round_up);
+    return cudaGetLastError();
+  }
   if (elem == MXG_E2M1) {
     if (dual)
       mx_colwise_kernel<MXG_E2M1, true><<<grid, kColThreads, 0, stream>>>(

@@ -92,12 +92,14 @@ typedef enum mxg_scale_layout { MXG_SCALE_PLAIN = 0, MXG_SCALE_PACKED = 1 } mxg_
  *   data         : codes, row r at (uint8*)data + r*ld  (ld >= cols or cols/2 bytes)
  *   scale        : MXG_SCALE_PLAIN: UE8M0 bytes, row r at scale + r*scale_ld,
  *                  entries [0, cols/32);
- *                  MXG_SCALE_PACKED: the packed order of mx_quantize_rowwise_packed
- *                  (16-byte aligned; scale_ld is ignored), cut into the same
- *                  segments as the call's experts: the m_splits for the forward
- *                  activations and the dgrad gradient, G segments of N rows for
- *                  the forward weights.  The other operands (dgrad weights,
- *                  both wgrad operands) take plain scales only (MXG_ERR_UNSUPPORTED).
+ *                  MXG_SCALE_PACKED: the tensor-core staging order (16-byte
+ *                  aligned; scale_ld is ignored), cut into the same segments
+ *                  as the call's experts -- from mx_quantize_rowwise_packed for
+ *                  row-segmented operands (forward activations and dgrad
+ *                  gradient: the m_splits; forward weights: G segments of N
+ *                  rows) and from mx_quantize_colwise_segment_padded_packed for
+ *                  k-segmented ones (dgrad weights: G segments of N, pad 32;
+ *                  wgrad operands: the m_splits and the call's pad).
  *   elem         : MXG_E2M1 or MXG_E4M3
  *   scale_layout : mxg_scale_layout
  * Requirements: cols % 32 == 0; data 16-byte aligned (32 for E2M1 weights of
@@ -179,6 +181,29 @@ mxg_status mx_quantize_colwise_segment_padded(const void* x, int64_t rows, int64
                                               void* qT, int64_t ld_q, uint8_t* sT, int64_t ld_s,
                                               int64_t capacity, int64_t* d_pad_offsets,
                                               int32_t* d_status, void* stream);
+
+/* Bytes of the packed scales of a column-wise operand of `cols` rows
+ * (channels) and `capacity` padded positions over G experts:
+ * (capacity / 128 + G) * ceil(cols / 128) * 512 -- at least the k-chunks of
+ * every split.  -1 on invalid input. */
+int64_t mx_packed_colwise_scale_bytes(int64_t cols, int64_t capacity, int32_t G);
+
+/* mx_quantize_colwise_segment_padded with the scales written in the
+ * tensor-core staging order of a k-segmented operand (the dgrad weights, both
+ * wgrad operands): the chunk grid restarts at every expert's padded start,
+ * expert g's k-chunks being (sum over h < g of ceil(p_h / 128)) + c; chunk
+ * (kc, rt) at (kc * RT + rt) * 512 with RT = ceil(cols / 128); channel i of
+ * the row tile and block j of the chunk at (i % 32) * 16 + (i / 32) * 4 + j.
+ * The first mx_packed_colwise_scale_bytes(cols, capacity, G) bytes of
+ * s_packed (16-byte aligned, s_bytes at least that) are zeroed first, so
+ * every byte without a channel or block reads as scale 2^-127 (also when the
+ * splits turn out invalid; the codes are then left untouched).  Other
+ * arguments, checks and device errors as mx_quantize_colwise_segment_padded. */
+mxg_status mx_quantize_colwise_segment_padded_packed(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                                     const int32_t* d_m_splits, int32_t G, int32_t pad_multiple,
+                                                     int32_t elem, void* qT, int64_t ld_q, uint8_t* s_packed,
+                                                     int64_t s_bytes, int64_t capacity, int64_t* d_pad_offsets,
+                                                     int32_t* d_status, void* stream);
 
 /* Fused dual MX quantization: one read of x yields both operands of a
  * training step -- the row-wise operand (fwd / dgrad) and the column-wise

@@ -167,13 +167,30 @@ def test_gemm_host_checks(lib):
              ws, vp(FAKE), None) == 5                          # accumulate needs FP32
     assert w(ctypes.byref(dYt), ctypes.byref(Xt), vp(FAKE), 4, 900, 48, vp(FAKE), 2, 1, vp(FAKE),
              ws, vp(FAKE), None) == 2                          # pad % 32
-    dYp = _op(512, 256, 2); dYp.scale_layout = 1
-    Wtp = _op(512, 4 * 256, 2); Wtp.scale_layout = 1
-    assert d(ctypes.byref(dYp), ctypes.byref(Wtp), vp(FAKE), 4, vp(FAKE), 512, 1, vp(FAKE), ws,
-             vp(FAKE), None) == 5                              # dgrad weights: plain scales only
-    dYtp = _op(256, 1024, 1); dYtp.scale_layout = 1
+    dYtp = _op(256, 1024, 1); dYtp.scale_layout = 1; dYtp.scale = FAKE + 8
     assert w(ctypes.byref(dYtp), ctypes.byref(Xt), vp(FAKE), 4, 900, 32, vp(FAKE), 2, 1, vp(FAKE),
-             ws, vp(FAKE), None) == 5                          # wgrad operands: plain scales only
+             ws, vp(FAKE), None) == 3                          # packed wgrad scales must be 16-byte aligned
+
+
+def test_packed_colwise_host_checks(lib):
+    vp = ctypes.c_void_p
+    assert lib.mx_packed_colwise_scale_bytes(2048, 4096, 8) == (32 + 8) * 16 * 512
+    assert lib.mx_packed_colwise_scale_bytes(160, 0, 1) == 1 * 2 * 512
+    assert lib.mx_packed_colwise_scale_bytes(100, 64, 1) == -1 and lib.mx_packed_colwise_scale_bytes(64, 64, 0) == -1
+    f = lib.mx_quantize_colwise_segment_padded_packed
+    need = lib.mx_packed_colwise_scale_bytes(64, 96, 4)
+    #       x        rows cols ld_x splits    G  pad elem q        ld_q s        bytes cap poff      status
+    args = [vp(FAKE), 64, 64, 64, vp(FAKE), 4, 32, 1, vp(FAKE), 48, vp(FAKE), need, 96, vp(FAKE), vp(FAKE), None]
+    bad = list(args); bad[11] = need - 1
+    assert f(*bad) == 2                                                   # packed buffer too small
+    bad = list(args); bad[10] = vp(FAKE + 4)
+    assert f(*bad) == 3                                                   # packed scales misaligned
+    bad = list(args); bad[14] = None
+    assert f(*bad) == 1                                                   # NULL status
+    bad = list(args); bad[6] = 48
+    assert f(*bad) == 2                                                   # pad % 32
+    bad = list(args); bad[7] = 4
+    assert f(*bad) == 5                                                   # bad elem
 
 
 def test_packed_quantize_host_checks(lib):

@@ -162,3 +162,88 @@ def test_dgrad_with_packed_gradient():
     oracle.assert_gemm_close(dX.float().cpu().numpy(), oracle.grouped_dgrad(dYd, Wtd, splits), "dgrad packed dY")
     dYl = mxg.mx_quantize_rowwise_packed(bf16_to_dev(dy), "e2m1", m_splits=d_splits)
     assert torch.equal(mxg.grouped_gemm_dgrad(dYl, Wt, d_splits, check=True), dX)
+
+
+# ------------------------------------------------------------------ k-segmented (column-wise) operands
+
+@pytest.mark.parametrize("elem", ["e2m1", "e4m3"])
+@pytest.mark.parametrize("splits,pad,cols", [([37, 0, 5, 300, 64], 32, 160), ([200, 1, 0, 129], 128, 256),
+                                             ([256, 256, 256], 32, 96)])
+def test_colwise_packed_quantize(elem, splits, pad, cols):
+    mxg = _mxg()
+    splits = np.array(splits, dtype=np.int32)
+    x = synth.normal_bf16(np.random.default_rng(cols + pad), (int(splits.sum()), cols), std=2.0,
+                          outlier_frac=0.02)
+    op, poff = mxg.mx_quantize_colwise_segment_padded(bf16_to_dev(x), i32_to_dev(splits), pad, elem,
+                                                      check=True, packed=True)
+    d, s, p = oracle.quantize_mx_colwise_segment_padded(x, splits, pad, elem)
+    spad = int(p[-1])
+    assert np.array_equal(poff.cpu().numpy(), p)
+    cb = spad // 2 if elem == "e2m1" else spad
+    assert np.array_equal(op.data.cpu().numpy()[:, :cb], d)
+    ref = oracle.pack_scales_mma_kseg(s, p)
+    got = op.scale.cpu().numpy()
+    assert np.array_equal(got[: ref.size], ref)
+    bound = mxg.mx_packed_colwise_scale_bytes(cols, op.cols, len(splits))
+    assert (got[ref.size: bound] == 0).all()     # zeroed slack up to the bound
+
+
+def _kseg_oracle_operand(bits, splits, pad, elem, capacity):
+    """Oracle column-wise operand with oracle-packed scales (junk NaN scale
+    bytes past the packed ones: they must never be read)."""
+    mxg = _mxg()
+    from gpu_util import oracle_operand_colwise
+    op, deq, poff = oracle_operand_colwise(bits, splits, pad, elem, capacity=capacity)
+    _, s, _ = oracle.quantize_mx_colwise_segment_padded(bits, splits, pad, elem)
+    packed = oracle.pack_scales_mma_kseg(s, poff)
+    nbytes = mxg.mx_packed_colwise_scale_bytes(bits.shape[1], capacity, len(splits))
+    buf = np.full(nbytes, 0xFF, dtype=np.uint8)
+    buf[: packed.size] = packed
+    return mxg.MXOperand(op.data, u8_to_dev(buf), elem, capacity, "packed"), deq, poff
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "mxfp8"])
+def test_wgrad_with_oracle_packed_operands(kind):
+    """Segments of odd multiples of 32 (a half-filled MXFP4 step at every
+    expert's end, whose second block must carry the zero slack scale)."""
+    e = KINDS[kind][0]
+    splits = np.array([37, 0, 5, 300, 64, 33], dtype=np.int32)
+    G, S = len(splits), int(splits.sum())
+    N, K, pad = 160, 288, 32
+    rng = np.random.default_rng(61)
+    dy = synth.normal_bf16(rng, (S, N), outlier_frac=0.01)
+    x = synth.normal_bf16(rng, (S, K), outlier_frac=0.01)
+    cap = synth.padded_rows_capacity(S, G, pad)
+    dYt, dYtd, poff = _kseg_oracle_operand(dy, splits, pad, e, cap)
+    Xt, Xtd, _ = _kseg_oracle_operand(x, splits, pad, e, cap)
+    init = rng.standard_normal((G, N, K)).astype(np.float32) * np.float32(1e-3)
+    out = torch.from_numpy(init.copy()).to("cuda:0")
+    _mxg().grouped_gemm_wgrad(dYt, Xt, i32_to_dev(splits), S, pad, out=out, accumulate=True, check=True)
+    ref = oracle.grouped_wgrad(dYtd, Xtd, poff, out_init=init)
+    oracle.assert_gemm_close(out.cpu().numpy(), ref, f"wgrad {kind} oracle-packed")
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "mxfp8"])
+def test_dgrad_and_wgrad_library_packed_equal_plain(kind):
+    mxg = _mxg()
+    e = KINDS[kind][0]
+    splits = np.array([300, 0, 77, 513, 1, 129], dtype=np.int32)
+    G, S, N, K, pad = len(splits), int(splits.sum()), 256, 384, 32
+    rng = np.random.default_rng(71)
+    dy = bf16_to_dev(synth.normal_bf16(rng, (S, N), outlier_frac=0.01))
+    x = bf16_to_dev(synth.normal_bf16(rng, (S, K), outlier_frac=0.01))
+    w = bf16_to_dev(synth.normal_bf16(rng, (G * N, K), outlier_frac=0.01))
+    ds, ws = i32_to_dev(splits), i32_to_dev([N] * G)
+    dYq = mxg.mx_quantize_rowwise_packed(dy, e, m_splits=ds)
+    Wt, _ = mxg.mx_quantize_colwise_segment_padded(w, ws, 32, e, capacity=G * N, check=True)
+    Wtp, _ = mxg.mx_quantize_colwise_segment_padded(w, ws, 32, e, capacity=G * N, check=True, packed=True)
+    assert torch.equal(mxg.grouped_gemm_dgrad(dYq, Wtp, ds, check=True), mxg.grouped_gemm_dgrad(dYq, Wt, ds, check=True))
+    cap = mxg.mx_padded_rows_capacity(S, G, pad)
+    outs = []
+    for packed in (False, True):
+        dYt, _ = mxg.mx_quantize_colwise_segment_padded(dy, ds, pad, e, capacity=cap, check=True, packed=packed)
+        Xt, _ = mxg.mx_quantize_colwise_segment_padded(x, ds, pad, e, capacity=cap, check=True, packed=packed)
+        o = torch.full((G, N, K), 0.5, dtype=torch.float32, device="cuda:0")
+        mxg.grouped_gemm_wgrad(dYt, Xt, ds, S, pad, out=o, accumulate=True, check=True)
+        outs.append(o)
+    assert torch.equal(outs[0], outs[1])
