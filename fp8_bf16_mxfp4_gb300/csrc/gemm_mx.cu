@@ -251,7 +251,8 @@ template <int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
-                           const __grid_constant__ CUtensorMap tmOut, const Params p) {
+                           const __grid_constant__ CUtensorMap tmOut,
+                           const __grid_constant__ CUtensorMap tmOut32, const Params p) {
   using Cfg = KindCfg<kKind>;
   using L = Smem<kKind>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -295,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmA);
     ptx::prefetch_tmap(&tmB);
     ptx::prefetch_tmap(&tmOut);
+    ptx::prefetch_tmap(&tmOut32);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -489,13 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && (full0 || full1)) {
-        for (int b = 0; b < 2; ++b) {
-          if (!(b == 0 ? full0 : full1)) continue;
-          const uint32_t src = buf + (uint32_t)(b * kEpiBoxBytes);
-          const int yy = (int)(y0 + b * kEpiBoxRows);
-          if (reduce) ptx::tma_reduce_add_2d(&tmOut, src, (int)x, yy);
-          else ptx::tma_store_2d(&tmOut, src, (int)x, yy);
-        }
+        // both boxes inside the expert: one 32-row box (the same rows in the same swizzle)
+        const void* map = full1 ? (const void*)&tmOut32 : (const void*)&tmOut;
+        if (reduce) ptx::tma_reduce_add_2d(map, buf, (int)x, (int)y0);
+        else ptx::tma_store_2d(map, buf, (int)x, (int)y0);
         ptx::bulk_commit_group();
         pending = true;
       }
@@ -723,13 +722,14 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   if (!ok) return MXG_ERR_CUDA;
   // the output as tiled-store destination: columns = N (fwd) or K, rows = S
   // (fwd, dgrad) or G*N (wgrad); boxes of 16 rows x 128 bytes
-  CUtensorMap tmOut;
+  CUtensorMap tmOut, tmOut32;  // 16-row boxes, and 32-row boxes for warps whose rows are all valid
   {
     const bool f32 = a.out_dtype == MXG_OUT_F32;
     const int64_t ocols = a.pass == MXG_PASS_FWD ? a.N : a.K;
     const int64_t orows = a.pass == MXG_PASS_WGRAD ? (int64_t)a.G * a.N : a.total_rows;
-    if (!make_tmap(&tmOut, a.out, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ocols,
-                   orows, a.ld_out * (f32 ? 4 : 2), f32 ? 32 : 64, kEpiBoxRows))
+    const CUtensorMapDataType dt = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_tmap(&tmOut, a.out, dt, ocols, orows, a.ld_out * (f32 ? 4 : 2), f32 ? 32 : 64, kEpiBoxRows) ||
+        !make_tmap(&tmOut32, a.out, dt, ocols, orows, a.ld_out * (f32 ? 4 : 2), f32 ? 32 : 64, 2 * kEpiBoxRows))
       return MXG_ERR_CUDA;
   }
 
@@ -755,7 +755,7 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
     }
   }
   const dim3 grid((unsigned)num_sms), block(kThreads);
-  void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmOut, (void*)&p};
+  void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmOut, (void*)&tmOut32, (void*)&p};
   if (cudaLaunchKernel(fn, grid, block, args, (size_t)smem, stream) != cudaSuccess) {
     cudaGetLastError();
     return MXG_ERR_CUDA;
