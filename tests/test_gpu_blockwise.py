@@ -107,6 +107,17 @@ def test_bw_fwd_parity(splits, N, K):
     oracle.assert_gemm_close(Y.float().cpu().numpy(), oracle.grouped_fwd(Ad, Wd, splits, N), "bw fwd")
 
 
+def test_bw_fwd_max_experts():
+    """G = 512 (the largest supported), most experts empty, a few with rows:
+    the plan's totals entry and the tile walk at the largest G."""
+    rng = np.random.default_rng(512)
+    splits = np.zeros(512, dtype=np.int32)
+    live = rng.choice(512, size=24, replace=False)
+    splits[live] = rng.integers(1, 200, size=24)
+    splits[511] = 130                                   # the last expert non-empty
+    test_bw_fwd_parity(splits.tolist(), 128, 128)
+
+
 @pytest.mark.parametrize("splits,N,K", [([0, 77, 300], 256, 384), ([128], 128, 256)])
 def test_bw_dgrad_parity(splits, N, K):
     mxg = _mxg()

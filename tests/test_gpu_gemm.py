@@ -301,3 +301,42 @@ def test_fwd_wide_dynamic_range(kind):
     for r in range(S):
         if np.abs(ref[r]).max() > 0:
             oracle.assert_gemm_close(got[r:r + 1], ref[r:r + 1], f"wide range {kind} row {r}")
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "a8w4"])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_fwd_into_a_strided_output_leaves_the_padding_alone(kind, out_dtype):
+    """out is a view [S, N] of a wider buffer (ld_out = N + 64): the tiled
+    stores clip at column N, so the 64 padding columns keep their sentinel;
+    ragged experts exercise the partial-row boxes."""
+    mxg = _mxg()
+    ea, eb = KINDS[kind]
+    splits = np.array([0, 1, 127, 129, 300, 17], dtype=np.int32)
+    G, S, N, K = len(splits), int(splits.sum()), 288, 256
+    rng = np.random.default_rng(33)
+    x = synth.normal_bf16(rng, (S, K), outlier_frac=0.01)
+    w = synth.normal_bf16(rng, (G * N, K), outlier_frac=0.01)
+    A, Ad = oracle_operand_rowwise(x, ea)
+    W, Wd = oracle_operand_rowwise(w, eb)
+    big = torch.full((S, N + 64), 7.0, dtype=out_dtype, device="cuda:0")
+    out = big[:, :N]
+    mxg.grouped_gemm_fwd(A, W, i32_to_dev(splits), N, out=out, check=True)
+    oracle.assert_gemm_close(out.float().cpu().numpy(), oracle.grouped_fwd(Ad, Wd, splits, N), f"fwd {kind} strided")
+    assert (big[:, N:] == 7.0).all()
+
+
+def test_dgrad_into_a_strided_output_leaves_the_padding_alone():
+    mxg = _mxg()
+    splits = np.array([0, 50, 131, 7], dtype=np.int32)
+    G, S, N, K = len(splits), int(splits.sum()), 96, 288
+    rng = np.random.default_rng(34)
+    dy = synth.normal_bf16(rng, (S, N), outlier_frac=0.01)
+    w = synth.normal_bf16(rng, (G * N, K), outlier_frac=0.01)
+    dY, dYd = oracle_operand_rowwise(dy, "e2m1")
+    from gpu_util import oracle_operand_colwise
+    Wt, Wtd, _ = oracle_operand_colwise(w, [N] * G, 32, "e2m1")
+    big = torch.full((S, K + 32), -3.0, dtype=torch.bfloat16, device="cuda:0")
+    out = big[:, :K]
+    mxg.grouped_gemm_dgrad(dY, Wt, i32_to_dev(splits), out=out, check=True)
+    oracle.assert_gemm_close(out.float().cpu().numpy(), oracle.grouped_dgrad(dYd, Wtd, splits), "dgrad strided")
+    assert (big[:, K:] == -3.0).all()
