@@ -708,6 +708,24 @@ def cores():
         return os.cpu_count()
 
 
+SYNTH_OF = {"a8w4_fwd": "a8w4_fwd", "mxfp4_moe_train": "mxfp4_moe_train", "mxfp8_moe_train": "mxfp4_moe_train",
+            "dense_mxfp4_m8192": "dense_mxfp4_m8192", "blockwise_fp8": "blockwise_fp8",
+            "blockwise_fp8_pow2": "blockwise_fp8"}
+
+
+def workload_config(name):
+    """The GPU arm's `config` for a workload, built from its seeded synthetic
+    description alone (no device memory): both arms print the same dict."""
+    cls = WORKLOAD_CLASSES[name]
+    w = synth.WORKLOADS[SYNTH_OF[name]]
+    obj = cls.__new__(cls)
+    obj.splits = w.splits()
+    obj.G, obj.N, obj.K = w.G, w.N, w.K
+    obj.pad = getattr(w, "pad", None)
+    obj.S = int(obj.splits.sum())
+    return obj.config()
+
+
 def run_reference(args):
     """The oracle as the reference arm, timed on the host cores.  Each step is
     one bounded sample of the workload, sized so that warm-up plus timed steps
@@ -734,7 +752,7 @@ def run_reference(args):
             "value": v, "unit": "TFLOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot_t / max(args.steps, 1) * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload} (bounded oracle sample)"},
+            "config": workload_config(args.workload),
             "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": c, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -332,3 +332,21 @@ def test_bw_dual_rejects_bad_splits_and_writes_nothing():
     assert rc == 0
     assert int(st.item()) == 4
     assert (q == 0xAB).all() and (s == 0xCD).all() and (qT == 0xAB).all() and (sT == 0xCD).all()
+
+
+def test_bw_bounded_wait_gives_up_cleanly():
+    """The blockwise GEMM with an absurdly short wait limit either finishes or
+    reports a timeout (its epilogue's bulk stores drained); the next normal
+    call is correct."""
+    mxg = _mxg()
+    lib = mxg._lib.load()
+    old = lib.mxg_get_wait_timeout_ns()
+    try:
+        lib.mxg_set_wait_timeout_ns(1)
+        try:
+            test_bw_fwd_parity([0, 130, 1, 300], 256, 384)
+        except mxg.MXGError as e:
+            assert e.code == 8
+    finally:
+        lib.mxg_set_wait_timeout_ns(old)
+    test_bw_fwd_parity([0, 130, 1, 300], 256, 384)
