@@ -252,7 +252,7 @@ class A8W4Forward:
     # DRAM bytes (read + write) of one forward call -- plan and GEMM kernels --
     # counted by ncu on GB300 (dram__bytes_read.sum + dram__bytes_write.sum).
     # Algorithmic bytes of the call: 519,045,120.
-    traffic_bytes = 488819968
+    traffic_bytes = 488806400
 
     def check(self):
         self.mxg.check_status(self.status)

@@ -72,6 +72,7 @@ constexpr int kEpiBoxRows = 16;
 constexpr int kEpiBoxBytes = kEpiBoxRows * 128;
 constexpr int kEpiWarpBytes = 2 * kEpiBoxBytes;
 constexpr int kSfTmemCol0 = 256;       // scale staging columns start after the accumulator
+constexpr int kStashCol = 384;         // FP32 epilogue: accumulator columns 128..255, copied here
 
 enum Kind { KIND_MXF4 = 0, KIND_A8W4 = 1, KIND_MXF8 = 2 };
 
@@ -83,6 +84,10 @@ struct KindCfg {
   static constexpr int kSfBytes = kKPS * kChunkBytes * 3;         // A: 1 row chunk, B: 2
   static constexpr int kSfCols = kKPS * 12;                       // TMEM columns per stage
 };
+static_assert(kSfTmemCol0 + kStages * KindCfg<KIND_MXF4>::kSfCols <= kStashCol &&
+                  kSfTmemCol0 + kStages * KindCfg<KIND_MXF8>::kSfCols <= kStashCol &&
+                  kStashCol + BN / 2 <= kTmemCols,
+              "the FP32 stash lies past every scale slot and inside the allocation");
 
 // ---------------------------------------------------------------------------
 // 2. Scale packing.  blockIdx.y selects the operand (0 = A, 1 = B).
@@ -471,7 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // clipped by the tensor map.  TMEM is handed back right after its last
     // read: BF16 first reads the whole tile into registers (BN/2 packed words
     // per thread), so that the buffer waits come after the hand-back; FP32
-    // sends each 32-column chunk as it is read.
+    // keeps the first half of its row in registers and copies the second half
+    // into TMEM columns that no MMA or scale slot uses, then hands back and
+    // writes both halves out while the next tile's MMAs run.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t buf = sbase + (uint32_t)(L::kEpiOff + quarter * kEpiWarpBytes);
@@ -568,13 +575,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        for (int c = 0; c < nch; ++c) {
-          uint32_t r[32];
-          read_chunk(c, r);
-          if (c == nch - 1) release();  // last read: the accumulator is free for the next tile
-          if (skip_out) continue;       // warp-uniform
-          send(r, col0 + c * 32, oy0, full0, full1, p.accumulate != 0);
-          if (direct) store_row_chunk_f32(p, orow, col0 + c * 32, r);
+        // Columns 128..255 are copied into the spare TMEM columns, 0..127 are
+        // read into registers, and the accumulator is handed back before any
+        // output is written: the next tile's MMAs overlap the write-out.
+        uint32_t h[BN / 2];
+#pragma unroll
+        for (int c = BN / 64; c < BN / 32; ++c) {
+          if (c < nch && e.Kc > 0) {  // warp-uniform
+            uint32_t r[32];
+            read_chunk(c, r);
+            ptx::tmem_st_32x32b_x32(tlane + (uint32_t)(kStashCol + (c - BN / 64) * 32), r);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < BN / 64; ++c) {
+          if (c < nch) {
+            uint32_t r[32];
+            read_chunk(c, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[c * 32 + i] = r[i];
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) h[c * 32 + i] = 0;
+          }
+        }
+        release();
+        if (nch > BN / 64 && e.Kc > 0) ptx::tmem_st_wait();  // the stash is complete before it is read
+        if (!skip_out) {
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) {
+            if (c < nch) {
+              send(&h[c * 32], col0 + c * 32, oy0, full0, full1, p.accumulate != 0);
+              if (direct) store_row_chunk_f32(p, orow, col0 + c * 32, &h[c * 32]);
+            }
+          }
+          for (int c = BN / 64; c < nch; ++c) {
+            uint32_t r[32];
+            if (e.Kc > 0) {
+              __syncwarp();
+              ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(kStashCol + (c - BN / 64) * 32), r);
+              ptx::tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = 0;
+            }
+            send(r, col0 + c * 32, oy0, full0, full1, p.accumulate != 0);
+            if (direct) store_row_chunk_f32(p, orow, col0 + c * 32, r);
+          }
         }
       }
       acc_phase ^= 1u;

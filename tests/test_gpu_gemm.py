@@ -145,6 +145,39 @@ def test_fp32_forward_many_tiles_per_cta(kind):
 
 
 @pytest.mark.parametrize("kind", ["mxfp4", "mxfp8"])
+@pytest.mark.parametrize("N", [416, 480])
+def test_fp32_output_column_tail_past_half_tile(kind, N):
+    """FP32 output whose last n-tile holds 160 or 224 columns: the second half
+    of that tile's accumulator is only partly used (5 or 7 of 8 column
+    chunks), on top of full tiles that use all of it."""
+    got, ref = _run_fwd(kind, [300, 5, 0, 129], N, 256, out_dtype=torch.float32, seed=N)
+    oracle.assert_gemm_close(got, ref, f"fwd fp32 {kind} N={N}")
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "mxfp8"])
+def test_wgrad_accumulate_column_tail_past_half_tile(kind):
+    """wgrad += with K = 448 output columns (a full n-tile and one of 192
+    columns) over experts of different contraction lengths."""
+    e = KINDS[kind][0]
+    splits = np.array([70, 0, 200, 33], dtype=np.int32)
+    G, S = len(splits), int(splits.sum())
+    N, K, pad = 192, 448, 32
+    rng = np.random.default_rng(448)
+    dy = synth.normal_bf16(rng, (S, N), outlier_frac=0.01)
+    x = synth.normal_bf16(rng, (S, K), outlier_frac=0.01)
+    cap = synth.padded_rows_capacity(S, G, pad)
+    dYt, dYtd, poff = oracle_operand_colwise(dy, splits, pad, e, capacity=cap)
+    Xt, Xtd, _ = oracle_operand_colwise(x, splits, pad, e, capacity=cap)
+    init = rng.standard_normal((G, N, K)).astype(np.float32) * np.float32(1e-3)
+    out = torch.from_numpy(init.copy()).to("cuda:0")
+    _mxg().grouped_gemm_wgrad(dYt, Xt, i32_to_dev(splits), S, pad, out=out, accumulate=True, check=True)
+    ref = oracle.grouped_wgrad(dYtd, Xtd, poff, out_init=init)
+    got = out.cpu().numpy()
+    oracle.assert_gemm_close(got, ref, f"wgrad {kind} K={K} acc")
+    assert np.array_equal(got[1], init[1])
+
+
+@pytest.mark.parametrize("kind", ["mxfp4", "mxfp8"])
 @pytest.mark.parametrize("accumulate", [False, True])
 def test_wgrad_many_tiles_per_cta(kind, accumulate):
     """Variable-K wgrad with more tiles than SMs (8 experts x 4 x 5 tiles, the
