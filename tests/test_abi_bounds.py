@@ -91,3 +91,25 @@ def test_packed_colwise_bound_covers_the_dgrad_weights(lib):
         poff = np.arange(G + 1) * ((N + 31) // 32 * 32)
         exact = int(oracle.kseg_chunk_prefix(poff)[-1]) * ((K + 127) // 128) * 512
         assert exact <= lib.mx_packed_colwise_scale_bytes(K, G * N, G)
+
+
+@pytest.mark.parametrize("rows,G", [(1, 1), (1000, 4), (4096, 32), (3 * 129, 3), (20000, 512)])
+def test_gemm_workspace_covers_every_routing(lib, rows, G):
+    """The GEMM scratch holds the plan tables and, for operands with plain
+    scales, both operands' scales re-laid out in the MMA order; its size is
+    fixed before the splits are known."""
+    rng = np.random.default_rng(rows * 17 + G)
+    N, K, pad = 160, 288, 32
+    kseg = lambda poff, C: int(oracle.kseg_chunk_prefix(poff)[-1]) * ((C + 127) // 128) * 512
+    plan = 5 * (G + 1) * 4
+    ws_f = lib.mxg_gemm_workspace_size(0, G, rows, N, K, pad)
+    ws_d = lib.mxg_gemm_workspace_size(1, G, rows, N, K, pad)
+    cap = lib.mx_padded_rows_capacity(rows, G, pad)
+    ws_w = lib.mxg_gemm_workspace_size(2, G, cap, N, K, pad)
+    w_rows = oracle.packed_scale_bytes([N] * G, K // 32)
+    wt = kseg(np.arange(G + 1) * N, K)
+    for m in _routings(rng, rows, G, 10):
+        assert plan + oracle.packed_scale_bytes(m, K // 32) + w_rows <= ws_f
+        assert plan + oracle.packed_scale_bytes(m, N // 32) + wt <= ws_d
+        poff = np.concatenate([[0], np.cumsum((m + pad - 1) // pad * pad)])
+        assert plan + kseg(poff, N) + kseg(poff, K) <= ws_w
