@@ -154,3 +154,109 @@ def test_pow2_colwise_segments_match_rowwise_of_each_expert():
         cg, sg = oracle.quantize_bw_1x128(seg, pow2=True)
         assert np.array_equal(codes[:, poff[g]: poff[g + 1]], cg)
         assert np.array_equal(s[:, poff[g] // 128: poff[g + 1] // 128], sg)
+
+
+# --------------------------------------------------------------------------
+# Dequantizer pins ("Add ROCm Triton blockwise FP8 grouped GEMM", PR #716:
+# the value is the E4M3 code times the fp32 scale of its own 1x128 block, or of
+# its own 128x128 tile).  The scale arrays have as many blocks on each axis so
+# that a transposed or shifted broadcast still has the right shape and must be
+# caught by value.  E4M3 codes used: 0x38 = 1.0, 0xB8 = -1.0, 0x7E = 448,
+# 0x01 = 2^-9, 0x00 = 0.
+# --------------------------------------------------------------------------
+def _pin_dequant_1x128(fn):
+    codes = np.full((3, 384), 0x38, dtype=np.uint8)
+    codes[1, 130] = 0xB8
+    codes[2, 300] = 0x7E
+    codes[0, 5] = 0x01
+    codes[2, 0] = 0x00
+    # row r, block b: 2^(3r + b) -- nine distinct scales
+    s = np.array([[1.0, 2.0, 4.0], [8.0, 16.0, 32.0], [64.0, 128.0, 256.0]], dtype=np.float32)
+    d = fn(codes, s)
+    assert d.shape == (3, 384)
+    # hand-worked elements: (row, col) -> code value x its block's scale
+    expect = {(0, 0): 1.0, (0, 127): 1.0, (0, 128): 2.0, (0, 200): 2.0, (0, 383): 4.0,
+              (1, 0): 8.0, (1, 130): -16.0, (1, 256): 32.0,
+              (2, 0): 0.0, (2, 1): 64.0, (2, 255): 128.0, (2, 300): 448.0 * 256.0,
+              (0, 5): 2.0 ** -9}
+    for (r, c), v in expect.items():
+        assert d[r, c] == v, ((r, c), d[r, c], v)
+    # every other element of a block equals that block's scale
+    for r in range(3):
+        for b in range(3):
+            blk = d[r, 128 * b: 128 * b + 128]
+            others = np.delete(blk, [i for i in range(128) if (r, 128 * b + i) in expect])
+            assert (others == 2.0 ** (3 * r + b)).all(), (r, b)
+
+
+def _pin_dequant_128x128(fn):
+    G, N, K = 2, 384, 384
+    codes = np.full((G, N, K), 0x38, dtype=np.uint8)
+    codes[0, 10, 300] = 0xB8
+    codes[1, 383, 0] = 0x7E
+    # expert g, tile (i, j): 2^(3i + j + 16g) -- eighteen distinct scales
+    s = np.array([[[2.0 ** (3 * i + j + 16 * g) for j in range(3)] for i in range(3)] for g in range(G)],
+                 dtype=np.float32)
+    d = fn(codes, s)
+    assert d.shape == (G, N, K)
+    expect = {(0, 0, 0): 1.0, (0, 10, 300): -4.0, (0, 300, 10): 64.0, (0, 200, 200): 16.0,
+              (0, 127, 128): 2.0, (0, 128, 127): 8.0, (1, 0, 0): 65536.0,
+              (1, 383, 0): 448.0 * 2.0 ** 22, (1, 383, 383): 2.0 ** 24}
+    for idx, v in expect.items():
+        assert d[idx] == v, (idx, d[idx], v)
+    for g in range(G):
+        for i in range(3):
+            for j in range(3):
+                t = d[g, 128 * i: 128 * i + 128, 128 * j: 128 * j + 128]
+                n_special = sum(1 for (gg, n, k) in expect
+                                if gg == g and n // 128 == i and k // 128 == j and expect[(gg, n, k)] != 2.0 ** (3 * i + j + 16 * g))
+                assert (t == 2.0 ** (3 * i + j + 16 * g)).sum() == 128 * 128 - n_special, (g, i, j)
+
+
+def test_dequantize_1x128_hand_worked():
+    _pin_dequant_1x128(oracle.dequantize_bw_1x128)
+
+
+def test_dequantize_128x128_hand_worked():
+    _pin_dequant_128x128(oracle.dequantize_bw_128x128)
+
+
+def test_dequantize_pins_catch_planted_axis_swaps():
+    """The pins above are not vacuous: a dequantizer that broadcasts its
+    scales along the wrong axis (transposed block grid, or tiles read
+    [K/128, N/128]) fails them."""
+    def swapped_1x128(codes, s):
+        return oracle.dequantize_bw_1x128(codes, np.ascontiguousarray(s.T))
+
+    def swapped_128x128(codes, s):
+        return oracle.dequantize_bw_128x128(codes, np.ascontiguousarray(np.swapaxes(s, 1, 2)))
+
+    def shifted_128x128(codes, s):   # expert axis misread
+        return oracle.dequantize_bw_128x128(codes, np.ascontiguousarray(s[::-1]))
+
+    for planted, pin in ((swapped_1x128, _pin_dequant_1x128), (swapped_128x128, _pin_dequant_128x128),
+                         (shifted_128x128, _pin_dequant_128x128)):
+        try:
+            pin(planted)
+        except AssertionError:
+            continue
+        raise AssertionError(f"pin did not catch {planted.__name__}")
+
+
+def test_dequantize_inverts_exact_constant_tiles():
+    """Tiles of constant 7 * 2^k quantize exactly (s = 2^k / 64 is exact in
+    fp32, the code is 448 = 0x7E), so dequantization must give back every
+    element exactly, tile by tile, for both schemes."""
+    ks = np.array([[-3, 0, 5], [9, -7, 2], [11, 1, -12]])
+    w = np.empty((1, 384, 384), dtype=np.float32)
+    for i in range(3):
+        for j in range(3):
+            w[0, 128 * i: 128 * i + 128, 128 * j: 128 * j + 128] = 7.0 * 2.0 ** ks[i, j]
+    w[0, 200:210, 130:140] *= -1.0
+    bits = synth.f32_to_bf16_bits(w)
+    codes, s = oracle.quantize_bw_128x128(bits)
+    assert (codes[0] & 0x7F == 0x7E).all()
+    assert np.array_equal(oracle.dequantize_bw_128x128(codes, s), w.astype(np.float64))
+    rows = bits[0, :3]                     # 3 rows x 3 blocks of 1x128
+    c1, s1 = oracle.quantize_bw_1x128(rows)
+    assert np.array_equal(oracle.dequantize_bw_1x128(c1, s1), w[0, :3].astype(np.float64))

@@ -207,3 +207,92 @@ def test_fp64_exactness_bound():
     s2 = s.copy()
     s2[0, 0] = 127 + 40
     assert not oracle.fp64_sum_is_exact(s2, nz, s, nz, "e4m3", "e4m3", 4096)
+
+
+# --------------------------------------------------------------------------
+# The fp64 reference on every configuration's operands.
+# --------------------------------------------------------------------------
+def _pass_shapes():
+    """(config, pass, A format, B format, contraction length, std, outliers)
+    for every pass of every configuration.  The wgrad contracts the largest
+    expert's padded token count."""
+    W = synth.WORKLOADS
+    out = [("tiny_mxfp4_fwd", "fwd", "e2m1", "e2m1", W["tiny_mxfp4_fwd"].K, 1.0, 0.0),
+           ("a8w4_fwd", "fwd", "e4m3", "e2m1", W["a8w4_fwd"].K, 1.0, 0.01)]
+    for cfg, fmt in (("mxfp4_moe_train", "e2m1"), ("mxfp8_moe_train", "e4m3"),
+                     ("blockwise_fp8", "bw"), ("blockwise_fp8_pow2", "bw_pow2"),
+                     ("dense_mxfp4_m2048", "e2m1"), ("dense_mxfp4_m4096", "e2m1"),
+                     ("dense_mxfp4_m8192", "e2m1")):
+        w = W[{"mxfp8_moe_train": "mxfp4_moe_train", "blockwise_fp8_pow2": "blockwise_fp8"}.get(cfg, cfg)]
+        m = w.splits().astype(np.int64)
+        pad = 128 if fmt.startswith("bw") else w.pad
+        tokens = int(((m.max() + pad - 1) // pad) * pad)
+        for p, L in (("fwd", w.K), ("dgrad", w.N), ("wgrad", tokens)):
+            out.append((cfg, p, fmt, fmt, L, w.std, 0.0))
+    return out
+
+
+def _sample_operand(rng, rows, L, fmt, std, outliers, weight):
+    """`rows` rows of length L drawn as the configuration draws them,
+    quantized along L; returns (dequantized float64, scale bytes or None,
+    nonzero-block mask or None)."""
+    x = synth.normal_bf16(rng, (rows, L), std=std, outlier_frac=outliers)
+    if fmt in ("bw", "bw_pow2"):
+        p2 = fmt == "bw_pow2"
+        if weight:     # 128x128 tiles
+            c, s = oracle.quantize_bw_128x128(x.reshape(1, rows, L), pow2=p2)
+            d = oracle.dequantize_bw_128x128(c, s)[0]
+            s = np.repeat(np.repeat(s[0], 128, axis=0), 4, axis=1)
+        else:
+            c, s = oracle.quantize_bw_1x128(x, pow2=p2)
+            d = oracle.dequantize_bw_1x128(c, s)
+            s = np.repeat(s, 4, axis=1)
+        if not p2:
+            return d, None, None
+        sb = (np.log2(s.astype(np.float64)) + 127).astype(np.uint8)     # exact powers of two
+        nz = np.abs(d).reshape(rows, L // 32, 32).max(axis=-1) > 0
+        return d, sb, nz
+    codes, scale = oracle.quantize_mx(x, fmt)
+    d = oracle.dequantize_mx(codes, scale, fmt)
+    nz = (codes & (0x7 if fmt == "e2m1" else 0x7F)).reshape(rows, L // 32, 32).max(axis=-1) > 0
+    return d, scale, nz
+
+
+# configurations whose fp64 sums are provably exact on the sampled operands
+# (sufficient condition of oracle.fp64_sum_is_exact); the others are held to
+# the rounding bound below.  MXFP8 (E4M3 x E4M3 with 32-element scales):
+# products span more than 52 bits over a 2048- to 7168-long sum; fp32
+# blockwise scales give 28-bit operand significands, so even single products
+# round in fp64.  Power-of-two blockwise scales vary little within a row
+# (one per 128 elements) and stay exact.
+EXACT = {"tiny_mxfp4_fwd", "a8w4_fwd", "mxfp4_moe_train", "blockwise_fp8_pow2", "dense_mxfp4_m2048",
+         "dense_mxfp4_m4096", "dense_mxfp4_m8192"}
+
+
+def test_fp64_reference_exact_or_bounded_per_config():
+    """For every pass of every configuration, on 64 x 64 sampled dot products
+    of the pass's full contraction length: either the sufficient exactness
+    condition holds, or the fp64 rounding bound gamma_{L+1} * sum|a_k b_k|
+    is below 0.1% of the smallest per-element allowance of the GEMM
+    comparison (1e-4 * rms(ref)).  Either way the oracle's own error cannot
+    decide a parity test."""
+    rng = np.random.default_rng(77)
+    seen = {}
+    for cfg, p, fa, fb, L, std, outl in _pass_shapes():
+        A, sa, nza = _sample_operand(rng, 64, L, fa, std, outl, weight=False)
+        B, sb, nzb = _sample_operand(rng, 64 if not fb.startswith("bw") or p == "wgrad" else 128, L, fb,
+                                     std, outl, weight=p != "wgrad")
+        exact = False
+        if sa is not None and sb is not None:
+            ea = "e2m1" if fa == "e2m1" else "e4m3"
+            eb = "e2m1" if fb == "e2m1" else "e4m3"
+            exact = oracle.fp64_sum_is_exact(sa, nza, sb, nzb, ea, eb, L)
+        seen.setdefault(cfg, []).append(exact)
+        ref = A @ B.T
+        mag = np.abs(A) @ np.abs(B).T
+        u = 2.0 ** -53
+        gamma = (L + 1) * u / (1 - (L + 1) * u)
+        floor = 1e-4 * float(np.sqrt(np.mean(ref * ref)))
+        assert float(gamma * mag.max()) <= 1e-3 * floor, (cfg, p, gamma * mag.max(), floor)
+    got_exact = {c for c, v in seen.items() if all(v)}
+    assert got_exact == EXACT, got_exact ^ EXACT
