@@ -25,7 +25,7 @@ __all__ = [
     "mx_quantize_rowwise_packed", "mx_packed_scale_bytes", "mx_packed_colwise_scale_bytes",
     "mx_quantize_dual_segment_padded",
     "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "gemm_workspace_size", "mx_gemm_dense",
-    "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns",
+    "mx_padded_rows_capacity", "check_status", "status_tensor", "set_wait_timeout_ns", "set_gemm_cta_group",
     "library_path", "BWOperand", "bw_quantize_1x128", "bw_quantize_128x128",
     "bw_quantize_colwise_padded", "bw_grouped_gemm_fwd", "bw_grouped_gemm_dgrad",
     "bw_grouped_gemm_wgrad", "bw_quantize_1x128_pow2", "bw_quantize_128x128_pow2",
@@ -121,6 +121,15 @@ def check_status(status: torch.Tensor | None = None, device=None) -> int:
 
 def set_wait_timeout_ns(ns: int):
     _lib.load().mxg_set_wait_timeout_ns(int(ns))
+
+
+def set_gemm_cta_group(n: int) -> int:
+    """Choose the MX GEMM kernel: 2 = CTA pairs sharing each 256x256 tile
+    (the default), 1 = the one-SM kernel.  Returns the previous choice."""
+    lib = _lib.load()
+    prev = int(lib.mxg_get_gemm_cta_group())
+    _ok(lib.mxg_set_gemm_cta_group(int(n)), "set_gemm_cta_group")
+    return prev
 
 
 def mx_padded_rows_capacity(rows: int, G: int, pad: int) -> int:

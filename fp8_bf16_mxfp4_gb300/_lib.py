@@ -113,6 +113,8 @@ SIGNATURES = {
     "mxg_status_string": (ctypes.c_char_p, [c_i32]),
     "mxg_set_wait_timeout_ns": (None, [c_u64]),
     "mxg_get_wait_timeout_ns": (c_u64, []),
+    "mxg_set_gemm_cta_group": (c_i32, [c_i32]),
+    "mxg_get_gemm_cta_group": (c_i32, []),
     "mxg_diag_bounded_wait": (c_i32, [c_vp, c_u64, c_vp]),
     "mxg_version": (c_i32, []),
 }

@@ -17,6 +17,8 @@ namespace mxg {
 
 static std::atomic<uint64_t> g_wait_timeout_ns{2000000000ull};
 uint64_t wait_timeout_ns() { return g_wait_timeout_ns.load(std::memory_order_relaxed); }
+static std::atomic<int> g_gemm_cta_group{2};
+int gemm_cta_group() { return g_gemm_cta_group.load(std::memory_order_relaxed); }
 
 namespace {
 
@@ -163,10 +165,16 @@ using namespace mxg;
 
 extern "C" {
 
-int32_t mxg_version(void) { return 100; }
+int32_t mxg_version(void) { return 200; }
 
 void mxg_set_wait_timeout_ns(uint64_t ns) { g_wait_timeout_ns.store(ns ? ns : 1, std::memory_order_relaxed); }
 uint64_t mxg_get_wait_timeout_ns(void) { return wait_timeout_ns(); }
+mxg_status mxg_set_gemm_cta_group(int32_t n) {
+  if (n != 1 && n != 2) return MXG_ERR_SHAPE;
+  mxg::g_gemm_cta_group.store(n, std::memory_order_relaxed);
+  return MXG_OK;
+}
+int32_t mxg_get_gemm_cta_group(void) { return mxg::gemm_cta_group(); }
 
 const char* mxg_status_string(mxg_status s) {
   switch (s) {

@@ -64,6 +64,7 @@ struct Params {
   uint64_t drain_ns;    // teardown waits for copies / MMAs still in flight (>= 200 ms)
   uint32_t idesc;
   int group_m;          // m-tiles per group of the tile order (see tile_mn)
+  int tile_m;           // rows of one scheduled tile: 128, or 256 for a CTA pair (0 = 128)
 };
 
 // Per-expert geometry of one pass (see the table at the top of the file).
@@ -109,7 +110,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int G = p.G;
   const int nt_n = p.pass == MXG_PASS_FWD ? (int)cdiv_d((int)p.N, p.bn) : (int)cdiv_d((int)p.K, p.bn);
-  const int wg_tiles = (int)(cdiv_d((int)p.N, kTileM) * cdiv_d((int)p.K, p.bn));
+  const int tm = p.tile_m > 0 ? p.tile_m : kTileM;  // scheduled tile rows (scale row tiles stay 128)
+  const int wg_tiles = (int)(cdiv_d((int)p.N, tm) * cdiv_d((int)p.K, p.bn));
   int64_t v[2][5];
   bool neg = false;
 #pragma unroll
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t* __res
     v[i][3] = (pg + 127) / 128;
     if (g >= G) v[i][4] = 0;
     else if (p.pass == MXG_PASS_WGRAD) v[i][4] = (pg > 0 || !p.accumulate) ? wg_tiles : 0;
-    else v[i][4] = v[i][1] * nt_n;
+    else v[i][4] = ((mm + tm - 1) / tm) * nt_n;
   }
   int64_t incl[5];
 #pragma unroll

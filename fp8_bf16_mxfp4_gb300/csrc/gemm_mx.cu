@@ -42,6 +42,13 @@
 //      Tiles (expert, m-tile, n-tile) are enumerated expert-major and strided
 //      over the CTAs; inside an expert, m-tiles run in groups (tile_mn) so
 //      that a group's A rows stay in L2 while the n-tiles sweep over them.
+//   By default the kernel runs as clusters of two CTAs on neighbouring SMs
+//   (kCta = 2): a pair owns a 256 x 256 tile, the even CTA issues the 2-SM
+//   block-scaled MMA (tcgen05.mma.cta_group::2, M = 256) for both, and each
+//   CTA stages its own 128 A rows and one 128-row half of the B tile (5-6
+//   stage ring), fills its own TMEM scale slots (its A rows, all 256 B rows)
+//   and writes its own 128 output rows.  mxg_set_gemm_cta_group(1) selects
+//   the one-SM form (kCta = 1: 128 x 256 tiles, 4 stages).
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -57,12 +64,10 @@
 namespace mxg {
 namespace {
 
-constexpr int BM = 128;           // tile rows (TMEM lanes)
+constexpr int BM = 128;           // tile rows of one CTA (TMEM lanes)
 constexpr int BN = 256;           // tile columns (TMEM fp32 columns)
-constexpr int kStages = 4;  // operand pipeline depth
 constexpr int kThreads = 320;
 constexpr int kATileBytes = BM * 128;  // 128 bytes of K per row per stage
-constexpr int kBTileBytes = BN * 128;
 constexpr int kChunkBytes = 512;       // 128 rows x 4 scale bytes
 constexpr int kTmemCols = 512;
 // Epilogue output staging: per epilogue warp (32 tile rows), two boxes of 16
@@ -84,10 +89,7 @@ struct KindCfg {
   static constexpr int kSfBytes = kKPS * kChunkBytes * 3;         // A: 1 row chunk, B: 2
   static constexpr int kSfCols = kKPS * 12;                       // TMEM columns per stage
 };
-static_assert(kSfTmemCol0 + kStages * KindCfg<KIND_MXF4>::kSfCols <= kStashCol &&
-                  kSfTmemCol0 + kStages * KindCfg<KIND_MXF8>::kSfCols <= kStashCol &&
-                  kStashCol + BN / 2 <= kTmemCols,
-              "the FP32 stash lies past every scale slot and inside the allocation");
+static_assert(kStashCol + BN / 2 <= kTmemCols, "the FP32 stash lies inside the allocation");
 
 // ---------------------------------------------------------------------------
 // 2. Scale packing.  blockIdx.y selects the operand (0 = A, 1 = B).
@@ -218,9 +220,17 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, 
 // ---------------------------------------------------------------------------
 // 3. The GEMM kernel.
 // ---------------------------------------------------------------------------
-template <int kKind>
+// Shared-memory layout of one CTA.  kCta = 1: the CTA stages a 128-row A tile
+// and the whole 256-row B tile of its 128x256 output tile.  kCta = 2: a CTA
+// pair computes a 256x256 tile with one MMA stream; each CTA stages its own
+// 128 rows of A and one 128-row half of B, so a stage is 32 KB instead of 48
+// KB and the ring is deeper.
+template <int kKind, int kCta>
 struct Smem {
-  static constexpr int kStageBytes = kATileBytes + kBTileBytes;
+  static constexpr int kStages = kCta == 1 ? 4 : (kKind == KIND_MXF4 ? 5 : 6);  // operand ring depth
+  static constexpr int kBRows = BN / kCta;  // B rows staged by this CTA
+  static constexpr int kBBytes = kBRows * 128;
+  static constexpr int kStageBytes = kATileBytes + kBBytes;
   static constexpr int kDataBytes = kStages * kStageBytes;
   static constexpr int kSfOff = kDataBytes;
   static constexpr int kBarOff = kSfOff + kStages * KindCfg<kKind>::kSfBytes;
@@ -229,6 +239,10 @@ struct Smem {
   // epilogue staging: one buffer per epilogue warp, 1024-byte aligned (swizzle atoms)
   static constexpr int kEpiOff = (kMiscOff + 16 + 1023) & ~1023;
   static constexpr int kTotal = kEpiOff + kEpiWarps * kEpiWarpBytes + 1024;  // + alignment slack
+  static_assert(kStageBytes % 1024 == 0, "stage tiles keep the 1024-byte swizzle-atom alignment");
+  static_assert(kTotal <= 232448, "fits the 227 KB of dynamic shared memory of one CTA");
+  static_assert(kSfTmemCol0 + kStages * KindCfg<kKind>::kSfCols <= kStashCol,
+                "the scale slots end before the FP32 stash columns");
 };
 
 // FP32 output: one 32-column chunk of a row, stored with 32-byte accesses,
@@ -252,24 +266,38 @@ MXG_DEVINL uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <int kKind>
+// kCta = 2 (launched as clusters of two CTAs): the even CTA of the pair
+// issues tcgen05.mma.cta_group::2 with M = 256 (its TMEM and A rows hold tile
+// rows 0-127, the odd CTA's rows 128-255) over B rows split between the two
+// CTAs' stages; both CTAs load their own operands and scales, their feeders
+// fill their own TMEM scale slots (A: the CTA's 128 rows; B: all 256 rows),
+// and their epilogues write their own 128 rows.  Hand-over: the even CTA's
+// issuer waits for the feeders and epilogues of both CTAs (remote arrivals on
+// its own sready / tmem_empty barriers) and commits every stage and every
+// accumulator to the barriers of both CTAs at once.
+template <int kKind, int kCta>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmOut,
                            const __grid_constant__ CUtensorMap tmOut32, const Params p) {
   using Cfg = KindCfg<kKind>;
-  using L = Smem<kKind>;
+  using L = Smem<kKind, kCta>;
+  constexpr int kStages = L::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G;
+  // the CTA's rank in its pair, and the tile walker's index / count (a pair walks together)
+  const uint32_t rank = kCta == 2 ? ptx::cluster_ctarank() : 0u;
+  const int unit = kCta == 2 ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
+  const int units = kCta == 2 ? (int)ptx::nclusters_x() : (int)gridDim.x;
 
   const PlanView pv = plan_view(const_cast<int32_t*>(p.plan), G);
   if (pv.hdr[0] == 0) return;  // invalid splits: nothing is written
   const int total_tiles = pv.hdr[1];
-  if ((int)blockIdx.x >= total_tiles) return;
+  if (unit >= total_tiles) return;  // the same decision in both CTAs of a pair
 
   // per-expert tables: read in place from the plan (a few loads per tile and role)
   const int32_t* t_off = pv.off;
@@ -286,15 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = tmem_full + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  // arrive on the issuing CTA's barrier (the even CTA of a pair)
+  auto arrive_issuer = [&](uint32_t bar) {
+    if constexpr (kCta == 2) ptx::mbar_arrive_cluster(ptx::mapa_shared(bar, 0));
+    else ptx::mbar_arrive(bar);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
-      ptx::mbar_init(sready_bar(s), 4);
+      ptx::mbar_init(sready_bar(s), 4 * kCta);  // the feeder warps of every CTA of the group
     }
     ptx::mbar_init(tmem_full, 1);
-    ptx::mbar_init(tmem_empty, 4);
+    ptx::mbar_init(tmem_empty, 4 * kCta);       // the epilogue warps of every CTA of the group
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
@@ -304,19 +337,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmOut32);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_g<kCta>(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish_g<kCta>();
   }
   ptx::tc_fence_before();
   __syncthreads();
+  // the peer's barriers are initialised before any remote arrival or commit reaches them
+  if constexpr (kCta == 2) ptx::cluster_sync();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // tile -> expert g, this CTA's 128-row m-tile mt, n-tile nt
   auto locate = [&](int tile, int& g, int& mt, int& nt, Geo& e) {
     g = find_prefix(t_tiles, G, tile);
     e = group_geo(p, t_off, t_rt, t_poff, t_kc, g);
     const int ntn = cdiv_d(e.Nn, BN);
-    tile_mn(tile - t_tiles[g], t_tiles[g + 1] - t_tiles[g], ntn, p.group_m, mt, nt);
+    int mg;
+    tile_mn(tile - t_tiles[g], t_tiles[g + 1] - t_tiles[g], ntn, p.group_m, mg, nt);
+    mt = mg * kCta + (int)rank;
   };
 
   if (warp == 0) {
@@ -330,19 +368,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rtA = p.pass == MXG_PASS_WGRAD ? p.rtA_fixed : pv.rt[G];
       const int rtB = p.rtB;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total_tiles && ok; tile += units) {
         int g, mt, nt;
         Geo e;
         locate(tile, g, mt, nt, e);
         const int nk = cdiv_d(e.Kc, Cfg::kStageK);
         const int nb_rows = min(2, cdiv_d(e.Nn - nt * BN, 128));
+        // The odd CTA of a pair whose rows lie past the expert loads no A
+        // (its rows are computed from stale data and never stored; their
+        // scale chunk may not exist).
+        const bool a_in = mt * BM < e.M;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           const int kc_valid = min(Cfg::kKPS, cdiv_d(e.Kc - kb * Cfg::kStageK, 128));
           // The 4-bit-unpacking load of the a8w4 weight tile counts the packed
           // source bytes (64 per row), although it fills 128 bytes per row.
-          constexpr uint32_t kBTx = kKind == KIND_A8W4 ? kBTileBytes / 2 : kBTileBytes;
-          const uint32_t bytes = kATileBytes + kBTx + kc_valid * kChunkBytes * (1 + nb_rows);
+          constexpr uint32_t kBTx = kKind == KIND_A8W4 ? L::kBBytes / 2 : L::kBBytes;
+          const uint32_t bytes = (a_in ? kATileBytes : 0) + kBTx +
+                                 kc_valid * kChunkBytes * ((a_in ? 1 : 0) + nb_rows);
           const uint32_t fb = full_bar(stage);
           ptx::mbar_arrive_expect_tx(fb, bytes);
           armed[stage] = true;
@@ -353,15 +396,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t kbk = e.b_k0 + (int64_t)kb * Cfg::kStageK;
           const int xa = kKind == KIND_MXF4 ? (int)(ka >> 1) : (int)ka;
           const int xb = kKind == KIND_MXF4 ? (int)(kbk >> 1) : (int)kbk;
-          ptx::tma_load_2d(sA, &tmA, xa, (int)(e.a_row0 + (int64_t)mt * BM), fb);
-          ptx::tma_load_2d(sB, &tmB, xb, (int)(e.b_row0 + (int64_t)nt * BN), fb);
+          if (a_in) ptx::tma_load_2d(sA, &tmA, xa, (int)(e.a_row0 + (int64_t)mt * BM), fb);
+          ptx::tma_load_2d(sB, &tmB, xb, (int)(e.b_row0 + (int64_t)nt * BN + (int64_t)rank * L::kBRows), fb);
           const uint32_t sf = sbase + L::kSfOff + stage * Cfg::kSfBytes;
           for (int c = 0; c < kc_valid; ++c) {
             const int kcA = e.a_kc0 + kb * Cfg::kKPS + c;
             const int kcB = e.b_kc0 + kb * Cfg::kKPS + c;
             const uint8_t* srcA = p.packA + ((int64_t)kcA * rtA + e.a_rt0 + mt) * kChunkBytes;
             const uint8_t* srcB = p.packB + ((int64_t)kcB * rtB + e.b_rt0 + 2 * nt) * kChunkBytes;
-            ptx::bulk_load(sf + c * kChunkBytes, srcA, kChunkBytes, fb);
+            if (a_in) ptx::bulk_load(sf + c * kChunkBytes, srcA, kChunkBytes, fb);
+            // the scales of all of the tile's B rows: the MMA of either CTA reads them all
             ptx::bulk_load(sf + Cfg::kKPS * kChunkBytes + c * 2 * kChunkBytes, srcB,
                            nb_rows * kChunkBytes, fb);
           }
@@ -377,20 +421,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int tile = unit; tile < total_tiles && ok; tile += units) {
         int g, mt, nt;
         Geo e;
         locate(tile, g, mt, nt, e);
+        // every epilogue warp of the group has read the previous accumulator
         if (!ptx::mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
         ptx::tc_fence_after();
         const int nk = cdiv_d(e.Kc, Cfg::kStageK);
         for (int kb = 0; kb < nk; ++kb) {
-          // the stage's data has landed and the feeders have put its scales in TMEM
+          // the stage's data has landed and the feeders have put its scales in TMEM (every CTA)
           if (!ptx::mbar_wait(sready_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           ptx::tc_fence_after();
           const int rem = e.Kc - kb * Cfg::kStageK;
@@ -409,20 +454,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sfa = tsf + 4 * c;
             const uint32_t sfb = tsf + Cfg::kKPS * 4 + 8 * c;
             if constexpr (kKind == KIND_MXF4)
-              ptx::mma_mxf4(tmem, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+              ptx::mma_mxf4_g<kCta>(tmem, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
             else
-              ptx::mma_mxf8f6f4(tmem, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+              ptx::mma_mxf8f6f4_g<kCta>(tmem, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
           }
           issued = true;
-          ptx::tc_commit(empty_bar(stage));
+          ptx::tc_commit_pair<kCta>(empty_bar(stage));
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        ptx::tc_commit(tmem_full);
+        ptx::tc_commit_pair<kCta>(tmem_full);
         acc_phase ^= 1u;
       }
-      if (issued) {  // every MMA has retired before TMEM is released
-        ptx::tc_commit(drain_bar);
+      if (issued) {  // every MMA (both CTAs' halves) has retired before TMEM is released
+        ptx::tc_commit_g<kCta>(drain_bar);
         volatile int no_abort = 0;
         ptx::mbar_wait(drain_bar, 0, &no_abort, p.status, p.drain_ns);
       }
@@ -439,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t* sf_lane = smem + L::kSfOff + lane * 16;
     int stage = 0;
     uint32_t phase = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    for (int tile = unit; tile < total_tiles; tile += units) {
       int g, mt, nt;
       Geo e;
       locate(tile, g, mt, nt, e);
@@ -458,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(sready_bar(stage));
+        if (lane == 0) arrive_issuer(sready_bar(stage));
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
@@ -509,9 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto release = [&]() {
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(tmem_empty);
+      if (lane == 0) arrive_issuer(tmem_empty);
     };
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    for (int tile = unit; tile < total_tiles; tile += units) {
       int g, mt, nt;
       Geo e;
       locate(tile, g, mt, nt, e);
@@ -633,10 +678,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  // Neither CTA of a pair leaves (or releases TMEM) while the other may still
+  // arrive on its barriers; the issuer's drain above has retired every MMA.
+  if constexpr (kCta == 2) ptx::cluster_sync();
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    ptx::tmem_dealloc_g<kCta>(tmem, kTmemCols);
   }
 }
 
@@ -666,6 +714,80 @@ PackSizes pack_sizes(int pass, int G, int64_t S, int64_t N, int64_t K, int pad) 
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct KernelInfo {
+  const void* fn;
+  int smem;
+};
+
+KernelInfo kernel_info(int kind, int cta) {
+  if (cta == 2) {
+    switch (kind) {
+      case KIND_MXF4: return {(const void*)grouped_mx_gemm_kernel<KIND_MXF4, 2>, Smem<KIND_MXF4, 2>::kTotal};
+      case KIND_A8W4: return {(const void*)grouped_mx_gemm_kernel<KIND_A8W4, 2>, Smem<KIND_A8W4, 2>::kTotal};
+      default: return {(const void*)grouped_mx_gemm_kernel<KIND_MXF8, 2>, Smem<KIND_MXF8, 2>::kTotal};
+    }
+  }
+  switch (kind) {
+    case KIND_MXF4: return {(const void*)grouped_mx_gemm_kernel<KIND_MXF4, 1>, Smem<KIND_MXF4, 1>::kTotal};
+    case KIND_A8W4: return {(const void*)grouped_mx_gemm_kernel<KIND_A8W4, 1>, Smem<KIND_A8W4, 1>::kTotal};
+    default: return {(const void*)grouped_mx_gemm_kernel<KIND_MXF8, 1>, Smem<KIND_MXF8, 1>::kTotal};
+  }
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_attr_mu;
+
+// The dynamic shared-memory opt-in, once per (device, kind, CTA group).
+bool ensure_smem_attr(const KernelInfo& ki, int kind, int cta, int dev) {
+  static bool done[kMaxDevices][3][2] = {};
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (dev >= 0 && dev < kMaxDevices && done[dev][kind][cta - 1]) return true;
+  if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (dev >= 0 && dev < kMaxDevices) done[dev][kind][cta - 1] = true;
+  return true;
+}
+
+// Number of CTA pairs of the 2-SM kernel that the device holds at once (one
+// CTA per SM), looked up once per (device, kind); 0 when clusters of two
+// cannot be scheduled there.
+int pair_cluster_count(int kind, int dev) {
+  static int cached[kMaxDevices][3];
+  static bool have[kMaxDevices][3] = {};
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (have[dev][kind]) return cached[dev][kind];
+  }
+  const KernelInfo ki = kernel_info(kind, 2);
+  int n = 0;
+  if (ensure_smem_attr(ki, kind, 2, dev)) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cfg.gridDim = dim3((unsigned)std::max(2, sms - (sms & 1)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)ki.smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, ki.fn, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  cached[dev][kind] = n;
+  have[dev][kind] = true;
+  return n;
+}
 
 
 }  // namespace
@@ -716,18 +838,26 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   p.status = a.status;
   p.timeout_ns = wait_timeout_ns();
   p.drain_ns = std::max<uint64_t>(p.timeout_ns, 200000000ull);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  // CTA pairs (2-SM MMA) unless the caller chose the one-SM kernel or the
+  // device cannot co-schedule pairs
+  const int pair_clusters = gemm_cta_group() == 2 ? pair_cluster_count(kind, dev) : 0;
+  const int cta = pair_clusters > 0 ? 2 : 1;
+  p.tile_m = BM * cta;
   {  // bytes of one A row along the contraction (wgrad: the mean expert's padded tokens)
     const double eb = kind == KIND_MXF4 ? 0.5 : 1.0;
     const double kc = a.pass == MXG_PASS_FWD ? (double)a.K
                     : a.pass == MXG_PASS_DGRAD ? (double)a.N : (double)a.a_cols / a.G;
-    p.group_m = tile_group_m(kc * eb);
+    p.group_m = std::max(1, tile_group_m(kc * eb) / cta);  // in scheduled tiles of BM * cta rows
   }
 
-  // instruction descriptor: dense, K-major A and B, UE8M0 scales, M=128, N=256
+  // instruction descriptor: dense, K-major A and B, UE8M0 scales, M = 128 per
+  // CTA (256 for a pair), N = 256
   uint32_t at = kind == KIND_MXF4 ? 1u : 0u;
   uint32_t bt = kind == KIND_MXF4 ? 1u : (kind == KIND_A8W4 ? 5u : 0u);
   p.idesc = (at << 7) | (bt << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
-            ((uint32_t)(BM >> 4) << 24);
+            ((uint32_t)((BM * cta) >> 4) << 24);
 
   // 1. plan
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.splits, p, reinterpret_cast<int32_t*>(ws));
@@ -748,23 +878,24 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
     if (cudaGetLastError() != cudaSuccess) return MXG_ERR_CUDA;
   }
 
-  // 3. tensor maps + GEMM
+  // 3. tensor maps + GEMM (each CTA of a pair loads one 128-row half of the B tile)
+  const int b_box = BN / cta;
   CUtensorMap tmA, tmB;
   bool ok;
   if (a.a_cols == 0) {
     // wgrad with zero capacity: every expert is empty and no tile loads data;
     // the maps only need to be well formed (over the workspace).
     ok = make_tmap(&tmA, ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, 16, 1, 16, 128, BM) &&
-         make_tmap(&tmB, ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, 16, 1, 16, 128, BN);
+         make_tmap(&tmB, ws, CU_TENSOR_MAP_DATA_TYPE_UINT8, 16, 1, 16, 128, b_box);
   } else if (kind == KIND_MXF4) {
     ok = make_tmap(&tmA, a.a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_cols / 2, a.a_rows, a.a_ld, 128, BM) &&
-         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_cols / 2, a.b_rows, a.b_ld, 128, BN);
+         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_cols / 2, a.b_rows, a.b_ld, 128, b_box);
   } else if (kind == KIND_A8W4) {
     ok = make_tmap(&tmA, a.a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_cols, a.a_rows, a.a_ld, 128, BM) &&
-         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.b_cols, a.b_rows, a.b_ld, 128, BN);
+         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, a.b_cols, a.b_rows, a.b_ld, 128, b_box);
   } else {
     ok = make_tmap(&tmA, a.a_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a_cols, a.a_rows, a.a_ld, 128, BM) &&
-         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_cols, a.b_rows, a.b_ld, 128, BN);
+         make_tmap(&tmB, a.b_data, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b_cols, a.b_rows, a.b_ld, 128, b_box);
   }
   if (!ok) return MXG_ERR_CUDA;
   // the output as tiled-store destination: columns = N (fwd) or K, rows = S
@@ -780,30 +911,28 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
       return MXG_ERR_CUDA;
   }
 
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static std::mutex mu;
-  static bool attr_set[64][3] = {};
-  const void* fn;
-  int smem;
-  switch (kind) {
-    case KIND_MXF4: fn = (const void*)grouped_mx_gemm_kernel<KIND_MXF4>; smem = Smem<KIND_MXF4>::kTotal; break;
-    case KIND_A8W4: fn = (const void*)grouped_mx_gemm_kernel<KIND_A8W4>; smem = Smem<KIND_A8W4>::kTotal; break;
-    default: fn = (const void*)grouped_mx_gemm_kernel<KIND_MXF8>; smem = Smem<KIND_MXF8>::kTotal; break;
-  }
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    if (dev < 64 && !attr_set[dev][kind]) {
-      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
-        cudaGetLastError();
-        return MXG_ERR_CUDA;
-      }
-      attr_set[dev][kind] = true;
-    }
-  }
-  const dim3 grid((unsigned)num_sms), block(kThreads);
+  const KernelInfo ki = kernel_info(kind, cta);
+  if (!ensure_smem_attr(ki, kind, cta, dev)) return MXG_ERR_CUDA;
   void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmOut, (void*)&tmOut32, (void*)&p};
-  if (cudaLaunchKernel(fn, grid, block, args, (size_t)smem, stream) != cudaSuccess) {
+  cudaError_t err;
+  if (cta == 1) {
+    err = cudaLaunchKernel(ki.fn, dim3((unsigned)num_sms), dim3(kThreads), args, (size_t)ki.smem, stream);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(2 * pair_clusters));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)ki.smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelExC(&cfg, ki.fn, args);
+  }
+  if (err != cudaSuccess) {
     cudaGetLastError();
     return MXG_ERR_CUDA;
   }

@@ -24,7 +24,8 @@
  * ---------------------------------------
  *  - All data pointers are DEVICE pointers owned by the caller; the library
  *    allocates nothing, keeps no state between calls (except the wait timeout
- *    below) and enqueues work on `stream` only, without synchronising, except
+ *    and the GEMM CTA-group choice below) and enqueues work on `stream` only,
+ *    without synchronising, except
  *    mxg_check_status.  `stream` is a cudaStream_t passed as void* (NULL = the
  *    legacy default stream).
  *  - Matrices are row-major.  Strides (`ld*`) are in BYTES for quantized codes
@@ -471,6 +472,18 @@ const char* mxg_status_string(mxg_status s);
 /* Time limit for every bounded wait inside the kernels (default 2 s). */
 void mxg_set_wait_timeout_ns(uint64_t ns);
 uint64_t mxg_get_wait_timeout_ns(void);
+
+/* Which MX GEMM kernel the grouped / dense MX GEMM calls launch (process-wide,
+ * read at each call).  2 (the default): clusters of two CTAs on neighbouring
+ * SMs share each 256 x 256 output tile through the 2-SM block-scaled MMA
+ * (tcgen05.mma.cta_group::2), so that every SM stages half of the tile's B
+ * rows; where the device cannot co-schedule such pairs the one-SM kernel runs
+ * instead.  1: the one-SM kernel (128 x 256 tiles).  Both give results inside
+ * the GEMM tolerance; they differ in speed only.  Any other value returns
+ * MXG_ERR_SHAPE and changes nothing.  Not specific to any passage of the
+ * pages: a scheduling choice of this implementation. */
+mxg_status mxg_set_gemm_cta_group(int32_t n);
+int32_t mxg_get_gemm_cta_group(void);
 
 /* Diagnostic for the bounded-wait machinery: launches one CTA that waits on
  * an mbarrier nothing ever arrives at, with the same bounded wait the GEMM

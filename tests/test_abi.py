@@ -51,7 +51,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_pure_host_functions(lib):
-    assert lib.mxg_version() == 100
+    assert lib.mxg_version() == 200
     assert lib.mx_padded_rows_capacity(131072, 32, 32) == ((131072 + 32 * 31) // 32) * 32
     assert lib.mx_padded_rows_capacity(3, 8, 32) == 96
     assert lib.mx_padded_rows_capacity(0, 4, 128) == 0
@@ -62,6 +62,12 @@ def test_pure_host_functions(lib):
     lib.mxg_set_wait_timeout_ns(12345)
     assert lib.mxg_get_wait_timeout_ns() == 12345
     lib.mxg_set_wait_timeout_ns(old)
+    prev = lib.mxg_get_gemm_cta_group()
+    assert prev == 2                                      # CTA pairs by default
+    assert lib.mxg_set_gemm_cta_group(1) == 0 and lib.mxg_get_gemm_cta_group() == 1
+    assert lib.mxg_set_gemm_cta_group(3) == 2 and lib.mxg_get_gemm_cta_group() == 1  # rejected, unchanged
+    assert lib.mxg_set_gemm_cta_group(0) == 2
+    assert lib.mxg_set_gemm_cta_group(prev) == 0
     assert lib.mxg_gemm_workspace_size(0, 0, 10, 32, 32, 32) == 0      # G < 1
     assert lib.mxg_gemm_workspace_size(2, 4, 1024, 256, 512, 48) == 0  # pad % 32
     assert lib.mxg_gemm_workspace_size(0, 4, 512, 256, 512, 32) > 0

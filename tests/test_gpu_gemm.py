@@ -31,6 +31,15 @@ def _mxg():
     return mxg
 
 
+@pytest.fixture(params=[2, 1], ids=["pair", "onesm"], autouse=True)
+def cta_group(request):
+    """Every case runs on the CTA-pair kernel (256-row tiles over two SMs,
+    the default) and on the one-SM kernel."""
+    prev = _mxg().set_gemm_cta_group(request.param)
+    yield request.param
+    _mxg().set_gemm_cta_group(prev)
+
+
 def _run_fwd(kind, splits, N, K, out_dtype=torch.bfloat16, seed=0, std=1.0, outliers=0.01):
     ea, eb = KINDS[kind]
     splits = np.asarray(splits, dtype=np.int32)
