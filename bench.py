@@ -341,9 +341,11 @@ class MXFP4Train:
 
 
 class DenseMXFP4:
-    """Dense MXFP4 per-pass GEMMs (G = 1), the largest point of the sweep:
-    seqlen 2048 x mbs 4 = 8192 tokens, hidden 8192, FFN 28672; fwd and dgrad
-    BF16 out, wgrad FP32 out (no accumulate)."""
+    """Dense MXFP4 per-pass GEMMs (G = 1) of the sweep "seqlen 2048 x mbs
+    {1, 2, 4}" (M = 2048, 4096, 8192 tokens), hidden 8192, FFN 28672: fwd TN,
+    dgrad NN and wgrad NT, each with BF16 and with FP32 output (six GEMM
+    calls per step, after the six quantizers)."""
+    M = 8192
     name = "dense_mxfp4_m8192"
     call_kernels = "plan + tcgen05 GEMM; scales arrive packed"
 
@@ -351,7 +353,7 @@ class DenseMXFP4:
         import torch
         import fp8_bf16_mxfp4_gb300 as mxg
         self.mxg = mxg
-        w = synth.WORKLOADS["dense_mxfp4_m8192"]
+        w = synth.WORKLOADS[self.name]
         self.splits = w.splits()
         self.G, self.N, self.K, self.pad = w.G, w.N, w.K, w.pad
         self.S = int(self.splits.sum())
@@ -366,8 +368,11 @@ class DenseMXFP4:
         self.w_splits = torch.full((1,), N, dtype=torch.int32, device=dev)
         self.cap = mxg.mx_padded_rows_capacity(S, G, self.pad)
         self.dw = torch.empty((G, N, K), device=dev, dtype=torch.float32)
+        self.dw16 = torch.empty((G, N, K), device=dev, dtype=torch.bfloat16)
         self.y = torch.empty((S, N), dtype=torch.bfloat16, device=dev)
+        self.y32 = torch.empty((S, N), dtype=torch.float32, device=dev)
         self.dx = torch.empty((S, K), dtype=torch.bfloat16, device=dev)
+        self.dx32 = torch.empty((S, K), dtype=torch.float32, device=dev)
         self.y_host = torch.empty((S, N), dtype=torch.bfloat16).pin_memory()
         self.dx_host = torch.empty((S, K), dtype=torch.bfloat16).pin_memory()
         ws = max(mxg.gemm_workspace_size("fwd", G, S, N, K), mxg.gemm_workspace_size("dgrad", G, S, N, K),
@@ -375,30 +380,40 @@ class DenseMXFP4:
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         f = 2.0 * S * N * K
-        self.flops = 3 * f
-        # six quantizers, all writing staging-order scales; three GEMM calls of plan + GEMM
-        self.launches_per_step = 6 + 3 * 2
+        self.flops = 6 * f
+        # six quantizers, all writing staging-order scales; six GEMM calls of plan + GEMM
+        self.launches_per_step = 6 + 6 * 2
         self.timed = _Timed()
-        self.gemm_info = {p: (f, FP4_OVER_BF16, "mxf4") for p in ("fwd", "dgrad", "wgrad")}
+        self.gemm_info = {f"{p}_{o}": (f, FP4_OVER_BF16, "mxf4")
+                          for p in ("fwd", "dgrad", "wgrad") for o in ("bf16", "f32")}
 
     def step(self, time_gemm=False):
-        mxg, N, pad = self.mxg, self.N, self.pad
-        Xq = mxg.mx_quantize_rowwise_packed(self.x, "e2m1", m_splits=self.d_splits, status=self.status)
+        import torch
+        mxg, N, pad, ws, st, T = self.mxg, self.N, self.pad, self.ws, self.status, self.timed
+        Xq = mxg.mx_quantize_rowwise_packed(self.x, "e2m1", m_splits=self.d_splits, status=st)
         Wq = mxg.mx_quantize_rowwise_packed(self.w, "e2m1", groups=1)
-        self.timed.run("fwd", lambda: mxg.grouped_gemm_fwd(Xq, Wq, self.d_splits, N, out=self.y,
-                                                           workspace=self.ws, status=self.status), time_gemm)
-        dYq = mxg.mx_quantize_rowwise_packed(self.dy, "e2m1", m_splits=self.d_splits, status=self.status)
+        T.run("fwd_bf16", lambda: mxg.grouped_gemm_fwd(Xq, Wq, self.d_splits, N, out=self.y, workspace=ws,
+                                                        status=st), time_gemm)
+        T.run("fwd_f32", lambda: mxg.grouped_gemm_fwd(Xq, Wq, self.d_splits, N, out=self.y32,
+                                                       out_dtype=torch.float32, workspace=ws, status=st),
+              time_gemm)
+        dYq = mxg.mx_quantize_rowwise_packed(self.dy, "e2m1", m_splits=self.d_splits, status=st)
         Wt, _ = mxg.mx_quantize_colwise_segment_padded(self.w, self.w_splits, 32, "e2m1",
-                                                       capacity=N, status=self.status, packed=True)
-        self.timed.run("dgrad", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx,
-                                                               workspace=self.ws, status=self.status), time_gemm)
+                                                       capacity=N, status=st, packed=True)
+        T.run("dgrad_bf16", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx, workspace=ws,
+                                                            status=st), time_gemm)
+        T.run("dgrad_f32", lambda: mxg.grouped_gemm_dgrad(dYq, Wt, self.d_splits, out=self.dx32,
+                                                           out_dtype=torch.float32, workspace=ws, status=st),
+              time_gemm)
         dYt, _ = mxg.mx_quantize_colwise_segment_padded(self.dy, self.d_splits, pad, "e2m1",
-                                                        capacity=self.cap, status=self.status, packed=True)
+                                                        capacity=self.cap, status=st, packed=True)
         Xt, _ = mxg.mx_quantize_colwise_segment_padded(self.x, self.d_splits, pad, "e2m1",
-                                                       capacity=self.cap, status=self.status, packed=True)
-        self.timed.run("wgrad", lambda: mxg.grouped_gemm_wgrad(dYt, Xt, self.d_splits, self.S, pad,
-                                                               out=self.dw, accumulate=False,
-                                                               workspace=self.ws, status=self.status), time_gemm)
+                                                       capacity=self.cap, status=st, packed=True)
+        T.run("wgrad_bf16", lambda: mxg.grouped_gemm_wgrad(dYt, Xt, self.d_splits, self.S, pad, out=self.dw16,
+                                                            out_dtype=torch.bfloat16, workspace=ws, status=st),
+              time_gemm)
+        T.run("wgrad_f32", lambda: mxg.grouped_gemm_wgrad(dYt, Xt, self.d_splits, self.S, pad, out=self.dw,
+                                                           accumulate=False, workspace=ws, status=st), time_gemm)
 
     e2e_in = (("x", "x_host"), ("dy", "dy_host"), ("d_splits", "splits_host"))
     e2e_out = (("y", "y_host"), ("dx", "dx_host"))
@@ -410,17 +425,27 @@ class DenseMXFP4:
         return (self.y_host.numel() + self.dx_host.numel()) * 2
 
     def config(self):
-        return {"workload": "dense MXFP4 per-pass GEMMs (G=1): M=8192 tokens (seqlen 2048 x mbs 4), "
-                            "hidden K=8192, FFN N=28672, inputs ~N(0,0.02); fwd TN and dgrad NN BF16 out, "
-                            "wgrad NT FP32 out",
+        return {"workload": f"dense MXFP4 per-pass GEMMs (G=1): M={self.S} tokens (seqlen 2048 x mbs "
+                            f"{self.S // 2048}), hidden K=8192, FFN N=28672, inputs ~N(0,0.02); fwd TN, "
+                            "dgrad NN, wgrad NT, each with BF16 and with FP32 output",
                 "G": 1, "S": self.S, "N": self.N, "K": self.K,
-                "step": "6 quantizers + fwd + dgrad + wgrad",
-                "l2": "W 470 MB and dY 470 MB BF16 exceed L2, no flush"}
+                "step": "6 quantizers + fwd, dgrad, wgrad x {BF16, FP32} out",
+                "l2": "W 470 MB BF16 and every step's operands together exceed L2, no flush"}
 
     dtype = "mxf4 (e2m1 x e2m1, fp32 accumulate)"
 
     def check(self):
         self.mxg.check_status(self.status)
+
+
+class DenseMXFP4M2048(DenseMXFP4):
+    M = 2048
+    name = "dense_mxfp4_m2048"
+
+
+class DenseMXFP4M4096(DenseMXFP4):
+    M = 4096
+    name = "dense_mxfp4_m4096"
 
 
 class MXFP8Train(MXFP4Train):
@@ -561,7 +586,7 @@ def torch_bf16():
 
 
 WORKLOAD_CLASSES = {c.name: c for c in (A8W4Forward, MXFP4Train, MXFP8Train, BlockwiseFP8, DenseMXFP4,
-                                        BlockwiseFP8Pow2)}
+                                        DenseMXFP4M2048, DenseMXFP4M4096, BlockwiseFP8Pow2)}
 
 
 def build_workload(name, dev):
@@ -668,6 +693,8 @@ ORACLE_SAMPLES = {
     "blockwise_fp8": (1024, 7168, "bw", "bw"),
     "blockwise_fp8_pow2": (1024, 7168, "bw_pow2", "bw_pow2"),
     "dense_mxfp4_m8192": (1024, 8192, "e2m1", "e2m1"),
+    "dense_mxfp4_m4096": (1024, 8192, "e2m1", "e2m1"),
+    "dense_mxfp4_m2048": (1024, 8192, "e2m1", "e2m1"),
 }
 
 
@@ -701,6 +728,32 @@ def oracle_sample(workload="a8w4_fwd", rows=None):
                        f"+ dequantize + fp64 matmul")
 
 
+def oracle_quantize_sample(workload="mxfp4_moe_train", rows=4096):
+    """Bounded oracle sample of the row-wise quantizer of the workload's
+    activation format: `rows` rows at the workload's K, timed in full, as
+    algorithmic GB/s (BF16 read + codes + scales written)."""
+    import oracle
+    _, K, ea, _ = ORACLE_SAMPLES[workload]
+    x = synth.normal_bf16(np.random.default_rng(54321), (rows, K))
+    t0 = time.perf_counter()
+    if ea in ("bw", "bw_pow2"):
+        oracle.quantize_bw_1x128(x, pow2=ea == "bw_pow2")
+        per_elt = 2 + 1 + 4 / 128
+    else:
+        oracle.quantize_mx_rowwise(x, ea)
+        per_elt = 2 + (0.5 if ea == "e2m1" else 1.0) + 1 / 32
+    dt = time.perf_counter() - t0
+    fmt = {"e2m1": "MXFP4", "e4m3": "MXFP8", "bw": "1x128 FP8", "bw_pow2": "1x128 FP8 pow2"}[ea]
+    return rows * K * per_elt / dt / 1e9, (f"oracle row-wise {fmt} quantize of {rows} x {K} BF16, "
+                                           f"{per_elt:g} algorithmic bytes per element")
+
+
+# Dense MMA instruction rates per SM and clock, measured on GB300 with
+# back-to-back 128x256 block-scaled MMAs from resident shared memory: one
+# 128x256x32 FP8 (or 128x256x64 FP4) MMA per 128 clocks.
+RAW_MMA_FLOP_PER_CLK = {"fp8": 2 * 128 * 256 * 32 / 128, "fp4": 2 * 128 * 256 * 64 / 128}
+
+
 def cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -709,7 +762,8 @@ def cores():
 
 
 SYNTH_OF = {"a8w4_fwd": "a8w4_fwd", "mxfp4_moe_train": "mxfp4_moe_train", "mxfp8_moe_train": "mxfp4_moe_train",
-            "dense_mxfp4_m8192": "dense_mxfp4_m8192", "blockwise_fp8": "blockwise_fp8",
+            "dense_mxfp4_m8192": "dense_mxfp4_m8192", "dense_mxfp4_m4096": "dense_mxfp4_m4096",
+            "dense_mxfp4_m2048": "dense_mxfp4_m2048", "blockwise_fp8": "blockwise_fp8",
             "blockwise_fp8_pow2": "blockwise_fp8"}
 
 
@@ -769,6 +823,8 @@ def run_gpu(args):
     __graft_entry__.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    import fp8_bf16_mxfp4_gb300 as mxg
+    mxg.set_gemm_cta_group(args.cta_group)
     wl = build_workload(args.workload, dev)
 
     for _ in range(args.warmup):
@@ -825,32 +881,44 @@ def run_gpu(args):
     steps = args.steps
     value = world * wl.flops * steps / (ms_max * 1e-3) / 1e12
     pk, src = peaks()
+    clocks = clk.summary()
+    # the burst bf16 figure for kernels timed in a region shorter than the
+    # sustained measurement's seconds-long loop, the sustained one otherwise
+    basis = "sustained" if ms_max >= 2000.0 else "burst"
+    bf16_peak = pk["bf16_tflops_sustained" if basis == "sustained" else "bf16_tflops"]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_mhz") or pk.get("sm_max_mhz", 2070.0)
     passes = {}
     for name, (f, ratio, kind) in wl.gemm_info.items():
         t = gemm_ms[name]
-        peak = pk["bf16_tflops_sustained"] * ratio
-        passes[name] = {"ms": t, "tflops": f / (t * 1e-3) / 1e12, "peak": peak,
-                        "frac": f / (t * 1e-3) / 1e12 / peak, "mma": kind}
+        peak = bf16_peak * ratio
+        tf = f / (t * 1e-3) / 1e12
+        raw = RAW_MMA_FLOP_PER_CLK["fp4" if kind.startswith("mxf4") else "fp8"] * sms * mhz * 1e6 / 1e12
+        passes[name] = {"ms": t, "tflops": tf, "peak": peak, "frac": tf / peak, "mma": kind,
+                        "raw_mma_tflops": raw, "frac_of_raw_mma": tf / raw}
     dom = max(passes, key=lambda k: passes[k]["ms"])
     d = passes[dom]
     cpu_f, cpu_t, sample = oracle_sample(args.workload)
+    q_gbs, q_sample = oracle_quantize_sample(args.workload)
     line = {
         "metric": "grouped MXFP4/a8w4 GEMM TFLOPS (fwd/dgrad/wgrad) and % of GB300 FP4/FP8 peak",
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "ms_per_step": ms_max / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-        "config": wl.config(),
+        "config": dict(wl.config(), gemm_cta_group=args.cta_group),
         "roofline": {"bound": "tensor", "achieved": d["tflops"], "peak": d["peak"], "unit": "TFLOP/s",
                      "frac": d["frac"], "traffic": getattr(wl, "traffic_bytes", None),
                      "kernel": f"grouped GEMM {dom} call ({getattr(wl, 'call_kernels', 'plan + scale pack + tcgen05 GEMM')})",
-                     "peak_source": f"{src}: bf16_tflops_sustained x {wl.gemm_info[dom][1]:g} "
-                                    f"(nominal {wl.gemm_info[dom][2]}/bf16 dense ratio)",
-                     "gemm_ms": d["ms"]},
+                     "peak_source": f"{src}: bf16_tflops ({basis}) x {wl.gemm_info[dom][1]:g} "
+                                    f"(nominal {wl.gemm_info[dom][2]}/bf16 dense ratio); of measured",
+                     "gemm_ms": d["ms"], "frac_of_raw_mma": d["frac_of_raw_mma"]},
         "passes": passes,
         "cpu_baseline": {"value": cpu_f / cpu_t / 1e12, "unit": "TFLOPS", "cores": cores(),
                          "kind": "oracle", "sample": sample},
+        "cpu_baseline_quantize": {"value": q_gbs, "unit": "GB/s", "cores": cores(), "kind": "oracle",
+                                  "sample": q_sample},
         "gpu_launches": wl.launches_per_step * steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     if e2e_ms is not None:
         line["e2e"] = {"value": world * wl.flops * steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
@@ -865,8 +933,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="a8w4_fwd", choices=sorted(WORKLOAD_CLASSES))
+    ap.add_argument("--workload", default="mxfp4_moe_train", choices=sorted(WORKLOAD_CLASSES))
     ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--cta-group", type=int, default=2, choices=[1, 2],
+                    help="MX GEMM kernel: 2 = CTA pairs sharing 256x256 tiles (default), 1 = one-SM kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
