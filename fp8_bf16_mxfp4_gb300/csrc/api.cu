@@ -375,17 +375,15 @@ size_t mxg_gemm_workspace_size(int32_t pass, int32_t G, int64_t S, int64_t N, in
 
 }  // extern "C"
 
-namespace {
-// The forward pass; d_m_splits == NULL means one expert of all A->rows rows
-// (the dense entry point, G == 1).
-mxg_status fwd_impl(const mxg_mx_operand* A, const mxg_mx_operand* W, const int32_t* d_m_splits,
-                    int32_t G, int64_t N, void* out, int64_t ld_out, int32_t out_dtype, void* ws,
-                    size_t ws_bytes, int32_t* d_status, void* stream) {
+// The forward's host checks that precede the workspace check, in the order
+// the forward entry points apply them.
+mxg_status mxg::fwd_host_checks(const mxg_mx_operand* A, const mxg_mx_operand* W, int32_t G, int64_t N,
+                           const void* out, int64_t ld_out, int32_t out_dtype, const int32_t* d_status) {
   mxg_status st;
   if ((st = check_operand(A, false, true)) != MXG_OK || (st = check_operand(W, false, true)) != MXG_OK)
     return st;
   if (d_status == nullptr) return MXG_ERR_NULL;
-  if ((st = check_out(out, A->rows, ld_out, N, out_dtype)) != MXG_OK) return st;
+  if ((st = check_out(const_cast<void*>(out), A->rows, ld_out, N, out_dtype)) != MXG_OK) return st;
   if (G < 1 || G > kMaxExperts || N <= 0 || N % 32 != 0) return MXG_ERR_SHAPE;
   if (W->rows == 0) return MXG_ERR_SHAPE;
   if (A->cols != W->cols || W->rows != (int64_t)G * N) return MXG_ERR_SHAPE;
@@ -395,6 +393,17 @@ mxg_status fwd_impl(const mxg_mx_operand* A, const mxg_mx_operand* W, const int3
     if (A->cols % 128 != 0) return MXG_ERR_SHAPE;
     if (!aligned(W->data, 32) || W->ld % 32 != 0) return MXG_ERR_ALIGN;
   }
+  return MXG_OK;
+}
+
+namespace {
+// The forward pass; d_m_splits == NULL means one expert of all A->rows rows
+// (the dense entry point, G == 1).
+mxg_status fwd_impl(const mxg_mx_operand* A, const mxg_mx_operand* W, const int32_t* d_m_splits,
+                    int32_t G, int64_t N, void* out, int64_t ld_out, int32_t out_dtype, void* ws,
+                    size_t ws_bytes, int32_t* d_status, void* stream) {
+  mxg_status st;
+  if ((st = fwd_host_checks(A, W, G, N, out, ld_out, out_dtype, d_status)) != MXG_OK) return st;
   const size_t need = gemm_workspace_bytes(MXG_PASS_FWD, G, A->rows, N, A->cols, 32);
   if (ws_bytes < need || (need > 0 && ws == nullptr)) return MXG_ERR_WORKSPACE;
   if (ws != nullptr && !aligned(ws, 256)) return MXG_ERR_ALIGN;

@@ -2,11 +2,12 @@
 // file-scope device array instead of a caller-provided workspace.
 //
 // Some callers cannot allocate device memory at the point where they run the
-// GEMM: code inside a CUDA stream-capture region (allocation calls are not
-// capturable), an inference engine plugin whose device memory is budgeted up
-// front and handed out by the host framework, or a latency-critical path that
-// must never enter the allocator.  This entry point serves them with a fixed
-// scratch area that is part of the library image on every GPU that loads it.
+// GEMM: an inference-engine plugin whose device memory is budgeted up front
+// and handed out by its host framework (it owns no allocator of its own), or a
+// latency-critical path that must never enter an allocator (a cudaMalloc can
+// synchronise the device and wait on the allocator's lock).  This entry point
+// serves them with a fixed scratch area that is part of the library image on
+// every GPU that loads it.
 #include <cstdint>
 #include <mutex>
 
@@ -53,7 +54,11 @@ extern "C" mxg_status grouped_gemm_fwd_noalloc(const mxg_mx_operand* A, const mx
                                                const int32_t* d_m_splits, int32_t G, int64_t N,
                                                void* out, int64_t ld_out, int32_t out_dtype,
                                                int32_t* d_status, void* stream) {
-  if (A == nullptr || W == nullptr || W->data == nullptr) return MXG_ERR_NULL;
+  // the forward's own argument checks come first, so that malformed arguments
+  // get the status grouped_gemm_fwd gives them
+  if (d_m_splits == nullptr) return MXG_ERR_NULL;
+  const mxg_status chk = mxg::fwd_host_checks(A, W, G, N, out, ld_out, out_dtype, d_status);
+  if (chk != MXG_OK) return chk;
   const size_t need = mxg_gemm_workspace_size(MXG_PASS_FWD, G, A->rows, N, A->cols, 32);
   if (need == 0) return MXG_ERR_SHAPE;
   if (need > mxg::kNoAllocScratchBytes) return MXG_ERR_WORKSPACE;  // problem too large

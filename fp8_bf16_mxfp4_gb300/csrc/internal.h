@@ -73,6 +73,10 @@ struct GemmArgs {
 };
 
 size_t gemm_workspace_bytes(int pass, int G, int64_t S, int64_t N, int64_t K, int pad);
+// Host checks of the forward entry points that precede the workspace check
+// (operands, status word, output, G, N, shapes, formats), in their order.
+mxg_status fwd_host_checks(const mxg_mx_operand* A, const mxg_mx_operand* W, int32_t G, int64_t N,
+                           const void* out, int64_t ld_out, int32_t out_dtype, const int32_t* d_status);
 mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_sms);
 
 // Grouped blockwise-FP8 GEMM.  See gemm_bw.cu.

@@ -293,20 +293,24 @@ mxg_status grouped_gemm_wgrad(const mxg_mx_operand* dYt, const mxg_mx_operand* X
 
 /* grouped_gemm_fwd for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point; it exists for code that must not
- * call cudaMalloc at GEMM time -- work recorded inside a CUDA stream capture,
- * an inference-engine plugin whose device memory is budgeted by its host, or a
- * latency-critical path that never enters an allocator.
+ * call cudaMalloc at GEMM time -- an inference-engine plugin whose device
+ * memory is budgeted and handed out by its host framework, or a
+ * latency-critical path that never enters an allocator (an allocation can
+ * synchronise the device or wait on the allocator's lock).
  *
  * Same arguments and results as grouped_gemm_fwd minus the workspace: the
  * scratch is a file-scope device array of 32 MiB (33554432 bytes) inside
  * libmxg.so, held on every GPU that loads the library until the process exits.
- * A problem whose workspace (mxg_gemm_workspace_size(MXG_PASS_FWD, ...))
- * exceeds 32 MiB is rejected with MXG_ERR_WORKSPACE before anything is
+ * The argument checks of grouped_gemm_fwd run first, in its order; then a
+ * problem whose workspace (mxg_gemm_workspace_size(MXG_PASS_FWD, ...))
+ * exceeds 32 MiB is rejected with MXG_ERR_WORKSPACE, before anything is
  * enqueued.  Nothing is allocated: no cudaMalloc / cudaFree and no allocating
  * library routine.
  *   - The first call on a device looks up the array's device address (with
- *     that device made current); make that first call before any stream
- *     capture begins.
+ *     that device made current) and keeps it for the life of the process;
+ *     make that first call before any stream capture begins.  Do not use this
+ *     entry point after a cudaDeviceReset in the same process: the kept
+ *     address is not looked up again.
  *   - Every call shares the one array; each call fully rewrites the parts it
  *     reads, so nothing has to be cleared between calls, but calls that may
  *     overlap on the GPU (different streams without ordering) race on it and

@@ -1,13 +1,15 @@
 """The allocation-free forward entry point (grouped_gemm_fwd_noalloc).
 
 It is for callers that may not allocate device memory when the GEMM runs
-(stream-capture regions, plugins with host-budgeted memory, latency-critical
-paths); its scratch is a fixed 32 MiB array inside the library.  Checked
-through the C ABI against the regular grouped_gemm_fwd on two calls in a row
-(different problems, so the second call cannot lean on what the first left in
-the shared scratch), within the tolerance the GEMM parity tests use.  This
-file is collected last so that a stop-at-first-failure run has already run
-every other test; it also passes alone in a fresh process."""
+(plugins whose device memory is budgeted by their host framework,
+latency-critical paths that never enter an allocator); its scratch is a fixed
+32 MiB array inside the library.  Checked through the C ABI against the
+regular grouped_gemm_fwd on calls in a row: a small problem, a larger one,
+then the small one again, so that stale plan or packed-scale bytes left by a
+different problem in the shared scratch would show.  The tolerance is the one
+the GEMM parity tests use.  This file is collected last so that a
+stop-at-first-failure run has already run every other test; it also passes
+alone in a fresh process."""
 
 import ctypes
 
@@ -49,10 +51,8 @@ def _noalloc(A, W, d_splits, N, out, status):
 
 def test_noalloc_matches_regular_forward_twice():
     import fp8_bf16_mxfp4_gb300 as mxg
-    cases = [
-        (1, [300, 0, 129, 77], 512, 1024, "e2m1", "e2m1"),
-        (2, [1218, 854, 819, 5], 1024, 4096, "e4m3", "e2m1"),
-    ]
+    small = (1, [300, 0, 129, 77], 512, 1024, "e2m1", "e2m1")
+    cases = [small, (2, [1218, 854, 819, 5], 1024, 4096, "e4m3", "e2m1"), small]
     for seed, splits, N, K, ea, eb in cases:
         A, W, d_splits = _problem(seed, splits, N, K, ea, eb)
         st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
@@ -64,16 +64,33 @@ def test_noalloc_matches_regular_forward_twice():
                                  f"noalloc vs grouped_gemm_fwd (seed {seed})")
 
 
+def _operand_c(buf, rows, cols):
+    """A well-formed E2M1 operand description (plain scales) whose pointers
+    lie in a small real buffer: the calls below reject the problem on the
+    host before anything could read it."""
+    import fp8_bf16_mxfp4_gb300 as mxg
+    return mxg._lib.MxOperandC(buf.data_ptr(), buf.data_ptr(), rows, cols, cols // 2, cols // 32, 1, 0)
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     import fp8_bf16_mxfp4_gb300 as mxg
+    lib = mxg._lib.load()
     G, N, K, S = 64, 4096, 8192, 1024      # packed weight scales alone need 64 MiB
     assert mxg.gemm_workspace_size("fwd", G, S, N, K) > 32 << 20
-    A = mxg.MXOperand(torch.empty((S, K // 2), dtype=torch.uint8, device="cuda:0"),
-                      torch.empty((S, K // 32), dtype=torch.uint8, device="cuda:0"), "e2m1", K)
-    W = mxg.MXOperand(torch.empty((1, K // 2), dtype=torch.uint8, device="cuda:0"),
-                      torch.empty((1, K // 32), dtype=torch.uint8, device="cuda:0"), "e2m1", K)
-    W.data = W.data.expand(G * N, K // 2)           # shape only; rejected before any access
-    W.scale = W.scale.expand(G * N, K // 32)
+    buf = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda:0")
+    a, w = _operand_c(buf, S, K), _operand_c(buf, G * N, K)
     out = torch.empty((S, N), dtype=torch.bfloat16, device="cuda:0")
     st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
-    assert _noalloc(A, W, i32_to_dev([S // G] * G), N, out, st) == 9   # MXG_ERR_WORKSPACE
+    d_splits = i32_to_dev([S // G] * G)
+    stream = mxg._stream(out.device)
+    assert lib.grouped_gemm_fwd_noalloc(ctypes.byref(a), ctypes.byref(w), mxg._ptr(d_splits), G, N, mxg._ptr(out),
+                                        N, 1, mxg._ptr(st), stream) == 9    # MXG_ERR_WORKSPACE
+    # a malformed problem gets the status the regular forward gives it, before the size test
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda:0")
+    bad_N = N - 16                                                   # N % 32 != 0
+    reg = lib.grouped_gemm_fwd(ctypes.byref(a), ctypes.byref(w), mxg._ptr(d_splits), G, bad_N, mxg._ptr(out),
+                               N, 1, mxg._ptr(ws), ws.numel(), mxg._ptr(st), stream)
+    assert reg == 2                                                  # MXG_ERR_SHAPE
+    assert lib.grouped_gemm_fwd_noalloc(ctypes.byref(a), ctypes.byref(w), mxg._ptr(d_splits), G, bad_N,
+                                        mxg._ptr(out), N, 1, mxg._ptr(st), stream) == reg
+    mxg.check_status(st)                                             # nothing was enqueued
