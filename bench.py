@@ -170,6 +170,23 @@ def _to_bf16(bits):
     return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
 
 
+# algorithmic bytes per element of a quantized operand (codes + scales)
+OPERAND_BYTES = {"e2m1": 0.5 + 1 / 32, "e4m3": 1 + 1 / 32, "bw_act": 1 + 4 / 128, "bw_w": 1 + 4 / 16384,
+                 "bw_pow2": 1 + 1 / 32}
+
+
+def padded_total(splits, pad):
+    return int(sum(-(-int(m) // pad) * pad for m in splits))
+
+
+def gemm_bytes(a_elems, a_fmt, b_elems, b_fmt, out_elems, out_bytes, accumulate=False):
+    """Algorithmic HBM bytes of one GEMM call: both operands read once (codes
+    and scales), the output written once (read and written when added in
+    place)."""
+    return (a_elems * OPERAND_BYTES[a_fmt] + b_elems * OPERAND_BYTES[b_fmt]
+            + out_elems * out_bytes * (2 if accumulate else 1))
+
+
 class _Timed:
     """Per-call CUDA events around the GEMM launches of the timed steps."""
 
@@ -222,6 +239,7 @@ class A8W4Forward:
         self.launches_per_step = 2 + 2   # two quantizers (scales written packed); plan + GEMM
         self.timed = _Timed()
         self.gemm_info = {"fwd": (self.flops, FP8_OVER_BF16, "mxf8f6f4 (a8w4)")}
+        self.pass_bytes = {"fwd": gemm_bytes(S * K, "e4m3", G * N * K, "e2m1", S * N, 2)}
 
     def step(self, time_gemm=False):
         mxg = self.mxg
@@ -249,10 +267,9 @@ class A8W4Forward:
                 "l2": "inputs larger than L2 (X 67 MB + W 940 MB BF16), no flush"}
 
     dtype = "mxf8f6f4 (e4m3 x e2m1, fp32 accumulate)"
-    # DRAM bytes (read + write) of one forward call -- plan and GEMM kernels --
-    # counted by ncu on GB300 (dram__bytes_read.sum + dram__bytes_write.sum).
-    # Algorithmic bytes of the call: 519,045,120.
-    traffic_bytes = 488806400
+    # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
+    # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
+    traffic_bytes = {"fwd": 284397312 + 210236672}
 
     def check(self):
         self.mxg.check_status(self.status)
@@ -263,6 +280,10 @@ class MXFP4Train:
     name = "mxfp4_moe_train"
     call_kernels = "plan + tcgen05 GEMM; scales arrive packed"
     elem = "e2m1"
+    # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
+    # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
+    traffic_bytes = {"fwd": 777739264 + 509565696, "dgrad": 399596544 + 1818053120,
+                     "wgrad": 2886021632 + 1842235136}
 
     def __init__(self, dev):
         import torch
@@ -297,6 +318,14 @@ class MXFP4Train:
         self.launches_per_step = 6 + 3 * 2
         self.timed = _Timed()
         self.gemm_info = {p: (f, FP4_OVER_BF16, "mxf4") for p in ("fwd", "dgrad", "wgrad")}
+        self.pass_bytes = self._pass_bytes(self.elem)
+
+    def _pass_bytes(self, e):
+        G, N, K, S = self.G, self.N, self.K, self.S
+        sp = padded_total(self.splits, self.pad)
+        return {"fwd": gemm_bytes(S * K, e, G * N * K, e, S * N, 2),
+                "dgrad": gemm_bytes(S * N, e, K * G * N, e, S * K, 2),
+                "wgrad": gemm_bytes(N * sp, e, K * sp, e, G * N * K, 4, accumulate=True)}
 
     def step(self, time_gemm=False):
         mxg, G, N, K, pad = self.mxg, self.G, self.N, self.K, self.pad
@@ -348,6 +377,11 @@ class DenseMXFP4:
     M = 8192
     name = "dense_mxfp4_m8192"
     call_kernels = "plan + tcgen05 GEMM; scales arrive packed"
+    # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
+    # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
+    traffic_bytes = {"fwd_bf16": 226694400 + 441006336, "fwd_f32": 393862656 + 897122560,
+                     "dgrad_bf16": 1026101504 + 121138944, "dgrad_f32": 1064483328 + 244952064,
+                     "wgrad_bf16": 336168960 + 430054400, "wgrad_f32": 489614592 + 889742592}
 
     def __init__(self, dev):
         import torch
@@ -386,6 +420,12 @@ class DenseMXFP4:
         self.timed = _Timed()
         self.gemm_info = {f"{p}_{o}": (f, FP4_OVER_BF16, "mxf4")
                           for p in ("fwd", "dgrad", "wgrad") for o in ("bf16", "f32")}
+        sp = padded_total(self.splits, self.pad)
+        self.pass_bytes = {}
+        for o, ob in (("bf16", 2), ("f32", 4)):
+            self.pass_bytes[f"fwd_{o}"] = gemm_bytes(S * K, "e2m1", N * K, "e2m1", S * N, ob)
+            self.pass_bytes[f"dgrad_{o}"] = gemm_bytes(S * N, "e2m1", K * N, "e2m1", S * K, ob)
+            self.pass_bytes[f"wgrad_{o}"] = gemm_bytes(N * sp, "e2m1", K * sp, "e2m1", N * K, ob)
 
     def step(self, time_gemm=False):
         import torch
@@ -441,11 +481,15 @@ class DenseMXFP4:
 class DenseMXFP4M2048(DenseMXFP4):
     M = 2048
     name = "dense_mxfp4_m2048"
+    traffic_bytes = {"fwd_bf16": 133869056 + 85080832, "fwd_f32": 135900672 + 183673600,
+                     "dgrad_bf16": 217267968 + 20288512, "dgrad_f32": 233902336 + 41399296,
+                     "wgrad_bf16": 101201152 + 416596224, "wgrad_f32": 282469120 + 879962368}
 
 
 class DenseMXFP4M4096(DenseMXFP4):
     M = 4096
     name = "dense_mxfp4_m4096"
+    traffic_bytes = {}    # not captured at this size
 
 
 class MXFP8Train(MXFP4Train):
@@ -453,11 +497,14 @@ class MXFP8Train(MXFP4Train):
     three passes (kind::mxf8f6f4)."""
     name = "mxfp8_moe_train"
     elem = "e4m3"
+    traffic_bytes = {"fwd": 1775431680 + 518178304, "dgrad": 817078784 + 1830243328,
+                     "wgrad": 3336232960 + 1853860352}
 
     def __init__(self, dev):
         super().__init__(dev)
         f = 2.0 * self.S * self.N * self.K
         self.gemm_info = {p: (f, FP8_OVER_BF16, "mxf8f6f4 (mxfp8)") for p in ("fwd", "dgrad", "wgrad")}
+        self.pass_bytes = self._pass_bytes("e4m3")
 
     def config(self):
         c = super().config()
@@ -473,6 +520,10 @@ class BlockwiseFP8:
     """Blockwise-FP8 grouped training step: fwd, dgrad, variable-K wgrad."""
     call_kernels = "plan + tcgen05 GEMM with CUDA-core promotion"
     name = "blockwise_fp8"
+    # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
+    # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
+    traffic_bytes = {"fwd": 712604416 + 251454720, "dgrad": 609754368 + 435942912,
+                     "wgrad": 408186112 + 887915008}
 
     def __init__(self, dev):
         import torch
@@ -503,6 +554,10 @@ class BlockwiseFP8:
         self.launches_per_step = 5 + 3 * 2   # five quantizers; three GEMM calls of two kernels
         self.timed = _Timed()
         self.gemm_info = {p: (f, FP8_OVER_BF16, "f8f6f4 + fp32 promotion") for p in ("fwd", "dgrad", "wgrad")}
+        sp = padded_total(self.splits, 128)
+        self.pass_bytes = {"fwd": gemm_bytes(S * K, "bw_act", G * N * K, "bw_w", S * N, 2),
+                           "dgrad": gemm_bytes(S * N, "bw_act", K * G * N, "bw_w", S * K, 2),
+                           "wgrad": gemm_bytes(N * sp, "bw_act", K * sp, "bw_act", G * N * K, 2)}
 
     def step(self, time_gemm=False):
         mxg, N = self.mxg, self.N
@@ -543,6 +598,8 @@ class BlockwiseFP8Pow2(BlockwiseFP8):
     passes run on the block-scaled MX GEMMs, with no promotion."""
     call_kernels = "plan + scale pack + tcgen05 GEMM"
     name = "blockwise_fp8_pow2"
+    traffic_bytes = {"fwd": 738866944 + 250812672, "dgrad": 623788800 + 436206848,
+                     "wgrad": 404199936 + 883418880}
 
     def __init__(self, dev):
         import torch
@@ -554,6 +611,10 @@ class BlockwiseFP8Pow2(BlockwiseFP8):
         self.launches_per_step = 5 + 3 * 3   # five quantizers; three GEMM calls of three kernels
         f = 2.0 * S * N * K
         self.gemm_info = {p: (f, FP8_OVER_BF16, "mxf8f6f4 (pow2 blockwise)") for p in ("fwd", "dgrad", "wgrad")}
+        sp = padded_total(self.splits, 128)
+        self.pass_bytes = {"fwd": gemm_bytes(S * K, "bw_pow2", G * N * K, "bw_pow2", S * N, 2),
+                           "dgrad": gemm_bytes(S * N, "bw_pow2", K * G * N, "bw_pow2", S * K, 2),
+                           "wgrad": gemm_bytes(N * sp, "bw_pow2", K * sp, "bw_pow2", G * N * K, 2)}
 
     def step(self, time_gemm=False):
         mxg, N = self.mxg, self.N
@@ -888,30 +949,46 @@ def run_gpu(args):
     bf16_peak = pk["bf16_tflops_sustained" if basis == "sustained" else "bf16_tflops"]
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mhz = clocks.get("sm_mhz") or pk.get("sm_max_mhz", 2070.0)
+    hbm = pk["hbm_gbs"]
     passes = {}
     for name, (f, ratio, kind) in wl.gemm_info.items():
         t = gemm_ms[name]
         peak = bf16_peak * ratio
         tf = f / (t * 1e-3) / 1e12
         raw = RAW_MMA_FLOP_PER_CLK["fp4" if kind.startswith("mxf4") else "fp8"] * sms * mhz * 1e6 / 1e12
+        nbytes = wl.pass_bytes[name]
+        t_tensor, t_hbm = f / (peak * 1e12), nbytes / (hbm * 1e9)     # seconds at each roof
         passes[name] = {"ms": t, "tflops": tf, "peak": peak, "frac": tf / peak, "mma": kind,
-                        "raw_mma_tflops": raw, "frac_of_raw_mma": tf / raw}
+                        "raw_mma_tflops": raw, "frac_of_raw_mma": tf / raw,
+                        "bytes": nbytes, "gbs": nbytes / (t * 1e-3) / 1e9,
+                        "bound": "hbm" if t_hbm > t_tensor else "tensor",
+                        "roofline_frac": max(t_tensor, t_hbm) / (t * 1e-3)}
     dom = max(passes, key=lambda k: passes[k]["ms"])
     d = passes[dom]
-    cpu_f, cpu_t, sample = oracle_sample(args.workload)
-    q_gbs, q_sample = oracle_quantize_sample(args.workload)
+    if args.skip_cpu_baseline:
+        cpu_f, cpu_t, sample, q_gbs, q_sample = 0.0, 1.0, "skipped", None, "skipped"
+    else:
+        cpu_f, cpu_t, sample = oracle_sample(args.workload)
+        q_gbs, q_sample = oracle_quantize_sample(args.workload)
     line = {
         "metric": "grouped MXFP4/a8w4 GEMM TFLOPS (fwd/dgrad/wgrad) and % of GB300 FP4/FP8 peak",
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "ms_per_step": ms_max / steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": dict(wl.config(), gemm_cta_group=args.cta_group),
-        "roofline": {"bound": "tensor", "achieved": d["tflops"], "peak": d["peak"], "unit": "TFLOP/s",
-                     "frac": d["frac"], "traffic": getattr(wl, "traffic_bytes", None),
-                     "kernel": f"grouped GEMM {dom} call ({getattr(wl, 'call_kernels', 'plan + scale pack + tcgen05 GEMM')})",
-                     "peak_source": f"{src}: bf16_tflops ({basis}) x {wl.gemm_info[dom][1]:g} "
-                                    f"(nominal {wl.gemm_info[dom][2]}/bf16 dense ratio); of measured",
-                     "gemm_ms": d["ms"], "frac_of_raw_mma": d["frac_of_raw_mma"]},
+        "roofline": dict(
+            ({"bound": "hbm", "achieved": d["gbs"], "peak": hbm, "unit": "GB/s", "frac": d["gbs"] / hbm,
+              "peak_source": f"{src}: hbm_gbs (copy); of measured",
+              "tensor_frac": d["frac"]} if d["bound"] == "hbm" else
+             {"bound": "tensor", "achieved": d["tflops"], "peak": d["peak"], "unit": "TFLOP/s", "frac": d["frac"],
+              "peak_source": f"{src}: bf16_tflops ({basis}) x {wl.gemm_info[dom][1]:g} "
+                             f"(nominal {wl.gemm_info[dom][2]}/bf16 dense ratio); of measured",
+              "hbm_frac": d["gbs"] / hbm}),
+            traffic=getattr(wl, "traffic_bytes", {}).get(dom) if isinstance(getattr(wl, "traffic_bytes", None), dict)
+            else None,
+            algorithmic_bytes=d["bytes"], flops=wl.gemm_info[dom][0],
+            kernel=f"grouped GEMM {dom} call ({getattr(wl, 'call_kernels', 'plan + scale pack + tcgen05 GEMM')})",
+            gemm_ms=d["ms"], frac_of_raw_mma=d["frac_of_raw_mma"]),
         "passes": passes,
         "cpu_baseline": {"value": cpu_f / cpu_t / 1e12, "unit": "TFLOPS", "cores": cores(),
                          "kind": "oracle", "sample": sample},
@@ -935,6 +1012,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mxfp4_moe_train", choices=sorted(WORKLOAD_CLASSES))
     ap.add_argument("--skip-e2e", action="store_true", help="skip the host-buffer end-to-end pass")
+    ap.add_argument("--skip-cpu-baseline", action="store_true",
+                    help="omit the oracle legs (profiling runs of the GPU kernels)")
     ap.add_argument("--cta-group", type=int, default=2, choices=[1, 2],
                     help="MX GEMM kernel: 2 = CTA pairs sharing 256x256 tiles (default), 1 = one-SM kernel")
     args = ap.parse_args()

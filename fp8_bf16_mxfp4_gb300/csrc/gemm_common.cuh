@@ -65,6 +65,7 @@ struct Params {
   uint32_t idesc;
   int group_m;          // m-tiles per group of the tile order (see tile_mn)
   int tile_m;           // rows of one scheduled tile: 128, or 256 for a CTA pair (0 = 128)
+  int a_scale_tma;      // A's packed scales have a fixed row-tile count: loaded through a tensor map
 };
 
 // Per-expert geometry of one pass (see the table at the top of the file).
@@ -226,6 +227,22 @@ EncodeTiledFn get_encode_fn() {
       cudaGetLastError();
   });
   return fn;
+}
+
+// 3-D map over a packed scale buffer: chunks of 128 32-bit words (512 bytes),
+// `rt` chunks per k-chunk row, `kc` k-chunk rows; box = `box_rt` x `box_kc`
+// whole chunks; no swizzle.
+bool make_scale_tmap(CUtensorMap* m, const void* base, int64_t rt, int64_t kc, int box_rt, int box_kc) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)(rt > 0 ? rt : 1), (cuuint64_t)(kc > 0 ? kc : 1)};
+  cuuint64_t strides[2] = {512, (cuuint64_t)(rt > 0 ? rt : 1) * 512};
+  cuuint32_t box[3] = {128, (cuuint32_t)box_rt, (cuuint32_t)box_kc};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 // 2-D K-major operand map: inner extent `inner` (in elements of `dt`), `rows`

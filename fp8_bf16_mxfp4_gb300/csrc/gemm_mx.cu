@@ -76,7 +76,7 @@ constexpr int kEpiWarps = 4;
 constexpr int kEpiBoxRows = 16;
 constexpr int kEpiBoxBytes = kEpiBoxRows * 128;
 constexpr int kEpiWarpBytes = 2 * kEpiBoxBytes;
-constexpr int kSfTmemCol0 = 256;       // scale staging columns start after the accumulator
+constexpr int kSfTmemCol0 = BN;        // scale slots start after the accumulator
 constexpr int kStashCol = 384;         // FP32 epilogue: accumulator columns 128..255, copied here
 
 enum Kind { KIND_MXF4 = 0, KIND_A8W4 = 1, KIND_MXF8 = 2 };
@@ -86,8 +86,7 @@ struct KindCfg {
   static constexpr int kMmaK = kKind == KIND_MXF4 ? 64 : 32;      // elements per MMA
   static constexpr int kStageK = kKind == KIND_MXF4 ? 256 : 128;  // elements per stage
   static constexpr int kKPS = kStageK / 128;                      // scale k-chunks per stage
-  static constexpr int kSfBytes = kKPS * kChunkBytes * 3;         // A: 1 row chunk, B: 2
-  static constexpr int kSfCols = kKPS * 12;                       // TMEM columns per stage
+  static constexpr int kSlotCols = kKPS * 12;                     // TMEM scale slot: A 4 + B 8 columns per k-chunk
 };
 static_assert(kStashCol + BN / 2 <= kTmemCols, "the FP32 stash lies inside the allocation");
 
@@ -224,25 +223,30 @@ __global__ void __launch_bounds__(128) pack_scales_kernel(Params p, PackSrc sa, 
 // and the whole 256-row B tile of its 128x256 output tile.  kCta = 2: a CTA
 // pair computes a 256x256 tile with one MMA stream; each CTA stages its own
 // 128 rows of A and one 128-row half of B, so a stage is 32 KB instead of 48
-// KB and the ring is deeper.
+// KB and the ring is deeper.  TMEM: the 256-column accumulator, then one scale
+// slot per stage (per 128-element k-chunk, 4 columns for the CTA's 128 A rows
+// and 8 for all 256 B rows, in the 32x128b.warpx4 replicated layout).
 template <int kKind, int kCta>
-struct Smem {
+struct Cfg {
+  using K = KindCfg<kKind>;
   static constexpr int kStages = kCta == 1 ? 4 : (kKind == KIND_MXF4 ? 5 : 6);  // operand ring depth
   static constexpr int kBRows = BN / kCta;  // B rows staged by this CTA
   static constexpr int kBBytes = kBRows * 128;
   static constexpr int kStageBytes = kATileBytes + kBBytes;
+  static constexpr int kBChunks = 2;        // 128-row scale chunks of the B tile
+  static constexpr int kSfBytes = K::kKPS * kChunkBytes * (1 + kBChunks);
   static constexpr int kDataBytes = kStages * kStageBytes;
   static constexpr int kSfOff = kDataBytes;
-  static constexpr int kBarOff = kSfOff + kStages * KindCfg<kKind>::kSfBytes;
-  static constexpr int kNumBars = 3 * kStages + 3;  // full, empty, sready, tmem_full, tmem_empty, drain
+  static constexpr int kBarOff = kSfOff + kStages * kSfBytes;
+  static constexpr int kNumBars = 3 * kStages + 3;  // full, empty, sready per stage; tmem_full, tmem_empty, drain
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem addr, abort flag
   // epilogue staging: one buffer per epilogue warp, 1024-byte aligned (swizzle atoms)
   static constexpr int kEpiOff = (kMiscOff + 16 + 1023) & ~1023;
   static constexpr int kTotal = kEpiOff + kEpiWarps * kEpiWarpBytes + 1024;  // + alignment slack
   static_assert(kStageBytes % 1024 == 0, "stage tiles keep the 1024-byte swizzle-atom alignment");
+  static_assert(kSfBytes % 512 == 0, "scale stages keep chunk (and 128-byte TMA) alignment");
   static_assert(kTotal <= 232448, "fits the 227 KB of dynamic shared memory of one CTA");
-  static_assert(kSfTmemCol0 + kStages * KindCfg<kKind>::kSfCols <= kStashCol,
-                "the scale slots end before the FP32 stash columns");
+  static_assert(kSfTmemCol0 + kStages * K::kSlotCols <= kStashCol, "the scale slots end before the FP32 stash columns");
 };
 
 // FP32 output: one 32-column chunk of a row, stored with 32-byte accesses,
@@ -280,9 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmOut,
-                           const __grid_constant__ CUtensorMap tmOut32, const Params p) {
-  using Cfg = KindCfg<kKind>;
-  using L = Smem<kKind, kCta>;
+                           const __grid_constant__ CUtensorMap tmOut32,
+                           const __grid_constant__ CUtensorMap tmSA,
+                           const __grid_constant__ CUtensorMap tmSB, const Params p) {
+  using KC = KindCfg<kKind>;
+  using L = Cfg<kKind, kCta>;
   constexpr int kStages = L::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -335,6 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmB);
     ptx::prefetch_tmap(&tmOut);
     ptx::prefetch_tmap(&tmOut32);
+    ptx::prefetch_tmap(&tmSB);
+    if (p.a_scale_tma) ptx::prefetch_tmap(&tmSA);
   }
   if (warp == 1) {
     ptx::tmem_alloc_g<kCta>(ptx::smem_u32(tmem_slot), kTmemCols);
@@ -359,71 +367,79 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Per stage: the A and B tiles (TMA), the B scale chunks of the stage's
+    // k-chunks (one TMA load of whole 512-byte chunks through a map over the
+    // packed scales), and the A scale chunks -- one TMA load when the A
+    // operand's row-tile count is fixed (wgrad), otherwise one bulk copy per
+    // k-chunk (the row-tile count of a row-segmented A is only known on the
+    // device).  Chunks past the operand are zero-filled; chunks of a
+    // neighbouring expert or a k tail carry scales that no stored output uses.
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t armed_phase[kStages];
-      bool armed[kStages];
-      for (int s = 0; s < kStages; ++s) { armed[s] = false; armed_phase[s] = 0; }
+      uint32_t armed = 0, armed_phase = 0;  // per stage: a load was issued / its phase
       const int rtA = p.pass == MXG_PASS_WGRAD ? p.rtA_fixed : pv.rt[G];
-      const int rtB = p.rtB;
       bool ok = true;
       for (int tile = unit; tile < total_tiles && ok; tile += units) {
         int g, mt, nt;
         Geo e;
         locate(tile, g, mt, nt, e);
-        const int nk = cdiv_d(e.Kc, Cfg::kStageK);
-        const int nb_rows = min(2, cdiv_d(e.Nn - nt * BN, 128));
+        const int nk = cdiv_d(e.Kc, KC::kStageK);
         // The odd CTA of a pair whose rows lie past the expert loads no A
         // (its rows are computed from stale data and never stored; their
         // scale chunk may not exist).
         const bool a_in = mt * BM < e.M;
+        const int ya = (int)(e.a_row0 + (int64_t)mt * BM);
+        const int yb = (int)(e.b_row0 + (int64_t)nt * BN + (int64_t)rank * L::kBRows);
+        const int qb = e.b_rt0 + ((nt * BN) >> 7);  // the B tile's first 128-row scale chunk
+        const uint8_t* srcA0 = p.packA + ((int64_t)e.a_kc0 * rtA + e.a_rt0 + mt) * kChunkBytes;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
-          const int kc_valid = min(Cfg::kKPS, cdiv_d(e.Kc - kb * Cfg::kStageK, 128));
+          const int kc_valid = min(KC::kKPS, cdiv_d(e.Kc - kb * KC::kStageK, 128));
           // The 4-bit-unpacking load of the a8w4 weight tile counts the packed
           // source bytes (64 per row), although it fills 128 bytes per row.
           constexpr uint32_t kBTx = kKind == KIND_A8W4 ? L::kBBytes / 2 : L::kBBytes;
-          const uint32_t bytes = (a_in ? kATileBytes : 0) + kBTx +
-                                 kc_valid * kChunkBytes * ((a_in ? 1 : 0) + nb_rows);
+          const uint32_t a_sf = !a_in ? 0u : p.a_scale_tma ? KC::kKPS * kChunkBytes : kc_valid * kChunkBytes;
+          const uint32_t bytes = (a_in ? kATileBytes : 0) + kBTx + a_sf + KC::kKPS * L::kBChunks * kChunkBytes;
           const uint32_t fb = full_bar(stage);
           ptx::mbar_arrive_expect_tx(fb, bytes);
-          armed[stage] = true;
-          armed_phase[stage] = phase;
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           const uint32_t sA = sbase + stage * L::kStageBytes;
           const uint32_t sB = sA + kATileBytes;
-          const int64_t ka = e.a_k0 + (int64_t)kb * Cfg::kStageK;
-          const int64_t kbk = e.b_k0 + (int64_t)kb * Cfg::kStageK;
+          const int64_t ka = e.a_k0 + (int64_t)kb * KC::kStageK;
+          const int64_t kbk = e.b_k0 + (int64_t)kb * KC::kStageK;
           const int xa = kKind == KIND_MXF4 ? (int)(ka >> 1) : (int)ka;
           const int xb = kKind == KIND_MXF4 ? (int)(kbk >> 1) : (int)kbk;
-          if (a_in) ptx::tma_load_2d(sA, &tmA, xa, (int)(e.a_row0 + (int64_t)mt * BM), fb);
-          ptx::tma_load_2d(sB, &tmB, xb, (int)(e.b_row0 + (int64_t)nt * BN + (int64_t)rank * L::kBRows), fb);
-          const uint32_t sf = sbase + L::kSfOff + stage * Cfg::kSfBytes;
-          for (int c = 0; c < kc_valid; ++c) {
-            const int kcA = e.a_kc0 + kb * Cfg::kKPS + c;
-            const int kcB = e.b_kc0 + kb * Cfg::kKPS + c;
-            const uint8_t* srcA = p.packA + ((int64_t)kcA * rtA + e.a_rt0 + mt) * kChunkBytes;
-            const uint8_t* srcB = p.packB + ((int64_t)kcB * rtB + e.b_rt0 + 2 * nt) * kChunkBytes;
-            if (a_in) ptx::bulk_load(sf + c * kChunkBytes, srcA, kChunkBytes, fb);
-            // the scales of all of the tile's B rows: the MMA of either CTA reads them all
-            ptx::bulk_load(sf + Cfg::kKPS * kChunkBytes + c * 2 * kChunkBytes, srcB,
-                           nb_rows * kChunkBytes, fb);
+          const uint32_t sf = sbase + L::kSfOff + stage * L::kSfBytes;
+          const int kc0 = kb * KC::kKPS;
+          if (a_in) ptx::tma_load_2d(sA, &tmA, xa, ya, fb);
+          ptx::tma_load_2d(sB, &tmB, xb, yb, fb);
+          // B scales: chunks (kc, qb .. qb+1) for the stage's k-chunks, kc-major
+          ptx::tma_load_3d(sf + KC::kKPS * kChunkBytes, &tmSB, 0, qb, e.b_kc0 + kc0, fb);
+          if (a_in) {
+            if (p.a_scale_tma) {
+              ptx::tma_load_3d(sf, &tmSA, 0, e.a_rt0 + mt, e.a_kc0 + kc0, fb);
+            } else {
+              for (int c = 0; c < kc_valid; ++c)
+                ptx::bulk_load(sf + c * kChunkBytes, srcA0 + (int64_t)(kc0 + c) * rtA * kChunkBytes, kChunkBytes, fb);
+            }
           }
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
       // do not leave copies in flight: wait (bounded) for every armed stage
       for (int s = 0; s < kStages; ++s)
-        if (armed[s]) {
+        if ((armed >> s) & 1u) {
           volatile int no_abort = 0;
-          ptx::mbar_wait(full_bar(s), armed_phase[s], &no_abort, p.status, p.drain_ns);
+          ptx::mbar_wait(full_bar(s), (armed_phase >> s) & 1u, &no_abort, p.status, p.drain_ns);
         }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && rank == 0) {
-      int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      int stage = 0, tcount = 0;
+      uint32_t phase = 0;
       bool ok = true;
       bool issued = false;
       for (int tile = unit; tile < total_tiles && ok; tile += units) {
@@ -431,32 +447,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         Geo e;
         locate(tile, g, mt, nt, e);
         // every epilogue warp of the group has read the previous accumulator
-        if (!ptx::mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+        if (!ptx::mbar_wait(tmem_empty, (uint32_t)(tcount & 1) ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
         ptx::tc_fence_after();
-        const int nk = cdiv_d(e.Kc, Cfg::kStageK);
+        const uint32_t dacc = tmem;
+        const int nk = cdiv_d(e.Kc, KC::kStageK);
         for (int kb = 0; kb < nk; ++kb) {
           // the stage's data has landed and the feeders have put its scales in TMEM (every CTA)
           if (!ptx::mbar_wait(sready_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           ptx::tc_fence_after();
-          const int rem = e.Kc - kb * Cfg::kStageK;
-          const int steps = min(4, cdiv_d(rem, Cfg::kMmaK));
+          const int rem = e.Kc - kb * KC::kStageK;
+          const int steps = min(4, cdiv_d(rem, KC::kMmaK));
           const uint32_t sA = sbase + stage * L::kStageBytes;
           const uint32_t sB = sA + kATileBytes;
-          const uint32_t tsf = tmem + kSfTmemCol0 + stage * Cfg::kSfCols;  // A: kKPS*4 cols, then B
+          const uint32_t tsf = tmem + kSfTmemCol0 + stage * KC::kSlotCols;  // A: kKPS*4 cols, then B
           const uint64_t adesc0 = ptx::smem_desc(sA, 16, 1024, 2);
           const uint64_t bdesc0 = ptx::smem_desc(sB, 16, 1024, 2);
           for (int j = 0; j < steps; ++j) {
-            const int kel = j * Cfg::kMmaK;  // element offset inside the stage
+            const int kel = j * KC::kMmaK;  // element offset inside the stage
             const int c = kel >> 7;
             const uint32_t sfid = (uint32_t)((kel & 127) >> 5);
             const uint32_t idesc = p.idesc | (sfid << 4) | (sfid << 29);
             const uint64_t adv = (uint64_t)((j * 32) >> 4);  // 32 bytes of K per MMA
             const uint32_t sfa = tsf + 4 * c;
-            const uint32_t sfb = tsf + Cfg::kKPS * 4 + 8 * c;
+            const uint32_t sfb = tsf + KC::kKPS * 4 + 8 * c;
             if constexpr (kKind == KIND_MXF4)
-              ptx::mma_mxf4_g<kCta>(tmem, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+              ptx::mma_mxf4_g<kCta>(dacc, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
             else
-              ptx::mma_mxf8f6f4_g<kCta>(tmem, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+              ptx::mma_mxf8f6f4_g<kCta>(dacc, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
           }
           issued = true;
           ptx::tc_commit_pair<kCta>(empty_bar(stage));
@@ -464,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         ptx::tc_commit_pair<kCta>(tmem_full);
-        acc_phase ^= 1u;
+        ++tcount;
       }
       if (issued) {  // every MMA (both CTAs' halves) has retired before TMEM is released
         ptx::tc_commit_g<kCta>(drain_bar);
@@ -474,11 +491,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------------ scale feeders
-    // Shared-memory chunk k of a stage (A chunks first, then B) goes to TMEM
-    // columns 4k..4k+3 of the stage's slot, every lane of this warp's quarter
-    // receiving the 16 bytes that tcgen05.cp 32x128b.warpx4 would have given
-    // it.  Chunks the producer skipped (k tail, short N tile) carry stale
-    // bytes into columns that no MMA of the stage reads.
+    // A stage's scale chunks (the A chunk of each k-chunk, then the two B
+    // chunks of each k-chunk) go to the stage's TMEM scale slot, every lane of
+    // this warp's quarter receiving the 16 bytes that tcgen05.cp
+    // 32x128b.warpx4 would have given it: A chunk c to columns 4c..4c+3, the
+    // two B chunks of k-chunk c to the next 8 columns.  Words of chunks past
+    // the operand, a neighbouring expert or a k tail carry scales into columns
+    // that no MMA reads for a stored output.
     const int quarter = warp & 3;
     const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16) + kSfTmemCol0;
     const uint8_t* sf_lane = smem + L::kSfOff + lane * 16;
@@ -488,17 +507,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g, mt, nt;
       Geo e;
       locate(tile, g, mt, nt, e);
-      const int nk = cdiv_d(e.Kc, Cfg::kStageK);
+      const int nk = cdiv_d(e.Kc, KC::kStageK);
       bool ok = true;
       for (int kb = 0; kb < nk; ++kb) {
         const bool landed = ptx::mbar_wait(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns);
         if (!__all_sync(0xffffffffu, landed)) { ok = false; break; }
-        const uint8_t* src = sf_lane + stage * Cfg::kSfBytes;
-        const uint32_t dst = tq + stage * Cfg::kSfCols;
+        const uint8_t* src = sf_lane + stage * L::kSfBytes;
+        const uint32_t dst = tq + stage * KC::kSlotCols;
 #pragma unroll
-        for (int k = 0; k < 3 * Cfg::kKPS; ++k) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + k * kChunkBytes);
-          ptx::tmem_st_32x32b_x4(dst + 4 * k, v.x, v.y, v.z, v.w);
+        for (int c = 0; c < KC::kKPS; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + c * kChunkBytes);
+          ptx::tmem_st_32x32b_x4(dst + 4 * c, v.x, v.y, v.z, v.w);
+        }
+#pragma unroll
+        for (int c = 0; c < KC::kKPS; ++c) {
+          const uint8_t* bsrc = src + (KC::kKPS + c * L::kBChunks) * kChunkBytes;
+          const uint4 v0 = *reinterpret_cast<const uint4*>(bsrc);
+          const uint4 v1 = *reinterpret_cast<const uint4*>(bsrc + kChunkBytes);
+          const uint32_t o[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          ptx::tmem_st_32x32b_x8(dst + 4 * KC::kKPS + 8 * c, o);
         }
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -518,18 +545,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // leaves the SM as whole lines instead of one 32-byte piece per row and
     // lane.  A box only partly inside the expert's rows is written by the
     // lanes of its valid rows directly; columns past the output's last are
-    // clipped by the tensor map.  TMEM is handed back right after its last
-    // read: BF16 first reads the whole tile into registers (BN/2 packed words
-    // per thread), so that the buffer waits come after the hand-back; FP32
-    // keeps the first half of its row in registers and copies the second half
-    // into TMEM columns that no MMA or scale slot uses, then hands back and
-    // writes both halves out while the next tile's MMAs run.
+    // clipped by the map.  TMEM is handed back
+    // right after its last read: BF16 first reads the whole tile into
+    // registers (BN/2 packed words per thread), so that the buffer waits come
+    // after the hand-back; FP32 keeps the first half of its row in registers
+    // and copies the second half into TMEM columns that no MMA or scale slot
+    // uses, then hands back and writes both halves out while the next tile's
+    // MMAs run.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
-    const uint32_t tlane = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t buf = sbase + (uint32_t)(L::kEpiOff + quarter * kEpiWarpBytes);
+    const uint32_t tlane0 = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t ebuf = sbase + (uint32_t)(L::kEpiOff + quarter * kEpiWarpBytes);
     const int brow = lane & 15;                                  // row inside this lane's box
     const uint32_t my_off = (uint32_t)((lane >> 4) * kEpiBoxBytes + brow * 128);
-    uint32_t acc_phase = 0;
+    int tcount = 0;
     bool pending = false;  // lane 0: bulk groups issued
     // stage this lane's 128-byte row piece v[0..31] and send the full boxes
     auto send = [&](const uint32_t* v, int64_t x, int64_t y0, bool full0, bool full1, bool reduce) {
@@ -538,31 +566,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        ptx::st_shared_v4(buf + my_off + (uint32_t)((k ^ (brow & 7)) << 4), v[4 * k], v[4 * k + 1],
+        ptx::st_shared_v4(ebuf + my_off + (uint32_t)((k ^ (brow & 7)) << 4), v[4 * k], v[4 * k + 1],
                           v[4 * k + 2], v[4 * k + 3]);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && (full0 || full1)) {
         // both boxes inside the expert: one 32-row box (the same rows in the same swizzle)
         const void* map = full1 ? (const void*)&tmOut32 : (const void*)&tmOut;
-        if (reduce) ptx::tma_reduce_add_2d(map, buf, (int)x, (int)y0);
-        else ptx::tma_store_2d(map, buf, (int)x, (int)y0);
+        if (reduce) ptx::tma_reduce_add_2d(map, ebuf, (int)x, (int)y0);
+        else ptx::tma_store_2d(map, ebuf, (int)x, (int)y0);
         ptx::bulk_commit_group();
         pending = true;
       }
-    };
-    auto release = [&]() {
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive_issuer(tmem_empty);
     };
     for (int tile = unit; tile < total_tiles; tile += units) {
       int g, mt, nt;
       Geo e;
       locate(tile, g, mt, nt, e);
-      const bool ready = ptx::mbar_wait(tmem_full, acc_phase, abort_flag, p.status, p.timeout_ns);
+      const bool ready = ptx::mbar_wait(tmem_full, (uint32_t)(tcount & 1), abort_flag, p.status, p.timeout_ns);
       if (!__all_sync(0xffffffffu, ready)) break;  // the warp leaves together (.aligned TMEM loads)
       ptx::tc_fence_after();
+      const uint32_t tlane = tlane0;
+      auto release = [&]() {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_issuer(tmem_empty);
+      };
       const int row0 = mt * BM + quarter * 32;  // the warp's first row inside the expert
       const int row = row0 + lane;
       const bool row_ok = row < e.M;
@@ -576,10 +605,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool skip_out = vrows <= 0 || (e.Kc == 0 && p.accumulate);   // nothing of this warp to write
       const int nch = ncols / 32;
       // 32 fp32 columns c of the accumulator (zeros for an empty contraction)
-      auto read_chunk = [&](int c, uint32_t* r) {
+      auto read_chunk = [&](uint32_t taddr, uint32_t* r) {
         if (e.Kc > 0) {
           __syncwarp();
-          ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(c * 32), r);
+          ptx::tmem_ld_32x32b_x32(taddr, r);
           ptx::tmem_ld_wait();
         } else {
 #pragma unroll
@@ -601,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < BN / 32; ++c) {
           if (c < nch) {
             uint32_t r[32];
-            read_chunk(c, r);
+            read_chunk(tlane + (uint32_t)(c * 32), r);
 #pragma unroll
             for (int i = 0; i < 16; ++i) h[c * 16 + i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
           } else {
@@ -628,15 +657,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = BN / 64; c < BN / 32; ++c) {
           if (c < nch && e.Kc > 0) {  // warp-uniform
             uint32_t r[32];
-            read_chunk(c, r);
-            ptx::tmem_st_32x32b_x32(tlane + (uint32_t)(kStashCol + (c - BN / 64) * 32), r);
+            read_chunk(tlane + (uint32_t)(c * 32), r);
+            ptx::tmem_st_32x32b_x32(tlane0 + (uint32_t)(kStashCol + (c - BN / 64) * 32), r);
           }
         }
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) {
           if (c < nch) {
             uint32_t r[32];
-            read_chunk(c, r);
+            read_chunk(tlane + (uint32_t)(c * 32), r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) h[c * 32 + i] = r[i];
           } else {
@@ -658,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
             if (e.Kc > 0) {
               __syncwarp();
-              ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(kStashCol + (c - BN / 64) * 32), r);
+              ptx::tmem_ld_32x32b_x32(tlane0 + (uint32_t)(kStashCol + (c - BN / 64) * 32), r);
               ptx::tmem_ld_wait();
             } else {
 #pragma unroll
@@ -669,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      acc_phase ^= 1u;
+      ++tcount;
     }
     // every bulk store has completed before the CTA ends
     if (lane == 0 && pending) ptx::bulk_wait_group0();
@@ -720,18 +749,17 @@ struct KernelInfo {
   int smem;
 };
 
+template <int kKind>
+KernelInfo kernel_info_kind(int cta) {
+  if (cta == 2) return {(const void*)grouped_mx_gemm_kernel<kKind, 2>, Cfg<kKind, 2>::kTotal};
+  return {(const void*)grouped_mx_gemm_kernel<kKind, 1>, Cfg<kKind, 1>::kTotal};
+}
+
 KernelInfo kernel_info(int kind, int cta) {
-  if (cta == 2) {
-    switch (kind) {
-      case KIND_MXF4: return {(const void*)grouped_mx_gemm_kernel<KIND_MXF4, 2>, Smem<KIND_MXF4, 2>::kTotal};
-      case KIND_A8W4: return {(const void*)grouped_mx_gemm_kernel<KIND_A8W4, 2>, Smem<KIND_A8W4, 2>::kTotal};
-      default: return {(const void*)grouped_mx_gemm_kernel<KIND_MXF8, 2>, Smem<KIND_MXF8, 2>::kTotal};
-    }
-  }
   switch (kind) {
-    case KIND_MXF4: return {(const void*)grouped_mx_gemm_kernel<KIND_MXF4, 1>, Smem<KIND_MXF4, 1>::kTotal};
-    case KIND_A8W4: return {(const void*)grouped_mx_gemm_kernel<KIND_A8W4, 1>, Smem<KIND_A8W4, 1>::kTotal};
-    default: return {(const void*)grouped_mx_gemm_kernel<KIND_MXF8, 1>, Smem<KIND_MXF8, 1>::kTotal};
+    case KIND_MXF4: return kernel_info_kind<KIND_MXF4>(cta);
+    case KIND_A8W4: return kernel_info_kind<KIND_A8W4>(cta);
+    default: return kernel_info_kind<KIND_MXF8>(cta);
   }
 }
 
@@ -789,7 +817,6 @@ int pair_cluster_count(int kind, int dev) {
   return n;
 }
 
-
 }  // namespace
 
 size_t gemm_workspace_bytes(int pass, int G, int64_t S, int64_t N, int64_t K, int pad) {
@@ -818,7 +845,6 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   Params p{};
   p.pass = a.pass;
   p.G = a.G;
-  p.bn = BN;
   p.accumulate = a.accumulate;
   p.out_dtype = a.out_dtype;
   p.S = a.total_rows;
@@ -840,16 +866,17 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   p.drain_ns = std::max<uint64_t>(p.timeout_ns, 200000000ull);
   int dev = 0;
   cudaGetDevice(&dev);
+  // contraction length of the A rows (wgrad: the mean expert's padded tokens)
+  const int64_t kc_len = a.pass == MXG_PASS_FWD ? a.K : a.pass == MXG_PASS_DGRAD ? a.N : a.a_cols / a.G;
   // CTA pairs (2-SM MMA) unless the caller chose the one-SM kernel or the
   // device cannot co-schedule pairs
   const int pair_clusters = gemm_cta_group() == 2 ? pair_cluster_count(kind, dev) : 0;
   const int cta = pair_clusters > 0 ? 2 : 1;
+  p.bn = BN;
   p.tile_m = BM * cta;
-  {  // bytes of one A row along the contraction (wgrad: the mean expert's padded tokens)
+  {  // bytes of one A row along the contraction
     const double eb = kind == KIND_MXF4 ? 0.5 : 1.0;
-    const double kc = a.pass == MXG_PASS_FWD ? (double)a.K
-                    : a.pass == MXG_PASS_DGRAD ? (double)a.N : (double)a.a_cols / a.G;
-    p.group_m = std::max(1, tile_group_m(kc * eb) / cta);  // in scheduled tiles of BM * cta rows
+    p.group_m = std::max(1, tile_group_m((double)kc_len * eb) / cta);  // in scheduled tiles of BM * cta rows
   }
 
   // instruction descriptor: dense, K-major A and B, UE8M0 scales, M = 128 per
@@ -900,6 +927,17 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
   if (!ok) return MXG_ERR_CUDA;
   // the output as tiled-store destination: columns = N (fwd) or K, rows = S
   // (fwd, dgrad) or G*N (wgrad); boxes of 16 rows x 128 bytes
+  // the packed scales as chunk grids: B always (its row-tile count is fixed),
+  // A for wgrad (likewise); a row-segmented A's scales go by bulk copies
+  const int kps = kind == KIND_MXF4 ? 2 : 1;  // scale k-chunks per stage
+  p.a_scale_tma = a.pass == MXG_PASS_WGRAD ? 1 : 0;
+  CUtensorMap tmSA, tmSB;
+  if (!make_scale_tmap(&tmSB, packB, ps.rtB, ps.kcB, 2, kps)) return MXG_ERR_CUDA;
+  if (p.a_scale_tma) {
+    if (!make_scale_tmap(&tmSA, packA, ps.rtA, ps.kcA, 1, kps)) return MXG_ERR_CUDA;
+  } else {
+    tmSA = tmSB;  // not read
+  }
   CUtensorMap tmOut, tmOut32;  // 16-row boxes, and 32-row boxes for warps whose rows are all valid
   {
     const bool f32 = a.out_dtype == MXG_OUT_F32;
@@ -913,7 +951,7 @@ mxg_status launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream, int num_s
 
   const KernelInfo ki = kernel_info(kind, cta);
   if (!ensure_smem_attr(ki, kind, cta, dev)) return MXG_ERR_CUDA;
-  void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmOut, (void*)&tmOut32, (void*)&p};
+  void* args[] = {(void*)&tmA, (void*)&tmB, (void*)&tmOut, (void*)&tmOut32, (void*)&tmSA, (void*)&tmSB, (void*)&p};
   cudaError_t err;
   if (cta == 1) {
     err = cudaLaunchKernel(ki.fn, dim3((unsigned)num_sms), dim3(kThreads), args, (size_t)ki.smem, stream);

@@ -33,8 +33,8 @@ def _mxg():
 
 @pytest.fixture(params=[2, 1], ids=["pair", "onesm"], autouse=True)
 def cta_group(request):
-    """Every case runs on the CTA-pair kernel (256-row tiles over two SMs,
-    the default) and on the one-SM kernel."""
+    """Every case runs on the CTA-pair kernel (256 x 256 tiles over two SMs,
+    the default) and on the one-SM kernel (128 x 256 tiles)."""
     prev = _mxg().set_gemm_cta_group(request.param)
     yield request.param
     _mxg().set_gemm_cta_group(prev)
