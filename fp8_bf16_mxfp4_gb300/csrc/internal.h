@@ -10,7 +10,7 @@
 namespace mxg {
 
 uint64_t wait_timeout_ns();
-int gemm_cta_group();  // 2: MX GEMMs on CTA pairs where possible; 1: one-SM kernel
+int gemm_cta_group();  // 2: MX and blockwise GEMMs on CTA pairs where possible; 1: one-SM kernels
 
 cudaError_t launch_mx_rowwise(const void* x, int64_t rows, int64_t cols, int64_t ld_x, int elem,
                               void* q, int64_t ld_q, uint8_t* s, int64_t ld_s,

@@ -65,6 +65,36 @@ MXG_DEVINL bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, in
   }
 }
 
+// As mbar_wait, for waiters off the critical path: each try_wait may suspend
+// the thread for up to `suspend_ns` (it resumes when the phase completes), so
+// that a long wait does not take issue slots from the warps that share its
+// SM sub-partition.
+MXG_DEVINL bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+MXG_DEVINL bool mbar_wait_quiet(uint32_t bar, uint32_t parity, volatile int* abort, int32_t* status,
+                                uint64_t timeout_ns, uint32_t suspend_ns = 1000) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, suspend_ns)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      report(status, MXG_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- clusters
 MXG_DEVINL uint32_t cluster_ctarank() {
   uint32_t r;
@@ -142,6 +172,10 @@ template <int N>
 MXG_DEVINL void bulk_wait_group_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 // every committed group has completed (its global writes performed)
 MXG_DEVINL void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// 16 bytes from shared memory as two 64-bit words (two packed fp32 pairs).
+MXG_DEVINL void ld_shared_v2_u64(uint32_t addr, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
 MXG_DEVINL void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
@@ -284,6 +318,39 @@ MXG_DEVINL void mma_f8f6f4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t 
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+template <int kCta>
+MXG_DEVINL void mma_f8f6f4_g(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kCta == 1) mma_f8f6f4(d, adesc, bdesc, idesc, accumulate);
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic): a 64-bit register holds two
+// IEEE fp32 values (low word first); each lane is rounded like its scalar op.
+MXG_DEVINL uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+MXG_DEVINL uint64_t u32x2_pack(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+// acc = a * b + acc, per lane, round to nearest even
+MXG_DEVINL void fma_f32x2(uint64_t& acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+MXG_DEVINL uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
 // Each thread of the warp reads 32 consecutive 32-bit columns of its lane.

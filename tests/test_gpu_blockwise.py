@@ -30,6 +30,15 @@ def _mxg():
     return mxg
 
 
+@pytest.fixture(params=[2, 1], ids=["pair", "onesm"])
+def cta_group(request):
+    """GEMM cases run on the CTA-pair kernel (256 x 256 tiles, 2-SM MMA, the
+    default) and on the one-SM kernel (128 x 128 tiles)."""
+    prev = _mxg().set_gemm_cta_group(request.param)
+    yield request.param
+    _mxg().set_gemm_cta_group(prev)
+
+
 def _f32_dev(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda:0")
 
@@ -92,7 +101,7 @@ def _act_operand(bits):
 
 @pytest.mark.parametrize("splits,N,K", [([0, 130, 1, 300], 256, 384), ([512], 128, 128),
                                         ([64, 64], 384, 1024)])
-def test_bw_fwd_parity(splits, N, K):
+def test_bw_fwd_parity(splits, N, K, cta_group):
     mxg = _mxg()
     splits = np.asarray(splits, dtype=np.int32)
     G, S = len(splits), int(splits.sum())
@@ -107,7 +116,18 @@ def test_bw_fwd_parity(splits, N, K):
     oracle.assert_gemm_close(Y.float().cpu().numpy(), oracle.grouped_fwd(Ad, Wd, splits, N), "bw fwd")
 
 
-def test_bw_fwd_max_experts():
+def test_bw_fwd_many_tiles(cta_group):
+    """More tiles than CTA pairs (the persistent loop wraps several times),
+    ragged experts whose last 256-row pair has its odd CTA past the rows, and
+    N with a half-wide last column tile."""
+    rng = np.random.default_rng(77)
+    splits = rng.integers(100, 700, size=40).astype(np.int32)
+    splits[[3, 17]] = 0
+    splits[5] = 129
+    test_bw_fwd_parity(splits.tolist(), 640, 256, cta_group)
+
+
+def test_bw_fwd_max_experts(cta_group):
     """G = 512 (the largest supported), most experts empty, a few with rows:
     the plan's totals entry and the tile walk at the largest G."""
     rng = np.random.default_rng(512)
@@ -115,11 +135,12 @@ def test_bw_fwd_max_experts():
     live = rng.choice(512, size=24, replace=False)
     splits[live] = rng.integers(1, 200, size=24)
     splits[511] = 130                                   # the last expert non-empty
-    test_bw_fwd_parity(splits.tolist(), 128, 128)
+    test_bw_fwd_parity(splits.tolist(), 128, 128, cta_group)
 
 
-@pytest.mark.parametrize("splits,N,K", [([0, 77, 300], 256, 384), ([128], 128, 256)])
-def test_bw_dgrad_parity(splits, N, K):
+@pytest.mark.parametrize("splits,N,K", [([0, 77, 300], 256, 384), ([128], 128, 256),
+                                        ([400, 3, 0, 260], 384, 640)])
+def test_bw_dgrad_parity(splits, N, K, cta_group):
     mxg = _mxg()
     splits = np.asarray(splits, dtype=np.int32)
     G, S = len(splits), int(splits.sum())
@@ -149,11 +170,12 @@ def _col_operand(bits, splits, capacity):
 
 
 @pytest.mark.parametrize("accumulate", [False, True])
-def test_bw_wgrad_parity(accumulate):
+@pytest.mark.parametrize("N,K", [(256, 384), (384, 640)])
+def test_bw_wgrad_parity(accumulate, N, K, cta_group):
     mxg = _mxg()
     splits = np.array([200, 0, 1, 300, 129], dtype=np.int32)
-    G, S, N, K = len(splits), int(splits.sum()), 256, 384
-    rng = np.random.default_rng(11 + accumulate)
+    G, S = len(splits), int(splits.sum())
+    rng = np.random.default_rng(11 + accumulate + N)
     dy = synth.normal_bf16(rng, (S, N), outlier_frac=0.01)
     x = synth.normal_bf16(rng, (S, K), outlier_frac=0.01)
     cap = synth.padded_rows_capacity(S, G, 128)
@@ -168,7 +190,7 @@ def test_bw_wgrad_parity(accumulate):
     assert np.array_equal(got[1], init[1] if accumulate else np.zeros_like(init[1]))
 
 
-def test_bw_gemm_rejects_bad_splits():
+def test_bw_gemm_rejects_bad_splits(cta_group):
     mxg = _mxg()
     rng = np.random.default_rng(2)
     A, _ = _act_operand(synth.normal_bf16(rng, (128, 128)))
@@ -334,7 +356,7 @@ def test_bw_dual_rejects_bad_splits_and_writes_nothing():
     assert (q == 0xAB).all() and (s == 0xCD).all() and (qT == 0xAB).all() and (sT == 0xCD).all()
 
 
-def test_bw_bounded_wait_gives_up_cleanly():
+def test_bw_bounded_wait_gives_up_cleanly(cta_group):
     """The blockwise GEMM with an absurdly short wait limit either finishes or
     reports a timeout (its epilogue's bulk stores drained); the next normal
     call is correct."""
@@ -344,9 +366,9 @@ def test_bw_bounded_wait_gives_up_cleanly():
     try:
         lib.mxg_set_wait_timeout_ns(1)
         try:
-            test_bw_fwd_parity([0, 130, 1, 300], 256, 384)
+            test_bw_fwd_parity([0, 130, 1, 300], 256, 384, cta_group)
         except mxg.MXGError as e:
             assert e.code == 8
     finally:
         lib.mxg_set_wait_timeout_ns(old)
-    test_bw_fwd_parity([0, 130, 1, 300], 256, 384)
+    test_bw_fwd_parity([0, 130, 1, 300], 256, 384, cta_group)

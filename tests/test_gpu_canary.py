@@ -256,7 +256,7 @@ def test_mx_gemms_stay_inside_their_outputs(cta_group, kind, packed):
         out.check("dense out"), ws.check("dense workspace")
 
 
-def test_blockwise_gemms_stay_inside_their_outputs():
+def test_blockwise_gemms_stay_inside_their_outputs(cta_group):
     lib, mxg = _lib(), _mxg()
     N, K, G = 256, 384, len(SPLITS)
     sp = i32_to_dev(SPLITS)
