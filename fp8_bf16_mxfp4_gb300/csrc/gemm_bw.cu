@@ -426,6 +426,12 @@ struct PairSmem {
   static_assert(kTotal <= 232448, "fits the dynamic shared memory of one CTA");
 };
 
+// Two fp32 values packed in a 64-bit word (low first) -> BF16x2, round to nearest even.
+MXG_DEVINL uint32_t pack_bf16x2_u64(uint64_t a) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float((uint32_t)a), __uint_as_float((uint32_t)(a >> 32)));
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 template <bool kWgrad>
 __global__ void __launch_bounds__(kPThreads, 1)
     grouped_bw_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -641,23 +647,26 @@ __global__ void __launch_bounds__(kPThreads, 1)
       locate(tile, g, mt, nt, e);
       const int nk = e.Kc / 128;
       const int row0 = mt * 128 + quarter * 32;  // the warp's first row inside the expert
-      const int row = row0 + lane;
-      const int64_t arow = e.a_row0 + row;
-      const bool arow_ok = row < e.M && arow < bp.a_rows;
       const int col0 = nt * kPBN + chalf * 128;  // the warp's first column
       const bool col_ok = col0 < e.Nn;           // the last tile of an odd 128-column count is half wide
-      const int64_t akb0 = e.a_k0 / 128, bkb0 = e.b_k0 / 128;
-      const float* sa_col = bp.sA + arow;
-      const float* sb_row = bp.sB + (e.b_row0 / 128 + col0 / 128) * bp.sB_ld + bkb0;  // fwd / dgrad
+      const int64_t akb0 = e.a_k0 / 128;
+      const int64_t oy0 = e.out_row0 + row0;
+      const int vrows = e.M - row0;              // the warp's rows inside the expert (may be <= 0)
       uint64_t acc[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) acc[i] = 0;
+      // thread = row of the tile, 128 columns of it per warp
+      const int row = row0 + lane;
+      const int64_t arow = e.a_row0 + row;
+      const bool arow_ok = row < e.M && arow < bp.a_rows;
+      const float* sa_col = bp.sA + arow;
+      const float* sb_row = bp.sB + (e.b_row0 / 128 + col0 / 128) * bp.sB_ld + e.b_k0 / 128;  // fwd / dgrad
       // the scales of K blocks kb .. kb + kPScaleAhead - 1, loaded that many
       // blocks ahead of their use (a global load outlasts one K block)
       float saq[kPScaleAhead], sbq[kPScaleAhead];
       auto load_scales = [&](int k, float& a, float& bsc) {
         a = (k < nk && arow_ok) ? __ldg(sa_col + (akb0 + k) * bp.sA_ld) : 0.f;
-        bsc = (k < nk && !wg && col_ok) ? __ldg(sb_row + k) : 0.f;
+        bsc = (!wg && k < nk && col_ok) ? __ldg(sb_row + k) : 0.f;
       };
 #pragma unroll
       for (int j = 0; j < kPScaleAhead; ++j) load_scales(j, saq[j], sbq[j]);
@@ -669,7 +678,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const uint32_t b = kcount & 1u;
         const uint64_t sa2 = ptx::f32x2_pack(sa, sa);
         const uint64_t f2 = ptx::f32x2_pack(sa * sb, sa * sb);
-        // wgrad: the stage's column scales of this warp's 128 columns, as fp32 pairs
+        // wgrad: the K block's column scales of this warp's 128 columns, as fp32 pairs
         const int sj = (int)(kcount % kPSbSlots);
         const ulonglong2* sbc =
             reinterpret_cast<const ulonglong2*>(smem + L::kSbOff + sj * L::kSbBytes + chalf * 128 * 4);
@@ -712,20 +721,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
       }
       if (!ok) break;
-      const int vrows = e.M - row0;
       if (!col_ok || vrows <= 0 || (nk == 0 && p.accumulate)) continue;  // warp-uniform: nothing to write
       const bool full0 = vrows >= 16, full1 = vrows >= 32;
       const bool direct = row < e.M && !((lane >> 4) == 0 ? full0 : full1);
-      const int64_t oy0 = e.out_row0 + row0;
       const int64_t orow = e.out_row0 + row;
       if (p.out_dtype == MXG_OUT_BF16) {
         uint32_t h[64];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const uint32_t lo = (uint32_t)acc[i], hi = (uint32_t)(acc[i] >> 32);
-          const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
-          h[i] = *reinterpret_cast<const uint32_t*>(&v);
-        }
+        for (int i = 0; i < 64; ++i) h[i] = pack_bf16x2_u64(acc[i]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) send(h + 32 * c, col0 + 64 * c, oy0, full0, full1, false);
         if (direct) {
@@ -735,14 +738,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
       } else {
         const uint32_t* v = reinterpret_cast<const uint32_t*>(acc);
+        const bool reduce = wg && p.accumulate != 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) send(v + 32 * c, col0 + 32 * c, oy0, full0, full1, p.accumulate != 0);
+        for (int c = 0; c < 4; ++c) send(v + 32 * c, col0 + 32 * c, oy0, full0, full1, reduce);
         if (direct) {
           float* dst = static_cast<float*>(p.out) + orow * p.ld_out + col0;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             uint32_t w[8];
-            if (p.accumulate) {
+            if (reduce) {
               ptx::ld_global_v8(dst + 8 * i, w);
 #pragma unroll
               for (int j = 0; j < 8; ++j) w[j] = __float_as_uint(__uint_as_float(w[j]) + __uint_as_float(v[8 * i + j]));
