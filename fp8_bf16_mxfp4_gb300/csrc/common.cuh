@@ -40,6 +40,15 @@ MXG_DEVINL uint32_t bf16x2_absmax_bits(uint32_t w) {
   return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
 }
 
+// The same over a 32-value block (16 words): the two 16-bit magnitude lanes
+// are maxed side by side (unsigned 16-bit SIMD max) and folded at the end.
+MXG_DEVINL uint32_t bf16x32_absmax_bits(const uint32_t* w) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
+  return max(m & 0xFFFFu, m >> 16);
+}
+
 // MX shared exponent from a BF16 magnitude pattern (OCP MX v1.0 rule with the
 // -127 floor): floor(log2(amax)) - emax clamped to [-127, 127]; -127 for 0.
 // With `round_up` (the TransformerEngine recipe of the PR #745 review: amax /

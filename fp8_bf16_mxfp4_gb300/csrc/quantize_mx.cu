@@ -45,11 +45,18 @@ MXG_DEVINL int mx_exponent(uint32_t am, bool round_up) {
 // E2M1 -> one 32-bit word (8 nibbles); E4M3 -> two 32-bit words.
 template <int kElem>
 MXG_DEVINL void quantize8(const uint32_t* w, float sinv, uint32_t* out) {
+  // both values of a word scaled by one packed fp32 multiply (per-lane IEEE
+  // round to nearest, subnormals kept: the same results as two scalar products)
   float v[8];
+  uint64_t s2;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(sinv));
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    v[2 * i] = bf16lo_to_f32(w[i]) * sinv;
-    v[2 * i + 1] = bf16hi_to_f32(w[i]) * sinv;
+    uint64_t p;
+    asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tmul.rn.f32x2 %0, t, %3;\n\t}"
+        : "=l"(p)
+        : "r"(w[i] << 16), "r"(w[i] & 0xFFFF0000u), "l"(s2));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v[2 * i]), "=f"(v[2 * i + 1]) : "l"(p));
   }
   // The hardware conversions keep the sign of a value that rounds to zero
   // (E2M1 0x8, E4M3 0x80), as the OCP rule and the oracle do.
@@ -84,9 +91,7 @@ __global__ void __launch_bounds__(kRowThreads) mx_rowwise_kernel(
       const uint4 v = __ldcs(src + i);
       w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
     }
-    uint32_t am = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) am = max(am, bf16x2_absmax_bits(w[i]));
+    const uint32_t am = bf16x32_absmax_bits(w);
     const int e = mx_exponent<kElem>(am, round_up);
     const float sinv = pow2_neg(e);
     if constexpr (kElem == MXG_E2M1) {
@@ -212,9 +217,7 @@ __global__ void __launch_bounds__(kRowThreads) mx_rowwise_packed_kernel(
           const uint4 v = __ldcs(src + k);
           w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
         }
-        uint32_t am = 0;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) am = max(am, bf16x2_absmax_bits(w[k]));
+        const uint32_t am = bf16x32_absmax_bits(w);
         const int e = mx_exponent<kElem>(am, round_up);
         const float sinv = pow2_neg(e);
         if constexpr (kElem == MXG_E2M1) {
@@ -365,9 +368,7 @@ MXG_DEVINL void bw_quantize8(const uint32_t* w, float s, uint32_t* o) {
 // low half) and writes its codes and scale.
 template <int kElem>
 MXG_DEVINL void emit_col_block(const uint32_t* w, uint8_t* qrow, uint8_t* srow, bool round_up) {
-  uint32_t am = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) am = max(am, bf16x2_absmax_bits(w[i]));
+  const uint32_t am = bf16x32_absmax_bits(w);
   const int e = mx_exponent<kElem>(am, round_up);
   const float sinv = pow2_neg(e);
   if constexpr (kElem == MXG_E2M1) {
@@ -387,6 +388,56 @@ MXG_DEVINL void emit_col_block(const uint32_t* w, uint8_t* qrow, uint8_t* srow, 
     __stcs(reinterpret_cast<uint4*>(qrow) + 1, o1);
   }
   *srow = (uint8_t)(e + 127);
+}
+
+// Column-wise blocks of a column pair straight from the staged tile: T[t] is
+// the 32-bit word (column c in the low half, c + 1 in the high half) of token
+// t of the block.  Both columns' amax come from one 16-bit SIMD max per word,
+// and each value is widened from its half of T[t] in place, so the pair needs
+// no byte permutes.  kHi selects column c + 1.  Same results as emit_col_block
+// on the column's own words.
+template <int kElem, bool kHi>
+MXG_DEVINL void quantize8_col(const uint32_t* T, uint64_t s2, uint32_t* out) {
+  float v[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t a = kHi ? (T[2 * k] & 0xFFFF0000u) : (T[2 * k] << 16);
+    const uint32_t b = kHi ? (T[2 * k + 1] & 0xFFFF0000u) : (T[2 * k + 1] << 16);
+    uint64_t p;
+    asm("{\n\t.reg .b64 t;\n\tmov.b64 t, {%1, %2};\n\tmul.rn.f32x2 %0, t, %3;\n\t}" : "=l"(p) : "r"(a), "r"(b), "l"(s2));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v[2 * k]), "=f"(v[2 * k + 1]) : "l"(p));
+  }
+  if constexpr (kElem == MXG_E2M1) {
+    out[0] = cvt_e2m1x8(v);
+  } else {
+    out[0] = cvt_e4m3x4(v[0], v[1], v[2], v[3]);
+    out[1] = cvt_e4m3x4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+template <int kElem, bool kHi>
+MXG_DEVINL uint32_t emit_col_half(const uint32_t* T, uint32_t am, uint8_t* qrow, bool round_up) {
+  const int e = mx_exponent<kElem>(am, round_up);
+  uint64_t s2;
+  const float sinv = pow2_neg(e);
+  asm("mov.b64 %0, {%1, %1};" : "=l"(s2) : "f"(sinv));
+  if constexpr (kElem == MXG_E2M1) {
+    uint4 o;
+    quantize8_col<kElem, kHi>(&T[0], s2, &o.x);
+    quantize8_col<kElem, kHi>(&T[8], s2, &o.y);
+    quantize8_col<kElem, kHi>(&T[16], s2, &o.z);
+    quantize8_col<kElem, kHi>(&T[24], s2, &o.w);
+    __stcs(reinterpret_cast<uint4*>(qrow), o);
+  } else {
+    uint4 o0, o1;
+    quantize8_col<kElem, kHi>(&T[0], s2, &o0.x);
+    quantize8_col<kElem, kHi>(&T[8], s2, &o0.z);
+    quantize8_col<kElem, kHi>(&T[16], s2, &o1.x);
+    quantize8_col<kElem, kHi>(&T[24], s2, &o1.z);
+    __stcs(reinterpret_cast<uint4*>(qrow), o0);
+    __stcs(reinterpret_cast<uint4*>(qrow) + 1, o1);
+  }
+  return (uint32_t)(e + 127);
 }
 
 // One column's quarter (32 tokens, 16 words) of a 128-token blockwise block
@@ -540,13 +591,9 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
     const int64_t jb = (tile_id / ntc) * kColTokens + 32 * blk;
     const int64_t col = (tile_id % ntc) * kColCols + 2 * cp;
     const uint32_t* tp = tile + (32 * blk) * 64 + blk * 8 + cp;
-    uint32_t wa[16], wb[16];
+    uint32_t T[32];  // token t of the block: column col (low half), col + 1 (high half)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t t0 = tp[(2 * i) * 64], t1 = tp[(2 * i + 1) * 64];
-      wa[i] = __byte_perm(t0, t1, 0x5410);  // column col:   tokens 2i, 2i+1
-      wb[i] = __byte_perm(t0, t1, 0x7632);  // column col+1
-    }
+    for (int t = 0; t < 32; ++t) T[t] = tp[t * 64];
     if constexpr (kBw == 0) {
       if (jb < ptot && col < cols) {  // beyond the last expert: nothing written
         const int64_t qoff = (jb >> 5) * kBytesPerBlock;
@@ -565,18 +612,25 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
           sa = s8 + col * ld_s + (jb >> 5);
           sb = s8 + (col + 1) * ld_s + (jb >> 5);
         }
-        emit_col_block<kElem>(wa, qT + col * ld_q + qoff, sa, round_up);
-        if (col + 1 < cols) emit_col_block<kElem>(wb, qT + (col + 1) * ld_q + qoff, sb, round_up);
+        uint32_t m = 0;
+#pragma unroll
+        for (int t = 0; t < 32; ++t) m = __vmaxu2(m, T[t] & 0x7FFF7FFFu);
+        *sa = (uint8_t)emit_col_half<kElem, false>(T, m & 0xFFFFu, qT + col * ld_q + qoff, round_up);
+        if (col + 1 < cols) *sb = (uint8_t)emit_col_half<kElem, true>(T, m >> 16, qT + (col + 1) * ld_q + qoff, round_up);
       }
     } else {
-      // the 128-token block's amax over the four quarter lanes (all lanes
-      // take part; validity is uniform per warp: cols % 32 == 0, ptot % 128 == 0)
-      uint32_t ama = 0, amb = 0;
+      uint32_t wa[16], wb[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        ama = max(ama, bf16x2_absmax_bits(wa[i]));
-        amb = max(amb, bf16x2_absmax_bits(wb[i]));
+        wa[i] = __byte_perm(T[2 * i], T[2 * i + 1], 0x5410);  // column col:   tokens 2i, 2i+1
+        wb[i] = __byte_perm(T[2 * i], T[2 * i + 1], 0x7632);  // column col+1
       }
+      // the 128-token block's amax over the four quarter lanes (all lanes
+      // take part; validity is uniform per warp: cols % 32 == 0, ptot % 128 == 0)
+      uint32_t m = 0;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) m = __vmaxu2(m, T[t] & 0x7FFF7FFFu);
+      uint32_t ama = m & 0xFFFFu, amb = m >> 16;
       ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 1));
       ama = max(ama, __shfl_xor_sync(0xffffffffu, ama, 2));
       amb = max(amb, __shfl_xor_sync(0xffffffffu, amb, 1));
@@ -681,9 +735,7 @@ __global__ void __launch_bounds__(kRowThreads) bw_rowwise_kernel(
 #pragma unroll
       for (int i = 0; i < 16; ++i) w[i] = 0;
     }
-    uint32_t am = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) am = max(am, bf16x2_absmax_bits(w[i]));
+    uint32_t am = bf16x32_absmax_bits(w);
     am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
     am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
     if (!live) continue;
@@ -742,9 +794,7 @@ __global__ void __launch_bounds__(256, kWCtasPerSm) bw_weight_kernel(
   load(id, v);
   for (; id < ntiles; id += gridDim.x) {
     const int64_t rb = id / nkb, kb = id - rb * nkb;
-    uint32_t am = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) am = max(am, bf16x2_absmax_bits(v[i]));
+    uint32_t am = max(bf16x32_absmax_bits(v), bf16x32_absmax_bits(v + 16));
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) am = max(am, __shfl_xor_sync(0xffffffffu, am, d));
     if ((t & 31) == 0) warp_max[t >> 5] = am;
