@@ -462,18 +462,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t tsf = tmem + kSfTmemCol0 + stage * KC::kSlotCols;  // A: kKPS*4 cols, then B
           const uint64_t adesc0 = ptx::smem_desc(sA, 16, 1024, 2);
           const uint64_t bdesc0 = ptx::smem_desc(sB, 16, 1024, 2);
-          for (int j = 0; j < steps; ++j) {
-            const int kel = j * KC::kMmaK;  // element offset inside the stage
-            const int c = kel >> 7;
-            const uint32_t sfid = (uint32_t)((kel & 127) >> 5);
-            const uint32_t idesc = p.idesc | (sfid << 4) | (sfid << 29);
-            const uint64_t adv = (uint64_t)((j * 32) >> 4);  // 32 bytes of K per MMA
-            const uint32_t sfa = tsf + 4 * c;
-            const uint32_t sfb = tsf + KC::kKPS * 4 + 8 * c;
-            if constexpr (kKind == KIND_MXF4)
-              ptx::mma_mxf4_g<kCta>(dacc, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
-            else
-              ptx::mma_mxf8f6f4_g<kCta>(dacc, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+          // unrolled (straight-line issue); the steps past a K tail are skipped
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j < steps) {
+              constexpr int kMmaK = KC::kMmaK;
+              const int kel = j * kMmaK;  // element offset inside the stage
+              const int c = kel >> 7;
+              const uint32_t sfid = (uint32_t)((kel & 127) >> 5);
+              const uint32_t idesc = p.idesc | (sfid << 4) | (sfid << 29);
+              const uint64_t adv = (uint64_t)((j * 32) >> 4);  // 32 bytes of K per MMA
+              const uint32_t sfa = tsf + 4 * c;
+              const uint32_t sfb = tsf + KC::kKPS * 4 + 8 * c;
+              if constexpr (kKind == KIND_MXF4)
+                ptx::mma_mxf4_g<kCta>(dacc, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+              else
+                ptx::mma_mxf8f6f4_g<kCta>(dacc, adesc0 + adv, bdesc0 + adv, idesc, sfa, sfb, (kb | j) != 0);
+            }
           }
           issued = true;
           ptx::tc_commit_pair<kCta>(empty_bar(stage));
