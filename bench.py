@@ -269,7 +269,7 @@ class A8W4Forward:
     dtype = "mxf8f6f4 (e4m3 x e2m1, fp32 accumulate)"
     # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
     # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
-    traffic_bytes = {"fwd": 284397312 + 210236672}
+    traffic_bytes = {"fwd": 284359680 + 210250240}
 
     def check(self):
         self.mxg.check_status(self.status)
@@ -282,8 +282,8 @@ class MXFP4Train:
     elem = "e2m1"
     # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
     # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
-    traffic_bytes = {"fwd": 777739264 + 509565696, "dgrad": 399596544 + 1818053120,
-                     "wgrad": 2886021632 + 1842235136}
+    traffic_bytes = {"fwd": 778252544 + 509844992, "dgrad": 399162368 + 1817635840,
+                     "wgrad": 2904818176 + 1843764480}
 
     def __init__(self, dev):
         import torch
@@ -379,9 +379,9 @@ class DenseMXFP4:
     call_kernels = "plan + tcgen05 GEMM; scales arrive packed"
     # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
     # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
-    traffic_bytes = {"fwd_bf16": 226694400 + 441006336, "fwd_f32": 393862656 + 897122560,
-                     "dgrad_bf16": 1026101504 + 121138944, "dgrad_f32": 1064483328 + 244952064,
-                     "wgrad_bf16": 336168960 + 430054400, "wgrad_f32": 489614592 + 889742592}
+    traffic_bytes = {"fwd_bf16": 228091392 + 441148928, "fwd_f32": 408301568 + 897167616,
+                     "dgrad_bf16": 1027663104 + 121481728, "dgrad_f32": 1066215680 + 245309696,
+                     "wgrad_bf16": 335457280 + 429426688, "wgrad_f32": 492259072 + 888988672}
 
     def __init__(self, dev):
         import torch
@@ -481,15 +481,17 @@ class DenseMXFP4:
 class DenseMXFP4M2048(DenseMXFP4):
     M = 2048
     name = "dense_mxfp4_m2048"
-    traffic_bytes = {"fwd_bf16": 133869056 + 85080832, "fwd_f32": 135900672 + 183673600,
-                     "dgrad_bf16": 217267968 + 20288512, "dgrad_f32": 233902336 + 41399296,
-                     "wgrad_bf16": 101201152 + 416596224, "wgrad_f32": 282469120 + 879962368}
+    traffic_bytes = {"fwd_bf16": 133881600 + 85341952, "fwd_f32": 135824128 + 183774464,
+                     "dgrad_bf16": 217504256 + 20405248, "dgrad_f32": 234043904 + 41545472,
+                     "wgrad_bf16": 109113856 + 416793856, "wgrad_f32": 284508928 + 879964928}
 
 
 class DenseMXFP4M4096(DenseMXFP4):
     M = 4096
     name = "dense_mxfp4_m4096"
-    traffic_bytes = {}    # not captured at this size
+    traffic_bytes = {"fwd_bf16": 144382464 + 198078720, "fwd_f32": 161155840 + 418041600,
+                     "dgrad_bf16": 481953280 + 55052288, "dgrad_f32": 502846464 + 113492224,
+                     "wgrad_bf16": 137751808 + 420025856, "wgrad_f32": 294193152 + 885810944}
 
 
 class MXFP8Train(MXFP4Train):
@@ -497,8 +499,8 @@ class MXFP8Train(MXFP4Train):
     three passes (kind::mxf8f6f4)."""
     name = "mxfp8_moe_train"
     elem = "e4m3"
-    traffic_bytes = {"fwd": 1775431680 + 518178304, "dgrad": 817078784 + 1830243328,
-                     "wgrad": 3336232960 + 1853860352}
+    traffic_bytes = {"fwd": 1795971840 + 518586112, "dgrad": 817723904 + 1828735488,
+                     "wgrad": 3288670976 + 1853220864}
 
     def __init__(self, dev):
         super().__init__(dev)
@@ -598,8 +600,8 @@ class BlockwiseFP8Pow2(BlockwiseFP8):
     passes run on the block-scaled MX GEMMs, with no promotion."""
     call_kernels = "plan + scale pack + tcgen05 GEMM"
     name = "blockwise_fp8_pow2"
-    traffic_bytes = {"fwd": 738866944 + 250812672, "dgrad": 623788800 + 436206848,
-                     "wgrad": 404199936 + 883418880}
+    traffic_bytes = {"fwd": 741398784 + 251155456, "dgrad": 623524352 + 436278528,
+                     "wgrad": 403493888 + 882491648}
 
     def __init__(self, dev):
         import torch
