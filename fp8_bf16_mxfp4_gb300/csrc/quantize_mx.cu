@@ -509,6 +509,9 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
   __shared__ SegTable tab;
   __shared__ __align__(16) uint32_t tile[kColTokens * (kColCols / 2) + 4 * 8];
   __shared__ int64_t src_row[2][kColTokens];  // source row of each position, or -1
+  // kPacked: per 32-token block of the tile, its chunk-grid offset
+  // (k-chunk * row tiles * 512 + block in the chunk), found once per tile
+  __shared__ int64_t blk_off[2][kColTokens / 32];
   __shared__ int32_t kcp[kMaxExperts + 1];     // kPacked: first k-chunk of each expert
   const bool first = blockIdx.x == 0;
   if (!build_seg_table(tab, splits, G, rows, pad, capacity, status, first)) return;
@@ -552,6 +555,12 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
       if (tok < tab.off[g + 1] - tab.off[g]) sr = tab.off[g] + tok;
     }
     src_row[buf][threadIdx.x] = sr;
+    if constexpr (kPacked) {
+      if ((threadIdx.x & 31) == 0 && g >= 0) {
+        const int64_t lb = (j - tab.poff[g]) >> 5;  // the expert's local 32-block
+        blk_off[buf][threadIdx.x >> 5] = ((int64_t)kcp[g] + (lb >> 2)) * ((cols + 127) >> 7) * 512 + (lb & 3);
+      }
+    }
   };
   auto load = [&](int64_t t, int buf, uint4* v) {
     const int64_t c0 = (t % ntc) * kColCols;
@@ -600,12 +609,8 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
         uint8_t* s8 = static_cast<uint8_t*>(sT);
         uint8_t *sa, *sb;
         if constexpr (kPacked) {
-          const int g = find_segment(tab, G, jb);      // jb < ptot: a valid expert
-          const int64_t lb = (jb - tab.poff[g]) >> 5;   // the expert's local 32-block
-          const int64_t kc = kcp[g] + (lb >> 2);
-          const int64_t rtn = (cols + 127) >> 7;
           const int i0 = (int)(col & 127);              // col even: col + 1 is in the same row tile
-          uint8_t* cb = s8 + (kc * rtn + (col >> 7)) * 512 + (lb & 3);
+          uint8_t* cb = s8 + blk_off[buf][blk] + (col >> 7) * 512;
           sa = cb + (i0 & 31) * 16 + (i0 >> 5) * 4;
           sb = cb + ((i0 + 1) & 31) * 16 + ((i0 + 1) >> 5) * 4;
         } else {
