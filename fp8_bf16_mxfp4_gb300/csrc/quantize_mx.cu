@@ -546,8 +546,16 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
   int64_t tile_id = blockIdx.x;
   if (tile_id >= ntiles) return;
 
-  auto fill_src = [&](int64_t t, int buf) {  // threads < kColTokens
-    const int64_t j = (t / ntc) * kColTokens + threadIdx.x;
+  // tile = token tile tt * ntc + column tile tc; the pair is advanced by the
+  // grid stride without dividing
+  const int64_t gq = gridDim.x / ntc, gr = gridDim.x % ntc;
+  auto advance = [&](int64_t& tt, int64_t& tc) {
+    tt += gq;
+    tc += gr;
+    if (tc >= ntc) { tc -= ntc; ++tt; }
+  };
+  auto fill_src = [&](int64_t tt, int buf) {  // threads < kColTokens
+    const int64_t j = tt * kColTokens + threadIdx.x;
     int64_t sr = -1;
     const int g = find_segment(tab, G, j);
     if (g >= 0) {
@@ -562,8 +570,8 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
       }
     }
   };
-  auto load = [&](int64_t t, int buf, uint4* v) {
-    const int64_t c0 = (t % ntc) * kColCols;
+  auto load = [&](int64_t tc, int buf, uint4* v) {
+    const int64_t c0 = tc * kColCols;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int idx = threadIdx.x + kColThreads * i;
@@ -576,9 +584,10 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
   };
 
   uint4 v[8];
-  if (threadIdx.x < kColTokens) fill_src(tile_id, 0);
+  int64_t cur_tt = tile_id / ntc, cur_tc = tile_id % ntc;
+  if (threadIdx.x < kColTokens) fill_src(cur_tt, 0);
   __syncthreads();
-  load(tile_id, 0, v);
+  load(cur_tc, 0, v);
   int buf = 0;
   const int lane = threadIdx.x & 31;
   const int cp = (threadIdx.x >> 5) * 8 + (lane >> 2);  // column pair 0..63
@@ -586,7 +595,9 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
   constexpr int kBytesPerBlock = kElem == MXG_E2M1 ? 16 : 32;
   for (; tile_id < ntiles; tile_id += gridDim.x) {
     const int64_t next = tile_id + gridDim.x;
-    if (next < ntiles && threadIdx.x < kColTokens) fill_src(next, buf ^ 1);
+    int64_t nxt_tt = cur_tt, nxt_tc = cur_tc;
+    advance(nxt_tt, nxt_tc);
+    if (next < ntiles && threadIdx.x < kColTokens) fill_src(nxt_tt, buf ^ 1);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int idx = threadIdx.x + kColThreads * i;
@@ -595,10 +606,10 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
       *reinterpret_cast<uint4*>(&tile[jr * 64 + (jr >> 5) * 8 + (cc >> 1)]) = v[i];
     }
     __syncthreads();  // tile and the next tile's source rows are visible
-    if (next < ntiles) load(next, buf ^ 1, v);
+    if (next < ntiles) load(nxt_tc, buf ^ 1, v);
 
-    const int64_t jb = (tile_id / ntc) * kColTokens + 32 * blk;
-    const int64_t col = (tile_id % ntc) * kColCols + 2 * cp;
+    const int64_t jb = cur_tt * kColTokens + 32 * blk;
+    const int64_t col = cur_tc * kColCols + 2 * cp;
     const uint32_t* tp = tile + (32 * blk) * 64 + blk * 8 + cp;
     uint32_t T[32];  // token t of the block: column col (low half), col + 1 (high half)
 #pragma unroll
@@ -649,7 +660,7 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
     if constexpr (kDual && kBw != 0) {
       // row-wise 1x128 blocks: warp w takes tile rows 16*it + 2w + (lane >> 4);
       // lane & 15 is the row's 16-byte chunk (8 columns)
-      const int64_t c0 = (tile_id % ntc) * kColCols;  // cols % 128 == 0: the block is the whole tile row
+      const int64_t c0 = cur_tc * kColCols;  // cols % 128 == 0: the block is the whole tile row
       const int sub = lane >> 4, ch = lane & 15, wid = threadIdx.x >> 5;
 #pragma unroll 2
       for (int it = 0; it < kColTokens / 16; ++it) {
@@ -684,7 +695,7 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
 #pragma unroll
         for (int bb = 0; bb < 2; ++bb) {
           const int b = 2 * (threadIdx.x & 1) + bb;
-          const int64_t colb = (tile_id % ntc) * kColCols + 32 * b;
+          const int64_t colb = cur_tc * kColCols + 32 * b;
           if (colb < cols) {
             const uint4* rp = reinterpret_cast<const uint4*>(tile + rr * 64 + (rr >> 5) * 8 + 16 * b);
             uint32_t w[16];
@@ -701,6 +712,8 @@ __global__ void __launch_bounds__(kColThreads, kColCtasPerSm) mx_colwise_kernel(
     }
     __syncthreads();  // the tile buffer is rewritten next iteration
     buf ^= 1;
+    cur_tt = nxt_tt;
+    cur_tc = nxt_tc;
   }
 }
 
