@@ -22,9 +22,9 @@
 //      range) starting on a fresh chunk -- the "scale packing" step that the
 //      HipKittens grouped MXFP8 kernel (PR #661) also performs.  Skipped for
 //      an operand whose quantizer already wrote that order (packed scales).
-//   3. the persistent GEMM kernel, one CTA per SM, 320 threads:
-//        warp 0    TMA producer: A/B data tiles (128-byte swizzle) and scale
-//                  chunks into a 4-stage shared-memory ring (mbarriers);
+//   3. the persistent GEMM kernel, one CTA per SM, 352 threads:
+//        warp 0    TMA producer: A/B data tiles (128-byte swizzle) into a
+//                  4-stage shared-memory ring (mbarriers);
 //        warp 1    TMEM owner and MMA issuer (one thread): 4 tcgen05.mma per
 //                  stage (kind::mxf4 for MXFP4, kind::mxf8f6f4 for MXFP8 /
 //                  a8w4) accumulating a 128x256 fp32 tile in TMEM;
@@ -34,7 +34,9 @@
 //        warps 6-9 scale feeders, one per 32-lane quarter of TMEM: each
 //                  stage's scale chunks go from shared memory to registers
 //                  and on into that stage's TMEM scale slot (tcgen05.st),
-//                  then the stage is handed to the MMA issuer.
+//                  then the stage is handed to the MMA issuer;
+//        warp 10   second producer: the stage's scale chunks (TMA / bulk
+//                  copies onto the same barrier).
 //      The feeders keep every tcgen05.cp out of the MMA issuer's stream:
 //      measured on GB300, a scale copy issued between MMAs (3 per FP8 stage,
 //      6 per FP4 stage) slowed the MMA stream by a third to two thirds, and
@@ -66,7 +68,7 @@ namespace {
 
 constexpr int BM = 128;           // tile rows of one CTA (TMEM lanes)
 constexpr int BN = 256;           // tile columns (TMEM fp32 columns)
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kATileBytes = BM * 128;  // 128 bytes of K per row per stage
 constexpr int kChunkBytes = 512;       // 128 rows x 4 scale bytes
 constexpr int kTmemCols = 512;
@@ -238,7 +240,7 @@ struct Cfg {
   static constexpr int kDataBytes = kStages * kStageBytes;
   static constexpr int kSfOff = kDataBytes;
   static constexpr int kBarOff = kSfOff + kStages * kSfBytes;
-  static constexpr int kNumBars = 3 * kStages + 3;  // full, empty, sready per stage; tmem_full, tmem_empty, drain
+  static constexpr int kNumBars = 4 * kStages + 3;  // full, empty, sready, sgo per stage; tmem_full, tmem_empty, drain
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem addr, abort flag
   // epilogue staging: one buffer per epilogue warp, 1024-byte aligned (swizzle atoms)
   static constexpr int kEpiOff = (kMiscOff + 16 + 1023) & ~1023;
@@ -315,7 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto sready_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); };  // scales in TMEM
-  const uint32_t tmem_full = bar0 + 8u * (3 * kStages);
+  auto sgo_bar = [&](int s) { return bar0 + 8u * (3 * kStages + s); };     // stage armed: load its scales
+  const uint32_t tmem_full = bar0 + 8u * (4 * kStages);
   const uint32_t tmem_empty = tmem_full + 8;
   const uint32_t drain_bar = tmem_full + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -331,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
       ptx::mbar_init(sready_bar(s), 4 * kCta);  // the feeder warps of every CTA of the group
+      ptx::mbar_init(sgo_bar(s), 1);
     }
     ptx::mbar_init(tmem_full, 1);
     ptx::mbar_init(tmem_empty, 4 * kCta);       // the epilogue warps of every CTA of the group
@@ -367,18 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Per stage: the A and B tiles (TMA), the B scale chunks of the stage's
-    // k-chunks (one TMA load of whole 512-byte chunks through a map over the
-    // packed scales), and the A scale chunks -- one TMA load when the A
-    // operand's row-tile count is fixed (wgrad), otherwise one bulk copy per
-    // k-chunk (the row-tile count of a row-segmented A is only known on the
-    // device).  Chunks past the operand are zero-filled; chunks of a
-    // neighbouring expert or a k tail carry scales that no stored output uses.
+    // Per stage: the A and B tiles (TMA), and the expected byte count of the
+    // whole stage -- tiles and scale chunks, which warp 10 loads onto the same
+    // barrier (a copy issue costs the issuing thread ~100 clocks, and five of
+    // them per stage took one thread longer than the stage's MMAs).
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_phase = 0;  // per stage: a load was issued / its phase
-      const int rtA = p.pass == MXG_PASS_WGRAD ? p.rtA_fixed : pv.rt[G];
       bool ok = true;
       for (int tile = unit; tile < total_tiles && ok; tile += units) {
         int g, mt, nt;
@@ -391,8 +391,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool a_in = mt * BM < e.M;
         const int ya = (int)(e.a_row0 + (int64_t)mt * BM);
         const int yb = (int)(e.b_row0 + (int64_t)nt * BN + (int64_t)rank * L::kBRows);
-        const int qb = e.b_rt0 + ((nt * BN) >> 7);  // the B tile's first 128-row scale chunk
-        const uint8_t* srcA0 = p.packA + ((int64_t)e.a_kc0 * rtA + e.a_rt0 + mt) * kChunkBytes;
         for (int kb = 0; kb < nk; ++kb) {
           if (!ptx::mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
           const int kc_valid = min(KC::kKPS, cdiv_d(e.Kc - kb * KC::kStageK, 128));
@@ -403,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t bytes = (a_in ? kATileBytes : 0) + kBTx + a_sf + KC::kKPS * L::kBChunks * kChunkBytes;
           const uint32_t fb = full_bar(stage);
           ptx::mbar_arrive_expect_tx(fb, bytes);
+          ptx::mbar_arrive(sgo_bar(stage));  // warp 10 loads the stage's scales
           armed |= 1u << stage;
           armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           const uint32_t sA = sbase + stage * L::kStageBytes;
@@ -411,20 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t kbk = e.b_k0 + (int64_t)kb * KC::kStageK;
           const int xa = kKind == KIND_MXF4 ? (int)(ka >> 1) : (int)ka;
           const int xb = kKind == KIND_MXF4 ? (int)(kbk >> 1) : (int)kbk;
-          const uint32_t sf = sbase + L::kSfOff + stage * L::kSfBytes;
-          const int kc0 = kb * KC::kKPS;
           if (a_in) ptx::tma_load_2d(sA, &tmA, xa, ya, fb);
           ptx::tma_load_2d(sB, &tmB, xb, yb, fb);
-          // B scales: chunks (kc, qb .. qb+1) for the stage's k-chunks, kc-major
-          ptx::tma_load_3d(sf + KC::kKPS * kChunkBytes, &tmSB, 0, qb, e.b_kc0 + kc0, fb);
-          if (a_in) {
-            if (p.a_scale_tma) {
-              ptx::tma_load_3d(sf, &tmSA, 0, e.a_rt0 + mt, e.a_kc0 + kc0, fb);
-            } else {
-              for (int c = 0; c < kc_valid; ++c)
-                ptx::bulk_load(sf + c * kChunkBytes, srcA0 + (int64_t)(kc0 + c) * rtA * kChunkBytes, kChunkBytes, fb);
-            }
-          }
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -494,6 +481,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_wait(drain_bar, 0, &no_abort, p.status, p.drain_ns);
       }
     }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ scale loads
+    // Per stage, once warp 0 has armed the stage's full barrier with the
+    // stage's whole byte count (so that warp 0's final wait on every armed
+    // stage covers these copies too): the B scale chunks of the stage's k-chunks (one TMA load of
+    // whole 512-byte chunks through a map over the packed scales), and the A
+    // scale chunks -- one TMA load when the A operand's row-tile count is
+    // fixed (wgrad), otherwise one bulk copy per k-chunk (the row-tile count
+    // of a row-segmented A is only known on the device).  Chunks past the
+    // operand are zero-filled; chunks of a neighbouring expert or a k tail
+    // carry scales that no stored output uses.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      const int rtA = p.pass == MXG_PASS_WGRAD ? p.rtA_fixed : pv.rt[G];
+      bool ok = true;
+      for (int tile = unit; tile < total_tiles && ok; tile += units) {
+        int g, mt, nt;
+        Geo e;
+        locate(tile, g, mt, nt, e);
+        const int nk = cdiv_d(e.Kc, KC::kStageK);
+        const bool a_in = mt * BM < e.M;
+        const int qb = e.b_rt0 + ((nt * BN) >> 7);  // the B tile's first 128-row scale chunk
+        const uint8_t* srcA0 = p.packA + ((int64_t)e.a_kc0 * rtA + e.a_rt0 + mt) * kChunkBytes;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!ptx::mbar_wait(sgo_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+          const int kc_valid = min(KC::kKPS, cdiv_d(e.Kc - kb * KC::kStageK, 128));
+          const uint32_t fb = full_bar(stage);
+          const uint32_t sf = sbase + L::kSfOff + stage * L::kSfBytes;
+          const int kc0 = kb * KC::kKPS;
+          // B scales: chunks (kc, qb .. qb+1) for the stage's k-chunks, kc-major
+          ptx::tma_load_3d(sf + KC::kKPS * kChunkBytes, &tmSB, 0, qb, e.b_kc0 + kc0, fb);
+          if (a_in) {
+            if (p.a_scale_tma) {
+              ptx::tma_load_3d(sf, &tmSA, 0, e.a_rt0 + mt, e.a_kc0 + kc0, fb);
+            } else {
+              for (int c = 0; c < kc_valid; ++c)
+                ptx::bulk_load(sf + c * kChunkBytes, srcA0 + (int64_t)(kc0 + c) * rtA * kChunkBytes, kChunkBytes, fb);
+            }
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
   } else if (warp >= 6) {
     // ------------------------------------------------------------ scale feeders
     // A stage's scale chunks (the A chunk of each k-chunk, then the two B
@@ -541,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
     }
   } else {
-    // ------------------------------------------------------------ epilogue
+    // ------------------------------------------------------------ epilogue (warps 2-5)
     // Warp q owns TMEM lane quarter q: rows q*32 .. q*32+31 of the tile.  The
     // output goes out through the warp's staging buffer: two 16-row boxes of
     // 128 bytes per row (64 BF16 / 32 FP32 columns) in the TMA 128-byte
