@@ -581,13 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // leaves the SM as whole lines instead of one 32-byte piece per row and
     // lane.  A box only partly inside the expert's rows is written by the
     // lanes of its valid rows directly; columns past the output's last are
-    // clipped by the map.  TMEM is handed back
-    // right after its last read: BF16 first reads the whole tile into
-    // registers (BN/2 packed words per thread), so that the buffer waits come
-    // after the hand-back; FP32 keeps the first half of its row in registers
-    // and copies the second half into TMEM columns that no MMA or scale slot
-    // uses, then hands back and writes both halves out while the next tile's
-    // MMAs run.
+    // clipped by the map.  TMEM is handed back right after its last read:
+    // BF16 copies the second half of its row into TMEM columns that no MMA or
+    // scale slot uses and reads the first half into registers as packed
+    // pairs; FP32 copies the second half the same way and keeps the first
+    // half in registers; either then hands back and writes both halves out
+    // while the next tile's MMAs run.
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const uint32_t tlane0 = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t ebuf = sbase + (uint32_t)(L::kEpiOff + quarter * kEpiWarpBytes);
@@ -652,35 +651,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       if (p.out_dtype == MXG_OUT_BF16) {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * p.ld_out + col0;
-        auto store_direct = [&](int c4, const uint32_t* v) {  // 64 columns of this lane's row
-          ptx::st_global_v8(dst + c4 * 64, v);
-          ptx::st_global_v8(dst + c4 * 64 + 16, v + 8);
-          if (c4 * 64 + 32 < ncols) {
-            ptx::st_global_v8(dst + c4 * 64 + 32, v + 16);
-            ptx::st_global_v8(dst + c4 * 64 + 48, v + 24);
+        // Hand-off: accumulator columns 128..255 are copied to the stash columns
+        // and columns 0..127 read and packed into registers, 64 columns (two
+        // loads) per load wait; TMEM is then handed back and the write-out
+        // overlaps the next tile's MMAs.  The store wait sits before the
+        // second half's loads: the compiler holds a tcgen05.st's source
+        // registers until it, and after the hand-back they would spill.  An
+        // empty contraction never wrote the accumulator: its output is zeros
+        // and the stash is unused.
+        constexpr int kHalf = BN / 2;
+        uint32_t hb[kHalf / 2];  // columns 0..127 of this lane's row as packed BF16 pairs
+        if (e.Kc > 0) {
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t f[64];
+            ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(kHalf + q * 64), f);
+            ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(kHalf + q * 64 + 32), f + 32);
+            ptx::tmem_ld_wait();
+            ptx::tmem_st_32x32b_x32(tlane0 + (uint32_t)(kStashCol + q * 64), f);
+            ptx::tmem_st_32x32b_x32(tlane0 + (uint32_t)(kStashCol + q * 64 + 32), f + 32);
           }
-        };
-        uint32_t h[BN / 2];
+          ptx::tmem_st_wait();
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          if (c < nch) {
-            uint32_t r[32];
-            read_chunk(tlane + (uint32_t)(c * 32), r);
+          for (int q = 0; q < 2; ++q) {
+            uint32_t f[64];
+            ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(q * 64), f);
+            ptx::tmem_ld_32x32b_x32(tlane + (uint32_t)(q * 64 + 32), f + 32);
+            ptx::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) h[c * 16 + i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) h[c * 16 + i] = 0;
+            for (int i = 0; i < 32; ++i) hb[q * 32 + i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
           }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kHalf / 2; ++i) hb[i] = 0;
         }
         release();
         if (!skip_out) {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + orow * p.ld_out + col0;
+          auto out64 = [&](int c4, const uint32_t* h) {  // 64 columns as packed BF16 pairs, staged and sent
+            send(h, col0 + c4 * 64, oy0, full0, full1, false);
+            if (direct) {  // this lane's row, written by the lane itself
+              ptx::st_global_v8(dst + c4 * 64, h);
+              ptx::st_global_v8(dst + c4 * 64 + 16, h + 8);
+              if (c4 * 64 + 32 < ncols) {
+                ptx::st_global_v8(dst + c4 * 64 + 32, h + 16);
+                ptx::st_global_v8(dst + c4 * 64 + 48, h + 24);
+              }
+            }
+          };
 #pragma unroll
-          for (int c4 = 0; c4 < BN / 64; ++c4) {
-            if (c4 * 64 < ncols) {  // warp-uniform
-              send(&h[c4 * 32], col0 + c4 * 64, oy0, full0, full1, false);
-              if (direct) store_direct(c4, &h[c4 * 32]);
+          for (int c4 = 0; c4 < kHalf / 64; ++c4)
+            if (c4 * 64 < ncols) out64(c4, hb + c4 * 32);  // warp-uniform
+#pragma unroll 1
+          for (int c4 = kHalf / 64; c4 < BN / 64; ++c4) {
+            if (c4 * 64 < ncols) {
+              uint32_t r[64];
+              if (e.Kc > 0) {
+                __syncwarp();
+                ptx::tmem_ld_32x32b_x32(tlane0 + (uint32_t)(kStashCol + (2 * c4 - kHalf / 32) * 32), r);
+                ptx::tmem_ld_32x32b_x32(tlane0 + (uint32_t)(kStashCol + (2 * c4 + 1 - kHalf / 32) * 32), r + 32);
+                ptx::tmem_ld_wait();
+              } else {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) r[i] = 0;
+              }
+              uint32_t h[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) h[i] = pack_bf16x2(r[2 * i], r[2 * i + 1]);
+              out64(c4, h);
             }
           }
         }
