@@ -269,7 +269,7 @@ class A8W4Forward:
     dtype = "mxf8f6f4 (e4m3 x e2m1, fp32 accumulate)"
     # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
     # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
-    traffic_bytes = {"fwd": 284359680 + 210250240}
+    traffic_bytes = {"fwd": 284407296 + 212500736}
 
     def check(self):
         self.mxg.check_status(self.status)
@@ -282,8 +282,8 @@ class MXFP4Train:
     elem = "e2m1"
     # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
     # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
-    traffic_bytes = {"fwd": 778252544 + 509844992, "dgrad": 399162368 + 1817635840,
-                     "wgrad": 2904818176 + 1843764480}
+    traffic_bytes = {"fwd": 768069888 + 508036352, "dgrad": 396351232 + 1817983232,
+                     "wgrad": 2797496064 + 1840005888}
 
     def __init__(self, dev):
         import torch
@@ -379,9 +379,9 @@ class DenseMXFP4:
     call_kernels = "plan + tcgen05 GEMM; scales arrive packed"
     # DRAM bytes (read + write) of one GEMM call per pass, counted by ncu on
     # GB300 for the current kernels (dram__bytes_read.sum + dram__bytes_write.sum).
-    traffic_bytes = {"fwd_bf16": 228091392 + 441148928, "fwd_f32": 408301568 + 897167616,
-                     "dgrad_bf16": 1027663104 + 121481728, "dgrad_f32": 1066215680 + 245309696,
-                     "wgrad_bf16": 335457280 + 429426688, "wgrad_f32": 492259072 + 888988672}
+    traffic_bytes = {"fwd_bf16": 225919488 + 440607744, "fwd_f32": 434404096 + 896570112,
+                     "dgrad_bf16": 1032064768 + 120869120, "dgrad_f32": 1069566976 + 244512768,
+                     "wgrad_bf16": 330752000 + 430036480, "wgrad_f32": 461681920 + 888530176}
 
     def __init__(self, dev):
         import torch
@@ -481,17 +481,17 @@ class DenseMXFP4:
 class DenseMXFP4M2048(DenseMXFP4):
     M = 2048
     name = "dense_mxfp4_m2048"
-    traffic_bytes = {"fwd_bf16": 133881600 + 85341952, "fwd_f32": 135824128 + 183774464,
-                     "dgrad_bf16": 217504256 + 20405248, "dgrad_f32": 234043904 + 41545472,
-                     "wgrad_bf16": 109113856 + 416793856, "wgrad_f32": 284508928 + 879964928}
+    traffic_bytes = {"fwd_bf16": 133795840 + 84969216, "fwd_f32": 134309888 + 183715328,
+                     "dgrad_bf16": 220680192 + 20125184, "dgrad_f32": 235941376 + 41113344,
+                     "wgrad_bf16": 120382976 + 416103168, "wgrad_f32": 268303616 + 879753728}
 
 
 class DenseMXFP4M4096(DenseMXFP4):
     M = 4096
     name = "dense_mxfp4_m4096"
-    traffic_bytes = {"fwd_bf16": 144382464 + 198078720, "fwd_f32": 161155840 + 418041600,
-                     "dgrad_bf16": 481953280 + 55052288, "dgrad_f32": 502846464 + 113492224,
-                     "wgrad_bf16": 137751808 + 420025856, "wgrad_f32": 294193152 + 885810944}
+    traffic_bytes = {"fwd_bf16": 143735040 + 198029824, "fwd_f32": 153152256 + 418276864,
+                     "dgrad_bf16": 484013568 + 54761216, "dgrad_f32": 504029696 + 112482560,
+                     "wgrad_bf16": 143730432 + 420033536, "wgrad_f32": 320843776 + 885835520}
 
 
 class MXFP8Train(MXFP4Train):
@@ -499,8 +499,8 @@ class MXFP8Train(MXFP4Train):
     three passes (kind::mxf8f6f4)."""
     name = "mxfp8_moe_train"
     elem = "e4m3"
-    traffic_bytes = {"fwd": 1795971840 + 518586112, "dgrad": 817723904 + 1828735488,
-                     "wgrad": 3288670976 + 1853220864}
+    traffic_bytes = {"fwd": 2330992384 + 522683648, "dgrad": 821914112 + 1831402496,
+                     "wgrad": 3288205056 + 1853214464}
 
     def __init__(self, dev):
         super().__init__(dev)
@@ -600,8 +600,8 @@ class BlockwiseFP8Pow2(BlockwiseFP8):
     passes run on the block-scaled MX GEMMs, with no promotion."""
     call_kernels = "plan + scale pack + tcgen05 GEMM"
     name = "blockwise_fp8_pow2"
-    traffic_bytes = {"fwd": 741398784 + 251155456, "dgrad": 623524352 + 436278528,
-                     "wgrad": 403493888 + 882491648}
+    traffic_bytes = {"fwd": 756197632 + 252655872, "dgrad": 628492544 + 437733376,
+                     "wgrad": 403800576 + 883552000}
 
     def __init__(self, dev):
         import torch
