@@ -183,27 +183,26 @@ __global__ void __launch_bounds__(kRowThreads) mx_rowwise_packed_kernel(
   const int64_t KBp = (KB + 3) & ~int64_t(3);
   const int64_t total = RT * 128 * KBp;
   const int64_t step = (int64_t)gridDim.x * kRowThreads;
+  // This thread's block t = prow * KBp + b, stepped by the grid stride without
+  // dividing; its row tile only grows, so its segment g is found by a forward
+  // scan (the last g with a first tile <= rt: non-empty, the next one starts
+  // after rt).
+  const int64_t t0 = (int64_t)blockIdx.x * kRowThreads + wid * 32 + lane;
+  int64_t prow = t0 / KBp, b = t0 - prow * KBp;
+  const int64_t sq = step / KBp, sr = step - sq * KBp;
+  int g = 0;
   for (int64_t base = (int64_t)blockIdx.x * kRowThreads + wid * 32; base < total; base += step) {
     const int64_t t = base + lane;
     uint32_t sbyte = 0;
-    int64_t prow = 0, b = 0;
     if (t < total) {
-      prow = t / KBp;
-      b = t - prow * KBp;
       const int rt = (int)(prow >> 7);
-      int g;
       int64_t m, row0;
       if constexpr (kSplits) {
-        int lo = 0, hi = G - 1;  // last g with s_rtp[g] <= rt: non-empty, since s_rtp[g + 1] > rt
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (s_rtp[mid] <= rt) lo = mid; else hi = mid - 1;
-        }
-        g = lo;
+        while (g + 1 < G && s_rtp[g + 1] <= rt) ++g;
         m = s_off[g + 1] - s_off[g];
         row0 = s_off[g];
       } else {
-        g = rt / tps;
+        while ((g + 1) * tps <= rt) ++g;
         m = seg_rows;
         row0 = (int64_t)g * seg_rows;
       }
@@ -251,6 +250,9 @@ __global__ void __launch_bounds__(kRowThreads) mx_rowwise_packed_kernel(
       const int64_t kc = b >> 2;
       *reinterpret_cast<uint32_t*>(sp + (kc * RT + rt) * 512 + (il & 31) * 16 + (il >> 5) * 4) = word;
     }
+    b += sr;
+    prow += sq;
+    if (b >= KBp) { b -= KBp; ++prow; }
   }
 }
 
